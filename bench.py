@@ -1,0 +1,380 @@
+"""Throughput of the fused disentangled-attention forward on GB300.
+
+One step = one df_attn_fwd call (planning kernel + fused attention kernels)
+over the long-context packed workload: 16 sequences of 8192 tokens, H = 12,
+d = 64, bf16 (DeBERTa-v3-base heads), inputs resident in HBM.  The metric is
+TFLOP/s counted as 8 n^2 d per head over valid tokens, plus tokens/s and the
+fraction of the dense bf16 tensor peak.
+
+    python bench.py [--gpus N --steps K --warmup W] [--impl reference]
+
+With N > 1 (torchrun, one rank per GPU) every rank runs its own copy of the
+workload (independent sequences, no collective on the data path): weak scaling.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+DEFAULT_WORKLOAD = "long_packed_h12d64"
+PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args(argv)
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def shard_sequences(lengths, rank: int, world: int):
+    """Every rank runs the full workload (weak scaling): its shard is a full copy."""
+    del rank, world
+    return list(lengths)
+
+
+def metric_flops(lengths, H, d):
+    return float(sum(8.0 * n * n * d * H for n in lengths))
+
+
+def algorithmic_flops(lengths, H, d, span):
+    """Dense contractions the method needs: Q.K^T and P.V (2 n^2 d each) plus the
+    two relative-position projections Q.PK^T and K.PQ^T (2 n (2 span) d each)."""
+    return float(sum(H * (4.0 * n * n * d + 8.0 * n * span * d) for n in lengths))
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return json.load(f), "measured"
+    return dict(PEAKS_FALLBACK), "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples while the timed region runs."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or not self.path or not os.path.exists(self.path):
+            return None
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                p = [c.strip() for c in line.split(",")]
+                if len(p) >= 9:
+                    rows.append(p)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows)}
+
+
+def traffic_record(kernel_file: str):
+    """DRAM bytes per launch of the dominant kernel from the committed ncu summary,
+    valid only while the kernel source is unchanged since the capture."""
+    rec = os.path.join(ROOT, "profiles", "traffic.json")
+    src = os.path.join(ROOT, "exact_attention_deberta_gb300", "csrc", kernel_file)
+    if not (os.path.exists(rec) and os.path.exists(src)):
+        return None
+    with open(rec) as f:
+        data = json.load(f)
+    with open(src, "rb") as f:
+        digest = hashlib.sha256(f.read()).hexdigest()[:16]
+    entry = data.get(kernel_file)
+    if not entry or entry.get("source_sha256_16") != digest:
+        return None
+    return entry
+
+
+def cpu_oracle_rate(x, budget_s: float = 12.0):
+    """The float64 oracle, as it stands, on a bounded sample of the same workload:
+    query rows of the first sequence / head.  Returns (TFLOP/s-equivalent, tokens/s,
+    rows, seconds, threads)."""
+    from oracle import attend_rows
+    kw = dict(buckets=x.w.buckets, max_rel=x.w.max_rel, span=x.w.span)
+    st, n = x.seq_slices()[0]
+    sl = lambda t: t[st:st + n] if x.w.layout == "packed" else t[0, :n]  # noqa: E731
+    q, k, v = sl(x.q), sl(x.k), sl(x.v)
+    rows_done, t_used, m = 0, 0.0, 32
+    while t_used < budget_s:
+        rows = np.arange(m) % n
+        t0 = time.perf_counter()
+        attend_rows(q, k, v, x.pk, x.pq, 0, rows, **kw)
+        dt = time.perf_counter() - t0
+        rows_done += m
+        t_used += dt
+        if dt < budget_s / 8:
+            m *= 2
+    flops = rows_done * 8.0 * n * x.w.d        # per row: 8 n d of the metric's 8 n^2 d
+    threads = _blas_threads()
+    return flops / t_used / 1e12, rows_done / t_used, rows_done, t_used, threads
+
+
+def _blas_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        info = threadpool_info()
+        if info:
+            return int(max(i.get("num_threads", 1) for i in info))
+    except Exception:
+        pass
+    return os.cpu_count() or 1
+
+
+def run_reference(args, rank, world):
+    """Reference arm: the float64 oracle timed on the host cores (rank 0 only)."""
+    if rank != 0:
+        return
+    from exact_attention_deberta_gb300 import synth
+    x = synth.make_inputs(args.workload)
+    from oracle import attend_rows
+    kw = dict(buckets=x.w.buckets, max_rel=x.w.max_rel, span=x.w.span)
+    st, n = x.seq_slices()[0]
+    sl = lambda t: t[st:st + n] if x.w.layout == "packed" else t[0, :n]  # noqa: E731
+    q, k, v = sl(x.q), sl(x.k), sl(x.v)
+    rows = np.arange(64)
+    for _ in range(args.warmup):
+        attend_rows(q, k, v, x.pk, x.pq, 0, rows[:8], **kw)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        attend_rows(q, k, v, x.pk, x.pq, 0, rows, **kw)
+    dt = time.perf_counter() - t0
+    flops = args.steps * rows.size * 8.0 * n * x.w.d
+    value = flops / dt / 1e12
+    cores = _blas_threads()
+    sample = f"{rows.size} query rows x 1 head of one {n}-token sequence per step"
+    line = {"impl": "reference", "metric": "disentangled-attn fwd TFLOP/s (8*L^2*d/head)",
+            "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": x.w.name, "sequences": len(x.lengths), "seq_len": int(x.w.L),
+                       "H": x.w.H, "d": x.w.d, "io_dtype": x.w.dtype, "layout": x.w.layout},
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    assert args.warmup >= 3, "at least 3 warm-up steps"
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+
+    from exact_attention_deberta_gb300.build import build
+    if rank == 0 or world == 1:
+        build()
+    if dist is not None:
+        dist.barrier()
+    from exact_attention_deberta_gb300 import binding, synth
+
+    x = synth.make_inputs(args.workload)
+    lengths = shard_sequences(x.lengths, rank, world)
+    H, d, span = x.w.H, x.w.d, x.w.span
+    kw = dict(buckets=x.w.buckets, max_rel=x.w.max_rel, span=span)
+    names = ("q", "k", "v", "pk", "pq", "key_mask", "cu_seqlens")
+    host = {n: getattr(x, n) for n in names if getattr(x, n) is not None}
+    dev = {n: t.cuda() for n, t in host.items()}
+    out = torch.empty_like(dev["q"])
+    B = len(x.lengths)
+    ws = torch.empty(binding.df_attn_workspace_size(B, H, x.w.L, d, **kw), dtype=torch.uint8,
+                     device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def step(inp, o):
+        if x.w.layout == "packed":
+            binding.df_attn_fwd(inp["q"], inp["k"], inp["v"], inp["pk"], inp["pq"],
+                                cu_seqlens=inp["cu_seqlens"], max_seqlen=x.w.L, out=o,
+                                workspace=ws, **kw)
+        else:
+            binding.df_attn_fwd(inp["q"], inp["k"], inp["v"], inp["pk"], inp["pq"],
+                                key_mask=inp["key_mask"], out=o, workspace=ws, **kw)
+
+    for _ in range(args.warmup):
+        step(dev, out)
+    torch.cuda.synchronize()
+    assert binding.df_attn_get_device_status(ws) == binding.DF_OK
+    launches_per_step = binding.df_attn_last_launch_count()
+
+    kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        t0.record(stream)
+        for i in range(args.steps):
+            binding.df_attn_set_profile_events(*kev[i])
+            step(dev, out)
+        t1.record(stream)
+        torch.cuda.synchronize()
+    binding.df_attn_set_profile_events(None, None)
+    if dist is not None:
+        dist.barrier()
+    ms = t0.elapsed_time(t1) / args.steps
+    kern_ms = sum(a.elapsed_time(b) for a, b in kev) / args.steps
+    assert binding.df_attn_get_device_status(ws) == binding.DF_OK
+
+    e2e = None
+    if not args.no_e2e:
+        pinned = {n: t.pin_memory() for n, t in host.items()}
+        dev2 = {n: torch.empty_like(t) for n, t in dev.items()}
+        out_h = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+        h2d = sum(t.numel() * t.element_size() for t in pinned.values())
+        d2h = out_h.numel() * out_h.element_size()
+        for _ in range(2):
+            for n in pinned:
+                dev2[n].copy_(pinned[n], non_blocking=True)
+            step(dev2, out)
+            out_h.copy_(out, non_blocking=True)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            for n in pinned:
+                dev2[n].copy_(pinned[n], non_blocking=True)
+            step(dev2, out)
+            out_h.copy_(out, non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = e0.elapsed_time(e1) / args.steps
+        e2e = (e2e_ms, h2d, d2h)
+
+    # max over ranks
+    times = torch.tensor([ms, kern_ms, e2e[0] if e2e else 0.0], dtype=torch.float64, device="cuda")
+    if dist is not None:
+        dist.all_reduce(times, op=dist.ReduceOp.MAX)
+    ms, kern_ms, e2e_ms = (float(t) for t in times.cpu())
+
+    flops_rank = metric_flops(lengths, H, d)
+    tokens_rank = float(sum(lengths))
+    value = world * flops_rank / (ms * 1e-3) / 1e12
+    peaks, peak_src = load_peaks()
+    tc = x.w.dtype in ("bf16", "fp16") and launches_per_step >= 3
+    algo = algorithmic_flops(lengths, H, d, span)
+    if tc:
+        bound, peak, unit = "tensor", float(peaks["bf16_tflops_sustained"]), "TFLOP/s"
+        if x.w.dtype == "fp16":
+            peak = float(peaks["bf16_tflops_sustained"])  # same dense rate as bf16
+        kernel_file = "df_tc.cu"
+    else:
+        # FP32 FFMA: 152 SMs x 128 lanes x 2 flop x 2.07 GHz
+        bound, peak, unit = "alu", 152 * 128 * 2 * 2.07e9 / 1e12, "TFLOP/s"
+        kernel_file = "df_simt.cu"
+    achieved = algo / (kern_ms * 1e-3) / 1e12
+    tr = traffic_record(kernel_file)
+    line = {
+        "metric": "disentangled-attn fwd TFLOP/s (8*L^2*d/head)",
+        "value": value,
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": x.w.dtype if tc else "f32",
+        "data": "synthetic",
+        "config": {"workload": x.w.name, "sequences": len(lengths), "seq_len": int(x.w.L),
+                   "H": H, "d": d, "io_dtype": x.w.dtype, "layout": x.w.layout,
+                   "buckets": x.w.buckets, "max_rel": x.w.max_rel, "span": span,
+                   "l2": "inputs larger than L2 (q,k,v,out %.0f MB)" % (
+                       4 * out.numel() * out.element_size() / 1e6)},
+        "tokens_per_s": world * tokens_rank / (ms * 1e-3),
+        "pct_bf16_peak_metric": value / world / float(peaks["bf16_tflops_sustained"]) * 100.0,
+        "gpu_launches": launches_per_step * args.steps,
+        "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
+                     "frac": achieved / peak, "traffic": tr.get("dram_bytes_per_launch") if tr else None,
+                     "kernel_ms": kern_ms, "peak_source": peak_src if bound == "tensor" else
+                     "derived: 152 SM x 128 FP32 lanes x 2 x 2.07 GHz"},
+    }
+    if e2e:
+        line["e2e"] = {"value": world * flops_rank / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+                       "h2d_bytes_per_step": e2e[1], "d2h_bytes_per_step": e2e[2]}
+    clocks = clk.summary()
+    line["clocks"] = clocks
+    if rank == 0 and not args.no_cpu_baseline:
+        tf, rows_s, rows, secs, thr = cpu_oracle_rate(x)
+        line["cpu_baseline"] = {"value": tf, "unit": "TFLOP/s", "cores": thr, "kind": "oracle",
+                                "sample": f"{rows} query rows of head 0 of one {int(lengths[0])}-token "
+                                          f"sequence, float64 numpy, {secs:.1f} s"}
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

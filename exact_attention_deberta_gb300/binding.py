@@ -1,0 +1,204 @@
+"""Thin ctypes binding of ``include/df_attn.h``: argument marshalling only.
+
+Every step of the attention runs inside ``libdfattn.so``; this module only
+turns torch tensors into pointers and sizes, allocates ``out`` / the workspace
+with torch when the caller does not pass them, and raises on a non-OK status.
+There is no fallback: if the library is missing, importing this module fails.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libdfattn.so")
+
+DF_OK, DF_ERR_INVALID_ARG, DF_ERR_UNSUPPORTED, DF_ERR_ALIGNMENT = 0, 1, 2, 3
+DF_ERR_WORKSPACE, DF_ERR_CUDA, DF_ERR_DEVICE_TIMEOUT = 4, 5, 6
+DF_BF16, DF_FP16, DF_FP32 = 0, 1, 2
+_DTYPE = {torch.bfloat16: DF_BF16, torch.float16: DF_FP16, torch.float32: DF_FP32}
+
+
+class DFError(RuntimeError):
+    def __init__(self, status: int, what: str = ""):
+        self.status = int(status)
+        super().__init__(f"{what}: {status_string(status)} (status {status})")
+
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(f"{LIB_PATH} is not built; run exact_attention_deberta_gb300.build.build() "
+                      "(or __graft_entry__.build())")
+
+_lib = ctypes.CDLL(LIB_PATH)
+_vp, _i, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+
+
+class _Layout(ctypes.Structure):
+    _fields_ = [("header", _sz), ("idx_table", _sz), ("items", _sz), ("scalars", _sz),
+                ("keybias", _sz), ("partial", _sz), ("total", _sz), ("max_items", _i),
+                ("t_pad", _i), ("table_half", _i)]
+
+
+_lib.df_attn_fwd.argtypes = [_vp] * 7 + [_i] * 9 + [_vp, _vp, _sz, _vp]
+_lib.df_attn_fwd.restype = _i
+_lib.df_attn_plan.argtypes = [_vp] * 6 + [_i] * 9 + [_vp, _vp, _sz, _vp]
+_lib.df_attn_plan.restype = _i
+_lib.df_attn_workspace_size.argtypes = [_i] * 7
+_lib.df_attn_workspace_size.restype = _sz
+_lib.df_attn_supported.argtypes = [_i] * 7
+_lib.df_attn_supported.restype = _i
+_lib.df_attn_status_string.argtypes = [_i]
+_lib.df_attn_status_string.restype = ctypes.c_char_p
+_lib.df_attn_get_device_status.argtypes = [_vp, _vp]
+_lib.df_attn_get_device_status.restype = _i
+_lib.df_rel_index_table.argtypes = [_i, _i, _i, _i, _vp, _vp]
+_lib.df_rel_index_table.restype = _i
+_lib.df_attn_workspace_layout.argtypes = [_i] * 7 + [ctypes.POINTER(_Layout)]
+_lib.df_attn_workspace_layout.restype = _i
+_lib.df_attn_set_profile_events.argtypes = [_vp, _vp]
+_lib.df_attn_set_profile_events.restype = None
+_lib.df_attn_set_wait_budget.argtypes = [ctypes.c_ulonglong]
+_lib.df_attn_set_wait_budget.restype = None
+_lib.df_attn_last_launch_count.argtypes = []
+_lib.df_attn_last_launch_count.restype = _i
+
+
+def status_string(status: int) -> str:
+    return _lib.df_attn_status_string(int(status)).decode()
+
+
+def _check(status: int, what: str):
+    if status != DF_OK:
+        raise DFError(status, what)
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def default_span(buckets: int, max_rel: int) -> int:
+    """DeBERTa's attention span: position_buckets if bucketing is on, else max_rel."""
+    return buckets if buckets > 0 else max_rel
+
+
+def df_attn_workspace_size(B, H, L, d, buckets=256, max_rel=512, span=None) -> int:
+    span = default_span(buckets, max_rel) if span is None else span
+    return int(_lib.df_attn_workspace_size(B, H, L, d, buckets, max_rel, span))
+
+
+def df_attn_supported(H, L, d, dtype, buckets=256, max_rel=512, span=None) -> int:
+    span = default_span(buckets, max_rel) if span is None else span
+    dt = _DTYPE[dtype] if isinstance(dtype, torch.dtype) else int(dtype)
+    return int(_lib.df_attn_supported(H, L, d, dt, buckets, max_rel, span))
+
+
+def df_attn_workspace_layout(B, H, L, d, buckets=256, max_rel=512, span=None) -> dict:
+    span = default_span(buckets, max_rel) if span is None else span
+    lay = _Layout()
+    _check(_lib.df_attn_workspace_layout(B, H, L, d, buckets, max_rel, span, ctypes.byref(lay)),
+           "df_attn_workspace_layout")
+    return {name: getattr(lay, name) for name, _ in _Layout._fields_}
+
+
+def _shape_args(q, key_mask, cu_seqlens, max_seqlen):
+    if (key_mask is None) == (cu_seqlens is None):
+        raise ValueError("pass exactly one of key_mask (padded) and cu_seqlens (packed)")
+    if key_mask is not None:
+        B, L, H, d = q.shape
+        return B, H, L, B * L, d
+    T, H, d = q.shape
+    B = cu_seqlens.numel() - 1
+    if max_seqlen is None:
+        raise ValueError("packed mode needs max_seqlen (an upper bound of every length)")
+    return B, H, int(max_seqlen), T, d
+
+
+def _prepare(q, k, v, pos_key, pos_query, key_mask, cu_seqlens, max_seqlen, buckets, max_rel,
+             span, out, workspace):
+    B, H, L, T, d = _shape_args(q, key_mask, cu_seqlens, max_seqlen)
+    span = default_span(buckets, max_rel) if span is None else span
+    for name, t in (("q", q), ("k", k), ("v", v), ("pos_key", pos_key), ("pos_query", pos_query)):
+        if t is None:
+            continue
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA tensor")
+        if t.dtype != q.dtype:
+            raise ValueError(f"{name} dtype {t.dtype} != q dtype {q.dtype}")
+    if q.dtype not in _DTYPE:
+        raise ValueError(f"unsupported dtype {q.dtype}")
+    if key_mask is not None and (key_mask.dtype != torch.uint8 or not key_mask.is_contiguous()):
+        raise ValueError("key_mask must be a contiguous uint8 tensor")
+    if cu_seqlens is not None and (cu_seqlens.dtype != torch.int32 or not cu_seqlens.is_contiguous()):
+        raise ValueError("cu_seqlens must be a contiguous int32 tensor")
+    if out is None:
+        out = torch.empty_like(q)
+    if workspace is None:
+        size = df_attn_workspace_size(B, H, L, d, buckets, max_rel, span)
+        workspace = torch.empty(max(size, 256), dtype=torch.uint8, device=q.device)
+    return B, H, L, T, d, span, out, workspace
+
+
+def df_attn_fwd(q, k, v, pos_key, pos_query, key_mask=None, cu_seqlens=None, *, max_seqlen=None,
+                buckets=256, max_rel=512, span=None, out=None, workspace=None, stream=None):
+    """Fused disentangled-attention forward; returns ``out`` (same layout as q)."""
+    B, H, L, T, d, span, out, workspace = _prepare(q, k, v, pos_key, pos_query, key_mask,
+                                                   cu_seqlens, max_seqlen, buckets, max_rel,
+                                                   span, out, workspace)
+    st = _lib.df_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(pos_key), _ptr(pos_query),
+                          _ptr(key_mask), _ptr(cu_seqlens), B, H, L, T, d, buckets, max_rel,
+                          span, _DTYPE[q.dtype], _ptr(out), _ptr(workspace),
+                          workspace.numel(), _stream(stream))
+    _check(st, "df_attn_fwd")
+    return out
+
+
+def df_attn_plan(q, k, pos_key, pos_query, key_mask=None, cu_seqlens=None, *, max_seqlen=None,
+                 buckets=256, max_rel=512, span=None, out=None, workspace=None, stream=None):
+    """Planning step alone; returns (out, workspace)."""
+    B, H, L, T, d, span, out, workspace = _prepare(q, k, None, pos_key, pos_query, key_mask,
+                                                   cu_seqlens, max_seqlen, buckets, max_rel,
+                                                   span, out, workspace)
+    st = _lib.df_attn_plan(_ptr(q), _ptr(k), _ptr(pos_key), _ptr(pos_query), _ptr(key_mask),
+                           _ptr(cu_seqlens), B, H, L, T, d, buckets, max_rel, span,
+                           _DTYPE[q.dtype], _ptr(out), _ptr(workspace), workspace.numel(),
+                           _stream(stream))
+    _check(st, "df_attn_plan")
+    return out, workspace
+
+
+def df_attn_get_device_status(workspace, stream=None) -> int:
+    return int(_lib.df_attn_get_device_status(_ptr(workspace), _stream(stream)))
+
+
+def df_rel_index_table(buckets, max_rel, span, max_len, out=None, stream=None, device="cuda"):
+    if out is None:
+        out = torch.empty(2 * max_len - 1, dtype=torch.int32, device=device)
+    _check(_lib.df_rel_index_table(buckets, max_rel, span, max_len, _ptr(out), _stream(stream)),
+           "df_rel_index_table")
+    return out
+
+
+def df_attn_set_profile_events(start=None, stop=None):
+    h = lambda e: None if e is None else ctypes.c_void_p(e.cuda_event)  # noqa: E731
+    _lib.df_attn_set_profile_events(h(start), h(stop))
+
+
+def df_attn_set_wait_budget(cycles: int):
+    _lib.df_attn_set_wait_budget(int(cycles))
+
+
+def df_attn_last_launch_count() -> int:
+    return int(_lib.df_attn_last_launch_count())
+
+
+raw_library = _lib

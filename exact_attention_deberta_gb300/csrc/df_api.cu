@@ -1,0 +1,238 @@
+// Host side of the C ABI declared in include/df_attn.h: argument checks,
+// workspace layout, planning launch and dispatch to the fused kernels.
+//
+// Error policy follows the strict-contract convention of the pages' prior art
+// (FastFlashAttention README, "API": an unsupported configuration is an error,
+// never a hidden slow path): every check runs before the first launch and a
+// failing one returns a status with nothing enqueued.
+#include "df_common.cuh"
+
+#include <math.h>
+#include <string.h>
+
+#include <atomic>
+
+namespace dfa {
+cudaError_t launch_tc(const Problem& p, cudaStream_t s, cudaEvent_t ev0, cudaEvent_t ev1,
+                      int* launches);
+bool tc_enabled();
+}  // namespace dfa
+
+namespace {
+
+using namespace dfa;
+
+std::atomic<unsigned long long> g_wait_budget{0};
+cudaEvent_t g_prof_start = nullptr;
+cudaEvent_t g_prof_stop = nullptr;
+std::atomic<int> g_last_launches{0};
+
+constexpr unsigned long long kDefaultWaitBudget = 1ull << 31;
+
+size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+struct Layout {
+  size_t header, idx, items, seqs, scal, keybias, partial, total;
+  int max_items, t_pad, lt;
+};
+
+Layout make_layout(int B, int H, int L, int d) {
+  Layout l{};
+  l.lt = ((L + 127) / 128) * 128 + 128;
+  const size_t T = (size_t)B * L;
+  l.t_pad = (int)(((T + 128 + 127) / 128) * 128);
+  l.max_items = B * H * ((L + kQBlock - 1) / kQBlock);
+  size_t off = 0;
+  l.header = off;
+  off = align256(off + sizeof(df_ws_header));
+  l.idx = off;
+  off = align256(off + (size_t)(2 * l.lt - 1) * sizeof(int32_t));
+  l.items = off;
+  off = align256(off + (size_t)l.max_items * sizeof(int4));
+  l.seqs = off;
+  off = align256(off + (size_t)B * sizeof(int4));
+  l.scal = off;
+  off = align256(off + (size_t)H * 4 * l.t_pad * sizeof(float));
+  l.keybias = off;
+  off = align256(off + (size_t)l.t_pad * sizeof(float));
+  l.partial = off;
+  off = align256(off + T * H * (size_t)(d + 2) * sizeof(float));
+  l.total = off;
+  return l;
+}
+
+df_status check_params(int H, int L, int d, df_dtype dtype, int buckets, int max_rel, int span) {
+  if (H < 1 || L < 1 || span < 1) return DF_ERR_INVALID_ARG;
+  if (dtype != DF_BF16 && dtype != DF_FP16 && dtype != DF_FP32) return DF_ERR_INVALID_ARG;
+  if (buckets > 0 && (buckets / 2 < 1 || buckets / 2 >= max_rel - 1)) return DF_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return DF_ERR_UNSUPPORTED;
+  if (L > 65536 || span > 65536 || H > 1024) return DF_ERR_UNSUPPORTED;
+  return DF_OK;
+}
+
+bool aligned16(const void* p) { return ((uintptr_t)p & 15) == 0; }
+
+df_status build_problem(const void* q, const void* k, const void* v, const void* pk,
+                        const void* pq, const uint8_t* key_mask, const int32_t* cu_seqlens,
+                        int B, int H, int L, int T, int d, int buckets, int max_rel, int span,
+                        df_dtype dtype, void* out, void* ws, size_t ws_bytes, bool need_v,
+                        Problem* p) {
+  df_status st = check_params(H, L, d, dtype, buckets, max_rel, span);
+  if (st != DF_OK) return st;
+  if (B < 0 || T < 0) return DF_ERR_INVALID_ARG;
+  const bool packed = cu_seqlens != nullptr;
+  if ((key_mask == nullptr) == (cu_seqlens == nullptr)) return DF_ERR_INVALID_ARG;
+  if ((long long)B * L > (1ll << 26)) return DF_ERR_UNSUPPORTED;
+  if (!packed && (long long)T != (long long)B * L) return DF_ERR_INVALID_ARG;
+  if (packed && (long long)T > (long long)B * L) return DF_ERR_INVALID_ARG;
+  // With no tokens at all the tensors may be empty (NULL data pointers).
+  if (T > 0 && (!q || !k || !out || (need_v && !v))) return DF_ERR_INVALID_ARG;
+  if (!pk || !pq) return DF_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(pk) || !aligned16(pq) || !aligned16(out) ||
+      (need_v && !aligned16(v)))
+    return DF_ERR_ALIGNMENT;
+  const Layout lay = make_layout(B, H, L, d);
+  if (!ws || ws_bytes < lay.total) return DF_ERR_WORKSPACE;
+  if (((uintptr_t)ws & 255) != 0) return DF_ERR_ALIGNMENT;
+  char* base = static_cast<char*>(ws);
+  Problem& P = *p;
+  memset(&P, 0, sizeof(P));
+  P.q = q; P.k = k; P.v = v; P.pk = pk; P.pq = pq;
+  P.key_mask = key_mask; P.cu_seqlens = cu_seqlens; P.out = out;
+  P.B = B; P.H = H; P.L = L; P.T = T; P.d = d;
+  P.buckets = buckets; P.max_rel = max_rel; P.span = span;
+  P.dtype = (int)dtype; P.packed = packed ? 1 : 0;
+  P.kscale = (float)(1.4426950408889634 / sqrt(3.0 * d));
+  P.hdr = reinterpret_cast<df_ws_header*>(base + lay.header);
+  P.idx = reinterpret_cast<int32_t*>(base + lay.idx);
+  P.items = reinterpret_cast<int4*>(base + lay.items);
+  P.seqs = reinterpret_cast<int4*>(base + lay.seqs);
+  P.scal = reinterpret_cast<float*>(base + lay.scal);
+  P.keybias = reinterpret_cast<float*>(base + lay.keybias);
+  P.partial = reinterpret_cast<float*>(base + lay.partial);
+  P.max_items = lay.max_items;
+  P.t_pad = lay.t_pad;
+  P.lt = lay.lt;
+  const unsigned long long wb = g_wait_budget.load();
+  P.wait_budget = wb ? wb : kDefaultWaitBudget;
+  return DF_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* df_attn_status_string(df_status s) {
+  switch (s) {
+    case DF_OK: return "ok";
+    case DF_ERR_INVALID_ARG: return "invalid argument";
+    case DF_ERR_UNSUPPORTED: return "unsupported configuration";
+    case DF_ERR_ALIGNMENT: return "pointer not 16-byte aligned (workspace: 256-byte)";
+    case DF_ERR_WORKSPACE: return "workspace missing or too small";
+    case DF_ERR_CUDA: return "CUDA runtime error";
+    case DF_ERR_DEVICE_TIMEOUT: return "device-side bounded wait ran out";
+  }
+  return "unknown status";
+}
+
+df_status df_attn_supported(int H, int L, int d, df_dtype dtype, int buckets, int max_rel,
+                            int span) {
+  return check_params(H, L, d, dtype, buckets, max_rel, span);
+}
+
+size_t df_attn_workspace_size(int B, int H, int L, int d, int buckets, int max_rel, int span) {
+  if (B < 0 || check_params(H, L, d, DF_BF16, buckets, max_rel, span) != DF_OK) return 0;
+  return make_layout(B, H, L, d).total;
+}
+
+df_status df_attn_workspace_layout(int B, int H, int L, int d, int buckets, int max_rel, int span,
+                                   df_ws_layout* layout) {
+  if (!layout || B < 0) return DF_ERR_INVALID_ARG;
+  const df_status st = check_params(H, L, d, DF_BF16, buckets, max_rel, span);
+  if (st != DF_OK) return st;
+  const Layout l = make_layout(B, H, L, d);
+  layout->header = l.header;
+  layout->idx_table = l.idx;
+  layout->items = l.items;
+  layout->scalars = l.scal;
+  layout->keybias = l.keybias;
+  layout->partial = l.partial;
+  layout->total = l.total;
+  layout->max_items = l.max_items;
+  layout->t_pad = l.t_pad;
+  layout->table_half = l.lt;
+  return DF_OK;
+}
+
+df_status df_attn_plan(const void* q, const void* k, const void* pos_key, const void* pos_query,
+                       const uint8_t* key_mask, const int32_t* cu_seqlens, int B, int H, int L,
+                       int total_tokens, int d, int buckets, int max_rel, int span,
+                       df_dtype dtype, void* out, void* workspace, size_t workspace_bytes,
+                       df_stream_t stream) {
+  Problem p;
+  df_status st = build_problem(q, k, nullptr, pos_key, pos_query, key_mask, cu_seqlens, B, H, L,
+                               total_tokens, d, buckets, max_rel, span, dtype, out, workspace,
+                               workspace_bytes, false, &p);
+  if (st != DF_OK) return st;
+  return launch_plan(p, (cudaStream_t)stream) == cudaSuccess ? DF_OK : DF_ERR_CUDA;
+}
+
+df_status df_attn_fwd(const void* q, const void* k, const void* v, const void* pos_key,
+                      const void* pos_query, const uint8_t* key_mask, const int32_t* cu_seqlens,
+                      int B, int H, int L, int total_tokens, int d, int buckets, int max_rel,
+                      int span, df_dtype dtype, void* out, void* workspace,
+                      size_t workspace_bytes, df_stream_t stream) {
+  Problem p;
+  df_status st = build_problem(q, k, v, pos_key, pos_query, key_mask, cu_seqlens, B, H, L,
+                               total_tokens, d, buckets, max_rel, span, dtype, out, workspace,
+                               workspace_bytes, true, &p);
+  if (st != DF_OK) return st;
+  cudaStream_t s = (cudaStream_t)stream;
+  if (launch_plan(p, s) != cudaSuccess) return DF_ERR_CUDA;
+  int launches = 0;
+  cudaError_t e;
+  if (dtype != DF_FP32 && tc_enabled()) {
+    e = launch_tc(p, s, g_prof_start, g_prof_stop, &launches);
+  } else {
+    if (g_prof_start) cudaEventRecord(g_prof_start, s);
+    e = launch_simt(p, s, &launches);
+    if (g_prof_stop) cudaEventRecord(g_prof_stop, s);
+  }
+  if (e != cudaSuccess) return DF_ERR_CUDA;
+  g_last_launches.store(1 + launches);
+  return DF_OK;
+}
+
+df_status df_attn_get_device_status(void* workspace, df_stream_t stream) {
+  if (!workspace) return DF_ERR_INVALID_ARG;
+  if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return DF_ERR_CUDA;
+  df_ws_header h;
+  if (cudaMemcpy(&h, workspace, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return DF_ERR_CUDA;
+  const int32_t zero[2] = {0, 0};
+  if (cudaMemcpy(workspace, zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess)
+    return DF_ERR_CUDA;
+  return (df_status)h.status;
+}
+
+df_status df_rel_index_table(int buckets, int max_rel, int span, int max_len, int32_t* idx,
+                             df_stream_t stream) {
+  if (!idx || max_len < 1 || max_len > 65536 || span < 1) return DF_ERR_INVALID_ARG;
+  if (buckets > 0 && (buckets / 2 < 1 || buckets / 2 >= max_rel - 1)) return DF_ERR_INVALID_ARG;
+  if (((uintptr_t)idx & 3) != 0) return DF_ERR_ALIGNMENT;
+  return launch_index_table(buckets, max_rel, span, max_len, idx, (cudaStream_t)stream) ==
+                 cudaSuccess
+             ? DF_OK
+             : DF_ERR_CUDA;
+}
+
+void df_attn_set_profile_events(df_event_t start, df_event_t stop) {
+  g_prof_start = (cudaEvent_t)start;
+  g_prof_stop = (cudaEvent_t)stop;
+}
+
+void df_attn_set_wait_budget(unsigned long long cycles) { g_wait_budget.store(cycles); }
+
+int df_attn_last_launch_count(void) { return g_last_launches.load(); }
+
+}  // extern "C"

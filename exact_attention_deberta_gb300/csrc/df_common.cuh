@@ -1,0 +1,102 @@
+// Shared definitions of the disentangled-attention CUDA library (sm_103a).
+//
+// The operation follows the DisentangledFlash 0.2.0 README ("Status": C2P/P2C
+// disentangled attention, factorized 2-D padding masks, packed cu_seqlens
+// inference) and the kernels-community "DisentangledFlash" discussion
+// ("Motivation": content-to-position and position-to-content terms added to
+// the content-to-content score, exact evaluation without the [B,H,L,L] matrix).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+#include "df_attn.h"
+
+namespace dfa {
+
+// Query rows per work item (one tcgen05 M=128 tile).
+constexpr int kQBlock = 128;
+// Keys per far tile of the tensor-core path.
+constexpr int kKBlock = 128;
+
+// Workspace views and call parameters handed to every kernel.
+struct Problem {
+  const void* q;
+  const void* k;
+  const void* v;
+  const void* pk;
+  const void* pq;
+  const uint8_t* key_mask;    // padded mode
+  const int32_t* cu_seqlens;  // packed mode
+  void* out;
+  int B, H, L, T, d;
+  int buckets, max_rel, span;
+  int dtype;                  // df_dtype
+  int packed;
+  float kscale;               // log2(e) / sqrt(3 d): logits are kept in log2 units
+  // workspace sections
+  df_ws_header* hdr;
+  int32_t* idx;               // [2 lt - 1]
+  int4* items;                // [max_items]
+  int4* seqs;                 // [B] planner scratch {start, n, nblk, order}
+  float* scal;                // [H][4][t_pad]
+  float* keybias;             // [t_pad]
+  float* partial;             // [T][H][d + 2]
+  int max_items;
+  int t_pad;
+  int lt;                     // index-table half width: idx of r at r + lt - 1, |r| < lt
+  unsigned long long wait_budget;
+};
+
+// DeBERTa log-bucketed relative position.  The identity inside |r| <= mid;
+// logarithmic growth that reaches 2 mid - 1 at |r| = max_rel - 1 outside it.
+// Evaluated in double precision (CUDA's log) so that no bucket edge moves.
+__device__ __forceinline__ int rel_bucket(int r, int buckets, int max_rel) {
+  if (buckets <= 0) return r;
+  const int mid = buckets / 2;
+  const int a = r < 0 ? -r : r;
+  if (a <= mid) return r;
+  const double f = log((double)a / (double)mid) / log((double)(max_rel - 1) / (double)mid);
+  const int g = (int)ceil(f * (double)(mid - 1)) + mid;
+  return r < 0 ? -g : g;
+}
+
+__device__ __forceinline__ int rel_index(int r, int buckets, int max_rel, int span) {
+  int u = rel_bucket(r, buckets, max_rel) + span;
+  u = u < 0 ? 0 : u;
+  return u > 2 * span - 1 ? 2 * span - 1 : u;
+}
+
+template <typename T> struct IO;
+template <> struct IO<float> {
+  static __device__ __forceinline__ float load(const float* p) { return *p; }
+  static __device__ __forceinline__ float to_f(float x) { return x; }
+  static __device__ __forceinline__ float from_f(float x) { return x; }
+};
+template <> struct IO<__nv_bfloat16> {
+  static __device__ __forceinline__ float load(const __nv_bfloat16* p) { return __bfloat162float(*p); }
+  static __device__ __forceinline__ float to_f(__nv_bfloat16 x) { return __bfloat162float(x); }
+  static __device__ __forceinline__ __nv_bfloat16 from_f(float x) { return __float2bfloat16_rn(x); }
+};
+template <> struct IO<__half> {
+  static __device__ __forceinline__ float load(const __half* p) { return __half2float(*p); }
+  static __device__ __forceinline__ float to_f(__half x) { return __half2float(x); }
+  static __device__ __forceinline__ __half from_f(float x) { return __float2half_rn(x); }
+};
+
+// First device-side error wins; later ones are dropped.
+__device__ __forceinline__ void raise_device_error(df_ws_header* hdr, int code, int where) {
+  if (atomicCAS(&hdr->status, 0, code) == 0) hdr->status_where = where;
+}
+
+}  // namespace dfa
+
+// Host-side launchers (defined in the .cu files).
+namespace dfa {
+cudaError_t launch_plan(const Problem& p, cudaStream_t s);
+cudaError_t launch_index_table(int buckets, int max_rel, int span, int max_len, int32_t* idx,
+                               cudaStream_t s);
+cudaError_t launch_simt(const Problem& p, cudaStream_t s, int* launches);
+}  // namespace dfa

@@ -1,0 +1,193 @@
+/*
+ * df_attn.h -- C ABI of the exact DeBERTa-v2/v3 disentangled-attention forward
+ * pass for NVIDIA GB300 (sm_103a).
+ *
+ * The operation (DisentangledFlash 0.2.0 README, section "Status":
+ * "DeBERTa-v2/v3-style C2P/P2C disentangled attention", "factorized 2-D padding
+ * masks", "packed, unpadded inference with cu_seqlens"; kernels-community
+ * discussion "DisentangledFlash", section "Motivation": content-to-position and
+ * position-to-content terms, evaluated exactly without materialising the
+ * [B, H, L, L] matrix):
+ *
+ *   score(i,j) = ( Q_i.K_j + Q_i.PK[idx(i-j)] + K_j.PQ[idx(i-j)] ) / sqrt(3 d)
+ *   idx(r)     = clamp(bucket(r) + span, 0, 2 span - 1)
+ *   bucket(r)  = r                                   for |r| <= buckets/2,
+ *              = sign(r) (mid + ceil(ln(|r|/mid) / ln((max_rel-1)/mid) (mid-1)))
+ *                                                    otherwise (mid = buckets/2);
+ *              = r for every r when buckets <= 0.
+ *   O_i        = sum_j softmax_j(score(i, .)) V_j  over valid keys j;
+ *   O_i        = 0 for a query row whose own mask bit is 0.
+ *
+ * Conventions shared by every entry point:
+ *   - All tensor pointers are DEVICE pointers owned by the caller.  The library
+ *     allocates nothing, never synchronises (except df_attn_get_device_status)
+ *     and enqueues all work on `stream` (NULL = legacy default stream).
+ *   - Layouts are dense row-major.  Padded mode: q, k, v, out are [B, L, H, d]
+ *     and key_mask is uint8 [B, L] (nonzero = valid; applied to keys and, as
+ *     the factorized mask, to query rows).  Packed mode: q, k, v, out are
+ *     [T, H, d] with int32 cu_seqlens [B + 1] (cu_seqlens[0] = 0,
+ *     cu_seqlens[B] = T, non-decreasing, every length <= L).  pos_key (PK) and
+ *     pos_query (PQ) are [2 span, H, d].  All of q, k, v, pos_key, pos_query,
+ *     out share `dtype`.
+ *   - Positions restart at 0 in every sequence (padded: index inside the batch
+ *     row; packed: offset from cu_seqlens[s]).
+ *   - Pointers must be 16-byte aligned (tensor-memory-access copies).
+ *   - Argument checks run on the host before any launch; a failing check
+ *     returns a status and enqueues nothing.  There is no fallback path.
+ */
+#ifndef DF_ATTN_H
+#define DF_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object as cudaStream_t / cudaEvent_t; declared here so that this header
+ * needs no CUDA include. */
+typedef struct CUstream_st* df_stream_t;
+typedef struct CUevent_st* df_event_t;
+
+typedef enum {
+  DF_OK = 0,
+  DF_ERR_INVALID_ARG = 1,     /* a pointer, size or parameter is out of contract */
+  DF_ERR_UNSUPPORTED = 2,     /* valid request this build does not implement (e.g. d = 48) */
+  DF_ERR_ALIGNMENT = 3,       /* a pointer is not 16-byte aligned */
+  DF_ERR_WORKSPACE = 4,       /* workspace NULL or smaller than df_attn_workspace_size() */
+  DF_ERR_CUDA = 5,            /* a CUDA runtime call failed (launch, tensor-map encode) */
+  DF_ERR_DEVICE_TIMEOUT = 6   /* a kernel's bounded wait ran out (read back by
+                                 df_attn_get_device_status) */
+} df_status;
+
+typedef enum { DF_BF16 = 0, DF_FP16 = 1, DF_FP32 = 2 } df_dtype;
+
+/*
+ * Fused forward pass.
+ *
+ *   q, k, v            [B, L, H, d] (padded) or [T, H, d] (packed), `dtype`
+ *   pos_key, pos_query [2 span, H, d], `dtype` (the projected relative embeddings)
+ *   key_mask           uint8 [B, L] in padded mode, NULL in packed mode
+ *   cu_seqlens         int32 [B + 1] in packed mode, NULL in padded mode
+ *   B                  batch rows (padded) or number of sequences (packed), >= 0
+ *   H, d               heads and head size; d in {64, 128}
+ *   L                  padded length, or an upper bound of every packed length
+ *                      (max_seqlen); 1 <= L <= 65536
+ *   total_tokens       rows of q/k/v/out: B*L in padded mode, cu_seqlens[B] in
+ *                      packed mode (the host cannot read cu_seqlens)
+ *   buckets, max_rel   DeBERTa position_buckets and max_relative_positions; with
+ *                      buckets > 0 it must hold 2 <= buckets/2 < max_rel - 1
+ *   span               attention span: PK/PQ have 2*span rows; span >= 1
+ *   dtype              DF_BF16 / DF_FP16 (tensor-core path) or DF_FP32 (strict
+ *                      fp32: FFMA on CUDA cores, no TF32)
+ *   out                same layout and dtype as q; every row is written (padded
+ *                      query rows and rows of empty sequences get zeros)
+ *   workspace          device scratch of at least df_attn_workspace_size() bytes,
+ *                      256-byte aligned; its contents need not be initialised
+ *                      and are overwritten by every call (calls that share a
+ *                      workspace must not overlap in time)
+ *   stream             CUDA stream for every launch
+ *
+ * Returns DF_OK once the work is enqueued; errors raised on the device are
+ * reported by df_attn_get_device_status().
+ */
+df_status df_attn_fwd(const void* q, const void* k, const void* v,
+                      const void* pos_key, const void* pos_query,
+                      const uint8_t* key_mask, const int32_t* cu_seqlens,
+                      int B, int H, int L, int total_tokens, int d,
+                      int buckets, int max_rel, int span, df_dtype dtype,
+                      void* out, void* workspace, size_t workspace_bytes,
+                      df_stream_t stream);
+
+/* Bytes of workspace df_attn_fwd / df_attn_plan need for these sizes (an upper
+ * bound over both layouts and every dtype; T is bounded by B*L).  Returns 0 for
+ * arguments df_attn_supported() rejects. */
+size_t df_attn_workspace_size(int B, int H, int L, int d, int buckets, int max_rel, int span);
+
+/* DF_OK if (H, L, d, dtype, buckets, max_rel, span) is implemented; otherwise
+ * DF_ERR_INVALID_ARG or DF_ERR_UNSUPPORTED.  Host only, no CUDA call. */
+df_status df_attn_supported(int H, int L, int d, df_dtype dtype, int buckets, int max_rel,
+                            int span);
+
+/* Static, NUL-terminated description of a status code. */
+const char* df_attn_status_string(df_status s);
+
+/* Synchronises `stream`, reads the device status word in `workspace` (written by
+ * the kernels of earlier calls on that workspace), clears it and returns it:
+ * DF_OK, or DF_ERR_DEVICE_TIMEOUT when a bounded wait ran out.  DF_ERR_CUDA if
+ * the copy itself fails. */
+df_status df_attn_get_device_status(void* workspace, df_stream_t stream);
+
+/*
+ * Relative-position index table (the first step of df_attn_fwd, exposed for
+ * testing): idx[r + max_len - 1] = clamp(bucket(r) + span, 0, 2 span - 1) for
+ * every r in [-(max_len-1), max_len-1].  `idx` is a device int32 array of
+ * 2*max_len - 1 entries.  The logarithm is evaluated in double precision.
+ */
+df_status df_rel_index_table(int buckets, int max_rel, int span, int max_len, int32_t* idx,
+                             df_stream_t stream);
+
+/* Where df_attn_fwd keeps its planning data inside the workspace (byte offsets
+ * from the workspace base, all 256-byte aligned).  Filled by
+ * df_attn_workspace_layout for the same sizes as df_attn_workspace_size. */
+typedef struct {
+  size_t header;     /* df_ws_header                                        */
+  size_t idx_table;  /* int32 [2 table_half - 1], idx of r at r + table_half - 1 */
+  size_t items;      /* int32x4 [max_items] work items {start, n, head, qblk} */
+  size_t scalars;    /* float [H][4][Tpad]: log2-scaled Q.PK[0], Q.PK[2span-1],
+                        K.PQ[0], K.PQ[2span-1] of every token (-inf for masked keys) */
+  size_t keybias;    /* float [Tpad]: 0 for a valid key, -inf otherwise       */
+  size_t partial;    /* float [T][H][d + 2] un-normalised partial output, max, sum */
+  size_t total;      /* == df_attn_workspace_size()                           */
+  int max_items;     /* capacity of the work-item list                        */
+  int t_pad;         /* Tpad = round_up(B*L + 128, 128)                       */
+  int table_half;    /* round_up(L, 128) + 128: the table covers |r| < table_half */
+} df_ws_layout;
+
+/* Header at workspace offset 0, written on the device by every call. */
+typedef struct {
+  int32_t status;        /* df_status of the first device-side error, else 0 */
+  int32_t status_where;  /* kernel / wait site that raised it                */
+  int32_t n_items;       /* work items planned (query blocks of 128 rows)    */
+  int32_t r_sat_pos;     /* smallest r with idx(r) = 2 span - 1 (>= L if none) */
+  int32_t r_sat_neg;     /* largest r with idx(r) = 0 (<= -L if none)          */
+  int32_t n_seqs;        /* sequences seen                                    */
+  int32_t reserved[10];
+} df_ws_header;
+
+df_status df_attn_workspace_layout(int B, int H, int L, int d, int buckets, int max_rel, int span,
+                                   df_ws_layout* layout);
+
+/* Planning step of df_attn_fwd alone (same arguments and checks): writes the
+ * index table, the saturation points, the work list (query blocks of 128 rows,
+ * longest sequences first) and the per-token position scalars into the
+ * workspace, and zeros the output rows of padded / masked query tokens.  Used
+ * by tests of the scheduler; df_attn_fwd runs it itself. */
+df_status df_attn_plan(const void* q, const void* k, const void* pos_key, const void* pos_query,
+                       const uint8_t* key_mask, const int32_t* cu_seqlens,
+                       int B, int H, int L, int total_tokens, int d,
+                       int buckets, int max_rel, int span, df_dtype dtype,
+                       void* out, void* workspace, size_t workspace_bytes, df_stream_t stream);
+
+/* Profiling hook (process-wide, not thread-safe): while set, df_attn_fwd
+ * records events[0] before and events[1] after its dominant attention kernel on
+ * `stream`.  Pass NULL to clear.  The events are created and owned by the
+ * caller. */
+void df_attn_set_profile_events(df_event_t start, df_event_t stop);
+
+/* Upper bound, in SM clock cycles, of every spin-wait on an mbarrier inside the
+ * kernels (process-wide; 0 restores the default of about 2^31 cycles, ~1 s).
+ * When a wait runs out the kernel records DF_ERR_DEVICE_TIMEOUT in the
+ * workspace header, drains its own copies in flight, frees its tensor memory
+ * and returns. */
+void df_attn_set_wait_budget(unsigned long long cycles);
+
+/* Number of kernel launches the last successful df_attn_fwd enqueued. */
+int df_attn_last_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DF_ATTN_H */

@@ -1,0 +1,105 @@
+"""The C-ABI library loads, exports every entry point of include/df_attn.h, and
+rejects out-of-contract arguments on the host (no GPU needed: every call here
+returns before its first CUDA call)."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "df_attn.h")
+
+
+@pytest.fixture(scope="module")
+def binding():
+    from exact_attention_deberta_gb300.build import build
+    build()
+    from exact_attention_deberta_gb300 import binding as b
+    return b
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(df_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = _declared_functions()
+    for must in ("df_attn_fwd", "df_attn_workspace_size", "df_attn_supported",
+                 "df_attn_status_string", "df_attn_get_device_status", "df_rel_index_table"):
+        assert must in names
+
+
+def test_every_declared_symbol_is_exported(binding):
+    lib = ctypes.CDLL(binding.LIB_PATH)
+    missing = [n for n in _declared_functions() if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_status_strings(binding):
+    for s in range(7):
+        assert binding.status_string(s) and binding.status_string(s) != "unknown status"
+    assert binding.status_string(99) == "unknown status"
+
+
+def test_supported_matrix(binding):
+    import torch
+    ok = binding.DF_OK
+    assert binding.df_attn_supported(12, 8192, 64, torch.bfloat16) == ok
+    assert binding.df_attn_supported(8, 8192, 128, torch.float16) == ok
+    assert binding.df_attn_supported(12, 2048, 64, torch.float32) == ok
+    assert binding.df_attn_supported(12, 512, 48, torch.bfloat16) == binding.DF_ERR_UNSUPPORTED
+    assert binding.df_attn_supported(12, 512, 32, torch.bfloat16) == binding.DF_ERR_UNSUPPORTED
+    assert binding.df_attn_supported(0, 512, 64, torch.bfloat16) == binding.DF_ERR_INVALID_ARG
+    assert binding.df_attn_supported(12, 0, 64, torch.bfloat16) == binding.DF_ERR_INVALID_ARG
+    # buckets/2 must stay below max_rel - 1 for the logarithm to grow
+    assert binding.df_attn_supported(12, 512, 64, torch.bfloat16, buckets=1024, max_rel=512,
+                                     span=1024) == binding.DF_ERR_INVALID_ARG
+    assert binding.df_attn_supported(12, 512, 64, 7) == binding.DF_ERR_INVALID_ARG
+
+
+def test_workspace_size_and_layout(binding):
+    size = binding.df_attn_workspace_size(16, 12, 8192, 64)
+    lay = binding.df_attn_workspace_layout(16, 12, 8192, 64)
+    assert size == lay["total"] > 0
+    offs = [lay[k] for k in ("header", "idx_table", "items", "scalars", "keybias", "partial")]
+    assert offs == sorted(offs) and all(o % 256 == 0 for o in offs)
+    assert lay["max_items"] == 16 * 12 * 64
+    assert lay["table_half"] == 8192 + 128
+    assert binding.df_attn_workspace_size(16, 12, 8192, 48) == 0
+
+
+def _fwd_raw(binding, **over):
+    """Call df_attn_fwd with fake (never dereferenced) aligned pointers."""
+    a = dict(q=0x10000, k=0x20000, v=0x30000, pk=0x40000, pq=0x50000, mask=0x60000, cu=None,
+             B=2, H=2, L=64, T=128, d=64, buckets=256, max_rel=512, span=256, dtype=0,
+             out=0x70000, ws=0x100000, ws_bytes=1 << 30)
+    a.update(over)
+    vp = lambda x: None if x is None else ctypes.c_void_p(x)  # noqa: E731
+    return binding.raw_library.df_attn_fwd(
+        vp(a["q"]), vp(a["k"]), vp(a["v"]), vp(a["pk"]), vp(a["pq"]), vp(a["mask"]), vp(a["cu"]),
+        a["B"], a["H"], a["L"], a["T"], a["d"], a["buckets"], a["max_rel"], a["span"], a["dtype"],
+        vp(a["out"]), vp(a["ws"]), a["ws_bytes"], None)
+
+
+def test_host_side_rejections(binding):
+    b = binding
+    assert _fwd_raw(b, mask=None) == b.DF_ERR_INVALID_ARG               # neither mask nor cu
+    assert _fwd_raw(b, cu=0x80000) == b.DF_ERR_INVALID_ARG              # both
+    assert _fwd_raw(b, d=96) == b.DF_ERR_UNSUPPORTED
+    assert _fwd_raw(b, T=127) == b.DF_ERR_INVALID_ARG                   # padded needs T = B*L
+    assert _fwd_raw(b, mask=None, cu=0x80000, T=129) == b.DF_ERR_INVALID_ARG  # T > B*L
+    assert _fwd_raw(b, q=0x10008) == b.DF_ERR_ALIGNMENT
+    assert _fwd_raw(b, out=0x70004) == b.DF_ERR_ALIGNMENT
+    assert _fwd_raw(b, ws=0x100010) == b.DF_ERR_ALIGNMENT
+    assert _fwd_raw(b, ws_bytes=1000) == b.DF_ERR_WORKSPACE
+    assert _fwd_raw(b, ws=None) == b.DF_ERR_WORKSPACE
+    assert _fwd_raw(b, v=None) == b.DF_ERR_INVALID_ARG
+    assert _fwd_raw(b, dtype=5) == b.DF_ERR_INVALID_ARG
+    assert _fwd_raw(b, B=-1) == b.DF_ERR_INVALID_ARG
+    assert b.raw_library.df_attn_get_device_status(None, None) == b.DF_ERR_INVALID_ARG
+    assert b.raw_library.df_rel_index_table(256, 512, 256, 0, ctypes.c_void_p(0x1000),
+                                            None) == b.DF_ERR_INVALID_ARG
