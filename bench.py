@@ -267,6 +267,9 @@ def main(argv=None):
 
     kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(args.steps)]
+    for a, b in kev:  # torch creates the CUDA events lazily, at their first record
+        a.record(stream)
+        b.record(stream)
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if dist is not None:
         dist.barrier()
