@@ -176,6 +176,24 @@ def df_attn_plan(q, k, pos_key, pos_query, key_mask=None, cu_seqlens=None, *, ma
     return out, workspace
 
 
+_lib.df_attn_fwd_noalloc.argtypes = [_vp] * 7 + [_i] * 9 + [_vp, _vp]
+_lib.df_attn_fwd_noalloc.restype = _i
+NOALLOC_SCRATCH_BYTES = 64 << 20
+
+
+def df_attn_fwd_noalloc(q, k, v, pos_key, pos_query, key_mask=None, cu_seqlens=None, *, out,
+                        max_seqlen=None, buckets=256, max_rel=512, span=None, stream=None):
+    """df_attn_fwd for callers that cannot allocate device memory: the library's
+    built-in scratch array replaces the workspace, and ``out`` must be provided."""
+    B, H, L, T, d = _shape_args(q, key_mask, cu_seqlens, max_seqlen)
+    span = default_span(buckets, max_rel) if span is None else span
+    st = _lib.df_attn_fwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(pos_key), _ptr(pos_query),
+                                  _ptr(key_mask), _ptr(cu_seqlens), B, H, L, T, d, buckets,
+                                  max_rel, span, _DTYPE[q.dtype], _ptr(out), _stream(stream))
+    _check(st, "df_attn_fwd_noalloc")
+    return out
+
+
 def df_attn_get_device_status(workspace, stream=None) -> int:
     return int(_lib.df_attn_get_device_status(_ptr(workspace), _stream(stream)))
 

@@ -186,6 +186,34 @@ void df_attn_set_wait_budget(unsigned long long cycles);
 /* Number of kernel launches the last successful df_attn_fwd enqueued. */
 int df_attn_last_launch_count(void);
 
+/*
+ * df_attn_fwd without a workspace argument, for callers that cannot allocate
+ * device memory (a plug-in inside a host application that owns all device
+ * memory and offers no allocator, a service that forbids cudaMalloc / cudaFree
+ * after start-up).  No counterpart exists in the pages: this is a packaging
+ * variant of df_attn_fwd, with identical arguments, results and errors except:
+ *   - the scratch is a fixed DF_ATTN_NOALLOC_SCRATCH_BYTES array compiled into
+ *     the library; every GPU that loads the library holds it until the process
+ *     exits;
+ *   - a problem whose df_attn_workspace_size() exceeds that size is rejected
+ *     with DF_ERR_WORKSPACE and nothing is enqueued;
+ *   - the first call on each device looks the array's device address up (once,
+ *     with that device current); make that first call before any stream capture;
+ *   - every call on a device shares the one array, which keeps the previous
+ *     call's contents: calls that overlap on the GPU (other streams, other host
+ *     threads) race on it and must be serialised by the caller;
+ *   - the device-side status word lives in that shared array and is not
+ *     reported through this entry point.
+ * It calls no cudaMalloc, cudaFree or other allocating routine.
+ */
+#define DF_ATTN_NOALLOC_SCRATCH_BYTES (64u << 20)
+df_status df_attn_fwd_noalloc(const void* q, const void* k, const void* v,
+                              const void* pos_key, const void* pos_query,
+                              const uint8_t* key_mask, const int32_t* cu_seqlens,
+                              int B, int H, int L, int total_tokens, int d,
+                              int buckets, int max_rel, int span, df_dtype dtype,
+                              void* out, df_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif
