@@ -20,6 +20,11 @@ def run_gpu(binding, x, *, out=None, workspace=None, dev_inputs=None):
     kw = dict(buckets=x.w.buckets, max_rel=x.w.max_rel, span=x.w.span)
     d = dev_inputs or {n: to_dev(getattr(x, n)) for n in ("q", "k", "v", "pk", "pq", "key_mask",
                                                           "cu_seqlens")}
+    check_status = workspace is None
+    if workspace is None:
+        B = d["q"].shape[0] if x.w.layout == "padded" else d["cu_seqlens"].numel() - 1
+        size = binding.df_attn_workspace_size(B, x.w.H, x.w.L, x.w.d, **kw)
+        workspace = torch.empty(max(size, 256), dtype=torch.uint8, device="cuda")
     if x.w.layout == "padded":
         o = binding.df_attn_fwd(d["q"], d["k"], d["v"], d["pk"], d["pq"], key_mask=d["key_mask"],
                                 out=out, workspace=workspace, **kw)
@@ -28,6 +33,9 @@ def run_gpu(binding, x, *, out=None, workspace=None, dev_inputs=None):
                                 cu_seqlens=d["cu_seqlens"], max_seqlen=x.w.L, out=out,
                                 workspace=workspace, **kw)
     torch.cuda.synchronize()
+    if check_status:
+        st = binding.df_attn_get_device_status(workspace)
+        assert st == binding.DF_OK, f"device status {binding.status_string(st)}"
     return o
 
 
