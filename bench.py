@@ -323,7 +323,7 @@ def main(argv=None):
     tokens_rank = float(sum(lengths))
     value = world * flops_rank / (ms * 1e-3) / 1e12
     peaks, peak_src = load_peaks()
-    tc = x.w.dtype in ("bf16", "fp16") and launches_per_step >= 3
+    tc = x.w.dtype in ("bf16", "fp16")
     algo = algorithmic_flops(lengths, H, d, span)
     if tc:
         bound, peak, unit = "tensor", float(peaks["bf16_tflops_sustained"]), "TFLOP/s"

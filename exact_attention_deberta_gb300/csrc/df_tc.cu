@@ -1,26 +1,28 @@
-// Tensor-core fused forward (bf16 / fp16 I/O, fp32 accumulation) on tcgen05:
-// TMA stages Q, K, V and the PK / PQ index band of each tile in shared memory,
-// tcgen05.mma accumulates Q.K^T, the band products and P.V in tensor memory,
-// and one warpgroup runs the gather and the online softmax.
+// Near-tile fused forward on tcgen05 (bf16 / fp16 I/O, fp32 accumulation), and
+// the host orchestration of the tensor-core path (planning kernel -> near tiles
+// -> far tiles).
 //
 // Operation: DisentangledFlash README "Status" (C2P/P2C disentangled attention,
 // FP16/BF16, factorized padding masks, packed cu_seqlens) and the kernels-community
 // "DisentangledFlash" discussion "Motivation" (exact, tiled and streaming, no
 // [B,H,L,L] matrix).
 //
-// Tiles are 128 queries x 128 keys.  A far tile (its whole relative-distance range
-// saturated, so one PK / PQ row) takes its position terms from the per-token
-// scalars of the planning kernel.  A near tile needs the band of index rows
-// [lo, lo + W), W <= 255: the band products C = Q.PK[band]^T and
-// P = K.PQ[band]^T are formed in two 128-column halves, drained from tensor
-// memory to shared memory, and every score element gathers
-//   C[i][idx(i-j) - lo] + P[j][idx(i-j) - lo].
-// This kernel runs the steps of a tile one after the other (one warpgroup,
-// every role in line); it is the correctness baseline of the tensor-core path.
-#include "df_common.cuh"
-#include "df_tc_ptx.cuh"
+// A near tile (128 queries x 128 keys whose relative distances are not all
+// saturated) needs the band of PK / PQ rows [lo, lo + W), W <= 255, that its
+// distances map to.  TMA stages Q, K, V and the band rows in 128-byte swizzled
+// shared memory; tcgen05.mma forms S = Q.K^T, C = Q.PK[band]^T and
+// P = K.PQ[band]^T (two 128-column halves) in tensor memory; the band products
+// are drained to shared memory, rotated by 4 words per row so that both the
+// drain and the gather are free of bank conflicts, and every score element
+// gathers  C[i][idx(i-j) - lo] + P[j][idx(i-j) - lo].  The online softmax and
+// P.V (P read back from tensor memory) follow.  One warpgroup runs every step
+// of a tile in turn.
+//
+// A query block whose key range also has far tiles leaves its un-normalised
+// partial state (O, running max, running sum) in the workspace for the
+// far-tile kernel; otherwise this kernel writes the final rows.
+#include "df_tc_common.cuh"
 
-#include <cuda.h>
 #include <cudaTypedefs.h>
 
 #include <algorithm>
@@ -34,16 +36,10 @@ using namespace ptx;
 
 constexpr int kThreads = 128;
 constexpr int kTile = 128;
-constexpr uint32_t kBoxBytes = 128 * 64 * 2;  // one 128-row x 64-column tile of 16-bit values
-constexpr unsigned long long kDrainBudget = 1ull << 31;
-
-struct TcMaps {
-  CUtensorMap q, k, v, pk, pq;
-};
 
 // Shared-memory carve-up (offsets from a 1024-byte aligned base).
 template <int D>
-struct TcSmem {
+struct NearSmem {
   static constexpr int kChunks = D / 64;
   static constexpr uint32_t q = 0;
   static constexpr uint32_t k = q + kChunks * kBoxBytes;
@@ -51,23 +47,17 @@ struct TcSmem {
   static constexpr uint32_t r = v + kChunks * kBoxBytes;  // PK band half, then drained C
   static constexpr uint32_t rp = r + 65536;               // PQ band half, then drained P
   static constexpr uint32_t tab = rp + 65536;             // int32 [256] local index table
-  static constexpr uint32_t colv = tab + 1024;            // float [128] per-key bias
+  static constexpr uint32_t colv = tab + 1024;            // float [128] key bias
   static constexpr uint32_t bars = colv + 512;
   static constexpr uint32_t tslot = bars + 64;
   static constexpr uint32_t bytes = tslot + 16;
   static constexpr uint32_t alloc = bytes + 1024;
 };
 
-template <int D>
-__device__ __forceinline__ uint64_t kmajor_desc(const uint8_t* tile, int ks) {
-  // K step ks (16 elements): chunk ks/4 of 64 columns, 32-byte offset inside it.
-  return sdesc_sw128(smem_u32(tile + (ks >> 2) * kBoxBytes + (ks & 3) * 32), 16, 1024);
-}
-
 template <int D, bool BF16>
 __global__ void __launch_bounds__(kThreads, 1)
-    tc_serial_kernel(const Problem p, const __grid_constant__ TcMaps maps) {
-  using SL = TcSmem<D>;
+    tc_near_kernel(const Problem p, const __grid_constant__ TcMaps maps) {
+  using SL = NearSmem<D>;
   constexpr int kChunks = SL::kChunks;
   constexpr uint32_t kIdescQK = idesc_f16(128, 128, BF16 ? 1 : 0, 0, 0);
   constexpr uint32_t kIdescPV = idesc_f16(128, D, BF16 ? 1 : 0, 0, 1);
@@ -133,7 +123,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   for (int it = blockIdx.x; it < n_items && failed_at == 0; it += gridDim.x) {
     const int4 item = p.items[it];
     const int start = item.x, n = item.y, h = item.z, i0 = item.w * kTile;
-    const float* scal_h = p.scal + (size_t)h * 4 * p.t_pad;
+    const int nkb = (n + kTile - 1) / kTile;
+    int jlo, jhi;
+    near_block_range(i0, nkb, rsp, rsn, &jlo, &jhi);
+    if (jhi <= jlo) continue;  // every tile is far: the far-tile kernel does the block
+    const bool has_far = jlo > 0 || jhi < nkb;
+
     if (tid == 0) {
       mbar_expect_tx(bar_load, kChunks * kBoxBytes);
       for (int c = 0; c < kChunks; ++c)
@@ -142,40 +137,28 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (!wait_all(bar_load, ph_load, 1)) break;
 
     const int i = i0 + row;
+    const size_t tok = (size_t)start + i;
     const bool row_in = i < n;
-    const bool row_out = row_in && p.keybias[start + i] == 0.f;
-    const float a_neg = row_in ? scal_h[start + i] : 0.f;
-    const float a_pos = row_in ? scal_h[(size_t)p.t_pad + start + i] : 0.f;
+    const bool row_out = row_in && p.keybias[tok] == 0.f;
     float m_run = -INFINITY, l_run = 0.f;
-    const int nkb = (n + kTile - 1) / kTile;
 
-    for (int jb = 0; jb < nkb; ++jb) {
+    for (int jb = jlo; jb < jhi; ++jb) {
       const int j0 = jb * kTile;
       const int rlo = i0 - j0 - (kTile - 1), rhi = i0 - j0 + (kTile - 1);
-      const bool far_pos = rlo >= rsp, far_neg = rhi <= rsn, far = far_pos || far_neg;
-      int lo = 0, W = 0;
-      if (!far) {
-        lo = p.idx[rlo + p.lt - 1];
-        W = p.idx[rhi + p.lt - 1] - lo + 1;
-        for (int e = tid; e < 2 * kTile - 1; e += kThreads) sTab[e] = p.idx[rlo + e + p.lt - 1] - lo;
-      }
+      const int lo = p.idx[rlo + p.lt - 1];
+      const int W = p.idx[rhi + p.lt - 1] - lo + 1;
+      for (int e = tid; e < 2 * kTile - 1; e += kThreads) sTab[e] = p.idx[rlo + e + p.lt - 1] - lo;
       {
         const int j = j0 + tid;
-        float cv;
-        if (j >= n) cv = -INFINITY;
-        else if (far) cv = scal_h[(far_pos ? 3 : 2) * (size_t)p.t_pad + start + j];
-        else cv = p.keybias[start + j];
-        sCol[tid] = cv;
+        sCol[tid] = j < n ? p.keybias[(size_t)start + j] : -INFINITY;
       }
       if (tid == 0) {
-        mbar_expect_tx(bar_load, (far ? 2 : 4) * kChunks * kBoxBytes);
+        mbar_expect_tx(bar_load, 4 * kChunks * kBoxBytes);
         for (int c = 0; c < kChunks; ++c) {
           tma_load_2d(sK + c * kBoxBytes, &maps.k, h * D + c * 64, start + j0, bar_load);
           tma_load_2d(sV + c * kBoxBytes, &maps.v, h * D + c * 64, start + j0, bar_load);
-          if (!far) {
-            tma_load_2d(sR + c * kBoxBytes, &maps.pk, h * D + c * 64, lo, bar_load);
-            tma_load_2d(sRp + c * kBoxBytes, &maps.pq, h * D + c * 64, lo, bar_load);
-          }
+          tma_load_2d(sR + c * kBoxBytes, &maps.pk, h * D + c * 64, lo, bar_load);
+          tma_load_2d(sRp + c * kBoxBytes, &maps.pq, h * D + c * 64, lo, bar_load);
         }
       }
       if (!wait_all(bar_load, ph_load, 2)) break;
@@ -183,15 +166,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
 #pragma unroll
         for (int k = 0; k < D / 16; ++k)
-          mma_ss(tS, kmajor_desc<D>(sQ, k), kmajor_desc<D>(sK, k), kIdescQK, k > 0);
-        if (!far) {
+          mma_ss(tS, kmajor_desc(sQ, k), kmajor_desc(sK, k), kIdescQK, k > 0);
 #pragma unroll
-          for (int k = 0; k < D / 16; ++k)
-            mma_ss(tA, kmajor_desc<D>(sQ, k), kmajor_desc<D>(sR, k), kIdescQK, k > 0);
+        for (int k = 0; k < D / 16; ++k)
+          mma_ss(tA, kmajor_desc(sQ, k), kmajor_desc(sR, k), kIdescQK, k > 0);
 #pragma unroll
-          for (int k = 0; k < D / 16; ++k)
-            mma_ss(tB, kmajor_desc<D>(sK, k), kmajor_desc<D>(sRp, k), kIdescQK, k > 0);
-        }
+        for (int k = 0; k < D / 16; ++k)
+          mma_ss(tB, kmajor_desc(sK, k), kmajor_desc(sRp, k), kIdescQK, k > 0);
         mma_commit(bar_mma);
       }
       if (!wait_all(bar_mma, ph_mma, 3)) break;
@@ -209,91 +190,88 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
 
-      if (!far) {
-        float* Cs = reinterpret_cast<float*>(sR);
-        float* Ps = reinterpret_cast<float*>(sRp);
-        const int nch = (W + 127) >> 7;
-        bool ok = true;
-        for (int hc = 0; hc < nch && ok; ++hc) {
-          if (hc > 0) {
-            if (tid == 0) {
-              mbar_expect_tx(bar_load, 2 * kChunks * kBoxBytes);
-              for (int c = 0; c < kChunks; ++c) {
-                tma_load_2d(sR + c * kBoxBytes, &maps.pk, h * D + c * 64, lo + 128, bar_load);
-                tma_load_2d(sRp + c * kBoxBytes, &maps.pq, h * D + c * 64, lo + 128, bar_load);
-              }
+      float* Cs = reinterpret_cast<float*>(sR);
+      float* Ps = reinterpret_cast<float*>(sRp);
+      const int nch = (W + 127) >> 7;
+      bool ok = true;
+      for (int hc = 0; hc < nch && ok; ++hc) {
+        if (hc > 0) {
+          if (tid == 0) {
+            mbar_expect_tx(bar_load, 2 * kChunks * kBoxBytes);
+            for (int c = 0; c < kChunks; ++c) {
+              tma_load_2d(sR + c * kBoxBytes, &maps.pk, h * D + c * 64, lo + 128, bar_load);
+              tma_load_2d(sRp + c * kBoxBytes, &maps.pq, h * D + c * 64, lo + 128, bar_load);
             }
-            if (!(ok = wait_all(bar_load, ph_load, 4))) break;
-            if (tid == 0) {
-              tc_fence_after();
-#pragma unroll
-              for (int k = 0; k < D / 16; ++k)
-                mma_ss(tA, kmajor_desc<D>(sQ, k), kmajor_desc<D>(sR, k), kIdescQK, k > 0);
-#pragma unroll
-              for (int k = 0; k < D / 16; ++k)
-                mma_ss(tB, kmajor_desc<D>(sK, k), kmajor_desc<D>(sRp, k), kIdescQK, k > 0);
-              mma_commit(bar_mma);
-            }
-            if (!(ok = wait_all(bar_mma, ph_mma, 5))) break;
+          }
+          if (!(ok = wait_all(bar_load, ph_load, 4))) break;
+          if (tid == 0) {
             tc_fence_after();
+#pragma unroll
+            for (int k = 0; k < D / 16; ++k)
+              mma_ss(tA, kmajor_desc(sQ, k), kmajor_desc(sR, k), kIdescQK, k > 0);
+#pragma unroll
+            for (int k = 0; k < D / 16; ++k)
+              mma_ss(tB, kmajor_desc(sK, k), kmajor_desc(sRp, k), kIdescQK, k > 0);
+            mma_commit(bar_mma);
           }
-          // drain this half of both bands: lane = query row for C, key row for P;
-          // each row is rotated by 4 * (row % 8) words (conflict-free writes and gathers)
-          {
-            uint32_t r[32];
-            const int rot = 4 * (row & 7);
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-              tmem_ld32(tA + lane_off + 32 * c, r);
-              tmem_ld_wait(r);
-#pragma unroll
-              for (int m = 0; m < 8; ++m) {
-                const int col = (32 * c + 4 * m + rot) & 127;
-                *reinterpret_cast<uint4*>(Cs + row * 128 + col) =
-                    make_uint4(r[4 * m], r[4 * m + 1], r[4 * m + 2], r[4 * m + 3]);
-              }
-            }
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-              tmem_ld32(tB + lane_off + 32 * c, r);
-              tmem_ld_wait(r);
-#pragma unroll
-              for (int m = 0; m < 8; ++m) {
-                const int col = (32 * c + 4 * m + rot) & 127;
-                *reinterpret_cast<uint4*>(Ps + row * 128 + col) =
-                    make_uint4(r[4 * m], r[4 * m + 1], r[4 * m + 2], r[4 * m + 3]);
-              }
-            }
-          }
-          tc_fence_before();
-          __syncthreads();
-          {
-            const int base = 128 * hc;
-            const float* crow = Cs + row * 128;
-            const int crot = 4 * (row & 7);
-#pragma unroll
-            for (int j = 0; j < kTile; ++j) {
-              const int u = sTab[row - j + kTile - 1] - base;
-              if ((unsigned)u < 128u)
-                x[j] += crow[(u + crot) & 127] + Ps[j * 128 + ((u + 4 * (j & 7)) & 127)];
-            }
-          }
-          fence_proxy_async_smem();
-          __syncthreads();
+          if (!(ok = wait_all(bar_mma, ph_mma, 5))) break;
+          tc_fence_after();
         }
-        if (!ok) break;
+        // drain this half of both bands: lane = query row for C, key row for P;
+        // each row is rotated by 4 * (row % 8) words
+        {
+          uint32_t r[32];
+          const int rot = 4 * (row & 7);
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            tmem_ld32(tA + lane_off + 32 * c, r);
+            tmem_ld_wait(r);
+#pragma unroll
+            for (int m = 0; m < 8; ++m) {
+              const int col = (32 * c + 4 * m + rot) & 127;
+              *reinterpret_cast<uint4*>(Cs + row * 128 + col) =
+                  make_uint4(r[4 * m], r[4 * m + 1], r[4 * m + 2], r[4 * m + 3]);
+            }
+          }
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            tmem_ld32(tB + lane_off + 32 * c, r);
+            tmem_ld_wait(r);
+#pragma unroll
+            for (int m = 0; m < 8; ++m) {
+              const int col = (32 * c + 4 * m + rot) & 127;
+              *reinterpret_cast<uint4*>(Ps + row * 128 + col) =
+                  make_uint4(r[4 * m], r[4 * m + 1], r[4 * m + 2], r[4 * m + 3]);
+            }
+          }
+        }
+        tc_fence_before();
+        __syncthreads();
+        {
+          const int base = 128 * hc;
+          const float* crow = Cs + row * 128;
+          const int crot = 4 * (row & 7);
+#pragma unroll
+          for (int j = 0; j < kTile; ++j) {
+            const int u = sTab[row - j + kTile - 1] - base;
+            if ((unsigned)u < 128u)
+              x[j] += crow[(u + crot) & 127] + Ps[j * 128 + ((u + 4 * (j & 7)) & 127)];
+          }
+        }
+        fence_proxy_async_smem();
+        __syncthreads();
       }
+      if (!ok) break;
 
       // logits in log2 units; masked keys at -inf
-      const float alpha = far ? (far_pos ? a_pos : a_neg) : 0.f;
       float mt = -INFINITY;
 #pragma unroll
       for (int j = 0; j < kTile; j += 4) {
         const float4 cv = *reinterpret_cast<const float4*>(sCol + j);
-        x[j + 0] = fmaf(x[j + 0], ks, cv.x + alpha);
-        x[j + 1] = fmaf(x[j + 1], ks, cv.y + alpha);
-        x[j + 2] = fmaf(x[j + 2], ks, cv.z + alpha);
-        x[j + 3] = fmaf(x[j + 3], ks, cv.w + alpha);
+        x[j + 0] = fmaf(x[j + 0], ks, cv.x);
+        x[j + 1] = fmaf(x[j + 1], ks, cv.y);
+        x[j + 2] = fmaf(x[j + 2], ks, cv.z);
+        x[j + 3] = fmaf(x[j + 3], ks, cv.w);
         mt = fmaxf(mt, fmaxf(fmaxf(x[j], x[j + 1]), fmaxf(x[j + 2], x[j + 3])));
       }
       // Re-base only when the maximum grows by more than 2^8 (exact: numerator and
@@ -301,11 +279,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       float scale = 1.f;
       const bool rebase = mt > m_run + 8.f;
       if (rebase) {
-        scale = exp2f(m_run - mt);
+        scale = ex2(m_run - mt);
         m_run = mt;
         l_run *= scale;
       }
-      if (jb > 0 && __any_sync(0xffffffffu, rebase)) {
+      if (jb > jlo && __any_sync(0xffffffffu, rebase)) {
         uint32_t r[32];
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
@@ -324,8 +302,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c = 0; c < 2; ++c) {
 #pragma unroll
           for (int e = 0; e < 32; ++e) {
-            const float p0 = exp2f(x[64 * c + 2 * e] - mb);
-            const float p1 = exp2f(x[64 * c + 2 * e + 1] - mb);
+            const float p0 = ex2(x[64 * c + 2 * e] - mb);
+            const float p1 = ex2(x[64 * c + 2 * e + 1] - mb);
             l_run += p0 + p1;
             r[e] = BF16 ? pack_bf16x2(p0, p1) : pack_f16x2(p0, p1);
           }
@@ -338,10 +316,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (tid == 0) {
         tc_fence_after();
 #pragma unroll
-        for (int k = 0; k < kTile / 16; ++k) {
-          const uint64_t bdesc = sdesc_sw128(sV_addr + k * 2048, kBoxBytes, 1024);
-          mma_ts(tO, tS + 8 * k, bdesc, kIdescPV, (jb > 0 || k > 0) ? 1u : 0u);
-        }
+        for (int k = 0; k < kTile / 16; ++k)
+          mma_ts(tO, tS + 8 * k, vtile_desc(sV_addr, k), kIdescPV, (jb > jlo || k > 0) ? 1u : 0u);
         mma_commit(bar_mma);
       }
       if (!wait_all(bar_mma, ph_mma, 6)) break;
@@ -349,26 +325,42 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (failed_at) break;
 
-    // epilogue: O / l in the I/O dtype
+    // epilogue: final rows, or the partial state for the far-tile kernel
     {
-      const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
-      T* dst = static_cast<T*>(p.out) + ((size_t)(start + i) * p.H + h) * D;
       uint32_t r[32];
+      if (has_far) {
+        float* dst = partial_o(p) + (tok * p.H + h) * D;
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        tmem_ld32(tO + lane_off + 32 * c, r);
-        tmem_ld_wait(r);
-        if (row_out) {
-          uint32_t w[16];
+        for (int c = 0; c < D / 32; ++c) {
+          tmem_ld32(tO + lane_off + 32 * c, r);
+          tmem_ld_wait(r);
+          if (row_in) {
 #pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            const float o0 = __uint_as_float(r[2 * e]) * inv;
-            const float o1 = __uint_as_float(r[2 * e + 1]) * inv;
-            w[e] = BF16 ? pack_bf16x2(o0, o1) : pack_f16x2(o0, o1);
+            for (int e = 0; e < 32; e += 4)
+              *reinterpret_cast<uint4*>(dst + 32 * c + e) = make_uint4(r[e], r[e + 1], r[e + 2], r[e + 3]);
           }
-          uint4* d4 = reinterpret_cast<uint4*>(dst + 32 * c);
+        }
+        if (row_in) partial_ml(p)[tok * p.H + h] = make_float2(m_run, l_run);
+      } else {
+        const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+        T* dst = static_cast<T*>(p.out) + (tok * p.H + h) * D;
 #pragma unroll
-          for (int e = 0; e < 4; ++e) d4[e] = make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
+        for (int c = 0; c < D / 32; ++c) {
+          tmem_ld32(tO + lane_off + 32 * c, r);
+          tmem_ld_wait(r);
+          if (row_out) {
+            uint32_t w[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              const float o0 = __uint_as_float(r[2 * e]) * inv;
+              const float o1 = __uint_as_float(r[2 * e + 1]) * inv;
+              w[e] = BF16 ? pack_bf16x2(o0, o1) : pack_f16x2(o0, o1);
+            }
+            uint4* d4 = reinterpret_cast<uint4*>(dst + 32 * c);
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              d4[e] = make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
+          }
         }
       }
     }
@@ -423,13 +415,13 @@ int sm_count() {
 }
 
 template <int D, bool BF16>
-cudaError_t launch_serial(const Problem& p, const TcMaps& maps, cudaStream_t s) {
-  const uint32_t bytes = TcSmem<D>::alloc;
-  cudaError_t e = cudaFuncSetAttribute(tc_serial_kernel<D, BF16>,
+cudaError_t launch_near_typed(const Problem& p, const TcMaps& maps, cudaStream_t s) {
+  const uint32_t bytes = NearSmem<D>::alloc;
+  cudaError_t e = cudaFuncSetAttribute(tc_near_kernel<D, BF16>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
   if (e != cudaSuccess) return e;
   const int grid = std::min(p.max_items, sm_count());
-  tc_serial_kernel<D, BF16><<<grid, kThreads, bytes, s>>>(p, maps);
+  tc_near_kernel<D, BF16><<<grid, kThreads, bytes, s>>>(p, maps);
   return cudaGetLastError();
 }
 
@@ -452,11 +444,12 @@ cudaError_t launch_tc(const Problem& p, cudaStream_t s, cudaEvent_t ev0, cudaEve
   if (ev0) cudaEventRecord(ev0, s);
   cudaError_t e;
   if (p.d == 64)
-    e = bf16 ? launch_serial<64, true>(p, maps, s) : launch_serial<64, false>(p, maps, s);
+    e = bf16 ? launch_near_typed<64, true>(p, maps, s) : launch_near_typed<64, false>(p, maps, s);
   else
-    e = bf16 ? launch_serial<128, true>(p, maps, s) : launch_serial<128, false>(p, maps, s);
+    e = bf16 ? launch_near_typed<128, true>(p, maps, s) : launch_near_typed<128, false>(p, maps, s);
+  if (e == cudaSuccess) e = launch_far(p, maps, s);
   if (ev1) cudaEventRecord(ev1, s);
-  *launches = 1;
+  *launches = 2;
   return e;
 }
 

@@ -1,0 +1,61 @@
+// Pieces shared by the two tensor-core kernels (near tiles, far tiles).
+#pragma once
+
+#include <cuda.h>
+
+#include "df_common.cuh"
+#include "df_tc_ptx.cuh"
+
+namespace dfa {
+
+constexpr uint32_t kBoxBytes = 128 * 64 * 2;  // one 128-row x 64-column box of 16-bit values
+constexpr unsigned long long kDrainBudget = 1ull << 31;
+
+struct TcMaps {
+  CUtensorMap q, k, v, pk, pq;
+};
+
+// K step ks (16 elements) of a K-major 128-row tile stored as 64-column,
+// 128-byte-swizzled boxes: box ks/4, 32-byte offset inside it.
+__device__ __forceinline__ uint64_t kmajor_desc(const uint8_t* tile, int ks) {
+  return ptx::sdesc_sw128(ptx::smem_u32(tile + (ks >> 2) * kBoxBytes + (ks & 3) * 32), 16, 1024);
+}
+
+// K step ks (16 key rows) of a 128-row V tile used as the MN-major B operand of
+// P.V: 16 rows x 128 B = 2048 B per step, 64-column boxes kBoxBytes apart.
+__device__ __forceinline__ uint64_t vtile_desc(uint32_t v_addr, int ks) {
+  return ptx::sdesc_sw128(v_addr + ks * 2048, kBoxBytes, 1024);
+}
+
+// Key blocks of query block i0 whose 128 x 128 tile is near (its relative
+// distances i - j in [i0 - j0 - 127, i0 - j0 + 127] are not all saturated).
+// The near blocks form one run [*jlo, *jhi); blocks before it are saturated on
+// the positive side (idx = 2 span - 1), blocks after it on the negative side.
+__device__ __forceinline__ void near_block_range(int i0, int nkb, int rsp, int rsn, int* jlo,
+                                                 int* jhi) {
+  int lo = 0, hi = 0;
+  for (int jb = 0; jb < nkb; ++jb) {
+    const int j0 = jb * 128;
+    if (i0 - j0 - 127 >= rsp) lo = jb + 1;      // saturated positive side
+    if (i0 - j0 + 127 > rsn) hi = jb + 1;       // not saturated on the negative side
+  }
+  *jlo = lo;
+  *jhi = hi > lo ? hi : lo;
+}
+
+// Partial softmax state handed from the near-tile kernel to the far-tile kernel:
+// un-normalised O rows (fp32) and (running max, running sum) per (token, head).
+__device__ __forceinline__ float* partial_o(const Problem& p) { return p.partial; }
+__device__ __forceinline__ float2* partial_ml(const Problem& p) {
+  return reinterpret_cast<float2*>(p.partial + (size_t)p.B * p.L * p.H * p.d);
+}
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+cudaError_t launch_far(const Problem& p, const TcMaps& maps, cudaStream_t s);
+
+}  // namespace dfa

@@ -1,0 +1,456 @@
+// Far-tile fused forward on tcgen05 (bf16 / fp16 I/O, fp32 accumulation).
+//
+// A far tile (128 queries x 128 keys) lies wholly in a saturated part of the
+// DeBERTa relative-position index, so its c2p and p2c terms are the per-token
+// scalars alpha_i = Q_i.PK[top or 0] and beta_j = K_j.PQ[top or 0]
+// (DisentangledFlash README, "Status": C2P/P2C disentangled attention; the
+// kernels-community "DisentangledFlash" discussion, "Motivation": exact,
+// tiled, streaming).  What remains per tile is flash attention with a rank-1
+// bias:  x_ij = (Q_i.K_j) * log2(e)/sqrt(3d) + alpha_i + beta_j.
+//
+// Warp roles of one CTA (one CTA per SM, persistent over the work list):
+//   warp 0      TMA producer: Q of the item, then K and V of every far tile into
+//               a ring of shared-memory stages;
+//   warp 1      tcgen05.mma issuer: S = Q.K^T into one of two TMEM score
+//               buffers, then O_b += P.V with P read back from TMEM;
+//   warps 2-5   softmax warpgroup 0: even far tiles, accumulator O_0;
+//   warps 6-9   softmax warpgroup 1: odd far tiles, accumulator O_1.
+// The two warpgroups keep independent running (max, sum, O) so that neither
+// waits for the other while the tensor core alternates between them; the two
+// partial results are merged at the end of the item.  Warpgroup 0 starts from
+// the partial state the near-tile kernel left for this query block.
+#include "df_tc_common.cuh"
+
+#include <algorithm>
+#include <type_traits>
+
+namespace dfa {
+
+namespace {
+
+using namespace ptx;
+
+constexpr int kFarThreads = 320;
+
+template <int D>
+struct FarSmem {
+  static constexpr int kChunks = D / 64;
+  static constexpr int kStages = D == 64 ? 4 : 2;
+  static constexpr uint32_t kTileBytes = kChunks * kBoxBytes;
+  static constexpr uint32_t q = 0;
+  static constexpr uint32_t kv = q + kTileBytes;                     // [stage][K | V]
+  static constexpr uint32_t beta = kv + kStages * 2 * kTileBytes;    // float [2 wg][2][128]
+  static constexpr uint32_t ml = beta + 2 * 2 * 128 * 4;             // float4 [2 wg][128]
+  static constexpr uint32_t bars = ml + 2 * 128 * 16;
+  // q_full, q_empty, kv_full[S], kv_empty[S], s_full[2], p_full[2], o_final, drain
+  static constexpr int kBars = 2 + 2 * kStages + 2 + 2 + 2;
+  static constexpr uint32_t misc = bars + kBars * 8;                 // abort flag, tmem slot
+  static constexpr uint32_t bytes = misc + 16;
+  static constexpr uint32_t alloc = bytes + 1024;
+};
+
+// Bounded wait that also gives up as soon as another role has aborted.  On a
+// timeout it records DF_ERR_DEVICE_TIMEOUT and raises the CTA's abort flag.
+// Callers keep their control flow identical after a failure (no early exit), so
+// that warp-collective instructions and named barriers stay matched.
+__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity,
+                                              unsigned long long budget, volatile int* abort,
+                                              df_ws_header* hdr, int where) {
+  if (*abort) return false;
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  for (;;) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort) return false;
+    if ((unsigned long long)(clock64() - t0) > budget) {
+      *abort = 1;
+      raise_device_error(hdr, DF_ERR_DEVICE_TIMEOUT, where);
+      return false;
+    }
+  }
+}
+
+__device__ __forceinline__ void named_sync(int id, int count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+struct ItemGeom {
+  int start, n, h, i0, nkb, jlo, jhi, nt;
+  __device__ __forceinline__ int block_of(int t) const { return t < jlo ? t : jhi + (t - jlo); }
+  __device__ __forceinline__ bool pos_side(int t) const { return t < jlo; }
+};
+
+__device__ __forceinline__ ItemGeom item_geom(const Problem& p, int it, int rsp, int rsn) {
+  const int4 item = p.items[it];
+  ItemGeom g;
+  g.start = item.x;
+  g.n = item.y;
+  g.h = item.z;
+  g.i0 = item.w * 128;
+  g.nkb = (g.n + 127) >> 7;
+  near_block_range(g.i0, g.nkb, rsp, rsn, &g.jlo, &g.jhi);
+  g.nt = g.jlo + (g.nkb - g.jhi);
+  return g;
+}
+
+template <int D, bool BF16>
+__global__ void __launch_bounds__(kFarThreads, 1)
+    tc_far_kernel(const Problem p, const __grid_constant__ TcMaps maps) {
+  using SL = FarSmem<D>;
+  constexpr int kChunks = SL::kChunks;
+  constexpr int S = SL::kStages;
+  constexpr uint32_t kIdescQK = idesc_f16(128, 128, BF16 ? 1 : 0, 0, 0);
+  constexpr uint32_t kIdescPV = idesc_f16(128, D, BF16 ? 1 : 0, 0, 1);
+  using T = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  uint8_t* sQ = sm + SL::q;
+  uint8_t* sKV = sm + SL::kv;
+  float* sBeta = reinterpret_cast<float*>(sm + SL::beta);
+  float4* sML = reinterpret_cast<float4*>(sm + SL::ml);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + SL::bars);
+  uint64_t* q_full = bars;
+  uint64_t* q_empty = bars + 1;
+  uint64_t* kv_full = bars + 2;
+  uint64_t* kv_empty = bars + 2 + S;
+  uint64_t* s_full = bars + 2 + 2 * S;
+  uint64_t* p_full = s_full + 2;
+  uint64_t* o_final = p_full + 2;
+  uint64_t* drain = o_final + 1;
+  volatile int* s_abort = reinterpret_cast<volatile int*>(sm + SL::misc);
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + SL::misc + 4);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    mbar_init(q_empty, 1);
+    for (int s = 0; s < S; ++s) {
+      mbar_init(kv_full + s, 1);
+      mbar_init(kv_empty + s, 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(s_full + b, 1);
+      mbar_init(p_full + b, 4);
+    }
+    mbar_init(o_final, 1);
+    mbar_init(drain, 1);
+    *s_abort = 0;
+    mbar_fence_init();
+    tma_prefetch_desc(&maps.q);
+    tma_prefetch_desc(&maps.k);
+    tma_prefetch_desc(&maps.v);
+  }
+  if (warp == 1) {
+    tmem_alloc(tslot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tslot;
+  const uint32_t tS[2] = {tmem, tmem + 128};
+  const uint32_t tO[2] = {tmem + 256, tmem + 256 + D};
+
+  const int n_items = p.hdr->n_items;
+  const int rsp = p.hdr->r_sat_pos, rsn = p.hdr->r_sat_neg;
+  const unsigned long long budget = p.wait_budget;
+  df_ws_header* hdr = p.hdr;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      uint32_t g = 0, qc = 0;
+      int issued[S];
+      for (int s = 0; s < S; ++s) issued[s] = 0;
+      for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
+        const ItemGeom ig = item_geom(p, it, rsp, rsn);
+        if (ig.nt == 0) continue;
+        if (wait_or_abort(q_empty, (qc & 1) ^ 1, budget, s_abort, hdr, 301)) {
+          mbar_expect_tx(q_full, SL::kTileBytes);
+          for (int c = 0; c < kChunks; ++c)
+            tma_load_2d(sQ + c * kBoxBytes, &maps.q, ig.h * D + c * 64, ig.start + ig.i0, q_full);
+        }
+        ++qc;
+        for (int t = 0; t < ig.nt; ++t, ++g) {
+          const int s = g % S;
+          const int row = ig.start + ig.block_of(t) * 128;
+          if (wait_or_abort(kv_empty + s, ((g / S) & 1) ^ 1, budget, s_abort, hdr, 302)) {
+            uint8_t* st = sKV + s * 2 * SL::kTileBytes;
+            mbar_expect_tx(kv_full + s, 2 * SL::kTileBytes);
+            for (int c = 0; c < kChunks; ++c) {
+              tma_load_2d(st + c * kBoxBytes, &maps.k, ig.h * D + c * 64, row, kv_full + s);
+              tma_load_2d(st + SL::kTileBytes + c * kBoxBytes, &maps.v, ig.h * D + c * 64, row,
+                          kv_full + s);
+            }
+            issued[s] = (int)(g / S) + 1;
+          }
+        }
+      }
+      // no copy may still be landing when the CTA leaves
+      for (int s = 0; s < S; ++s)
+        if (issued[s] > 0) mbar_wait(kv_full + s, (issued[s] - 1) & 1, kDrainBudget);
+      if (qc > 0) mbar_wait(q_full, (qc - 1) & 1, kDrainBudget);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      uint32_t g = 0, qc = 0, pc[2] = {0, 0};
+      const uint32_t kv_addr = smem_u32(sKV);
+      for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
+        const ItemGeom ig = item_geom(p, it, rsp, rsn);
+        if (ig.nt == 0) continue;
+        const bool has_partial = ig.jhi > ig.jlo;
+        const bool q_ok = wait_or_abort(q_full, qc & 1, budget, s_abort, hdr, 311);
+        ++qc;
+        for (int t = 0; t <= ig.nt; ++t) {
+          if (t < ig.nt) {
+            const uint32_t gs = g + t;
+            const int s = gs % S;
+            const bool ok = wait_or_abort(kv_full + s, (gs / S) & 1, budget, s_abort, hdr, 312);
+            if (ok && q_ok) {
+              tc_fence_after();
+              const uint8_t* kt = sKV + s * 2 * SL::kTileBytes;
+#pragma unroll
+              for (int k = 0; k < D / 16; ++k)
+                mma_ss(tS[t & 1], kmajor_desc(sQ, k), kmajor_desc(kt, k), kIdescQK, k > 0);
+              mma_commit(s_full + (t & 1));
+            }
+          }
+          if (t >= 1) {
+            const int b = (t - 1) & 1;
+            const bool ok = wait_or_abort(p_full + b, pc[b] & 1, budget, s_abort, hdr, 313);
+            ++pc[b];
+            if (ok) {
+              tc_fence_after();
+              const uint32_t gs = g + t - 1;
+              const int s = gs % S;
+              const uint32_t v_addr = kv_addr + s * 2 * SL::kTileBytes + SL::kTileBytes;
+              const bool carry = (t - 1 >= 2) || (b == 0 && has_partial);
+#pragma unroll
+              for (int k = 0; k < 128 / 16; ++k)
+                mma_ts(tO[b], tS[b] + 8 * k, vtile_desc(v_addr, k), kIdescPV,
+                       (k > 0 || carry) ? 1u : 0u);
+              mma_commit(kv_empty + s);
+            }
+          }
+        }
+        g += ig.nt;
+        mma_commit(q_empty);
+        mma_commit(o_final);
+      }
+      mma_commit(drain);
+      mbar_wait(drain, 0, kDrainBudget);
+    }
+  } else {
+    // ------------------------------------------------------------ softmax warpgroups
+    const int wg = (warp - 2) >> 2;          // 0 or 1
+    const int quad = warp & 3;               // TMEM lane quadrant of this warp
+    const int row = quad * 32 + lane;        // query row inside the block
+    const int tid_wg = threadIdx.x - 64 - 128 * wg;
+    const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+    const float ks = p.kscale;
+    float* beta_buf = sBeta + wg * 256;
+    uint32_t sc = 0, ic = 0, own = 0;
+    for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
+      const ItemGeom ig = item_geom(p, it, rsp, rsn);
+      if (ig.nt == 0) continue;
+      const bool has_partial = ig.jhi > ig.jlo;
+      const int i = ig.i0 + row;
+      const bool row_in = i < ig.n;
+      const size_t tok = (size_t)ig.start + i;
+      const bool row_out = row_in && p.keybias[tok] == 0.f;
+      const float* scal_h = p.scal + (size_t)ig.h * 4 * p.t_pad;
+      const float a_neg = row_in ? scal_h[tok] : 0.f;
+      const float a_pos = row_in ? scal_h[(size_t)p.t_pad + tok] : 0.f;
+      float m_run = -INFINITY, l_run = 0.f;
+      bool o_has = false;
+      if (wg == 0 && has_partial) {
+        // resume from the near-tile kernel's state of this query block
+        uint32_t r[32];
+        const float* src = partial_o(p) + (tok * p.H + ig.h) * D;
+        if (row_in) {
+          const float2 ml = partial_ml(p)[tok * p.H + ig.h];
+          m_run = ml.x;
+          l_run = ml.y;
+        }
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+#pragma unroll
+          for (int e = 0; e < 32; e += 4) {
+            float4 v = row_in ? *reinterpret_cast<const float4*>(src + 32 * c + e)
+                              : make_float4(0.f, 0.f, 0.f, 0.f);
+            r[e] = __float_as_uint(v.x);
+            r[e + 1] = __float_as_uint(v.y);
+            r[e + 2] = __float_as_uint(v.z);
+            r[e + 3] = __float_as_uint(v.w);
+          }
+          tmem_st32(tO[0] + lane_off + 32 * c, r);
+        }
+        tmem_st_wait();
+        o_has = true;
+      }
+      // beta of a tile: one value per thread, shared through shared memory
+      auto beta_of = [&](int t) -> float {
+        const int j = ig.block_of(t) * 128 + tid_wg;
+        if (j >= ig.n) return -INFINITY;
+        return scal_h[(ig.pos_side(t) ? 3 : 2) * (size_t)p.t_pad + ig.start + j];
+      };
+      float beta_next = wg < ig.nt ? beta_of(wg) : 0.f;
+      for (int t = wg; t < ig.nt; t += 2, ++own) {
+        float* bb = beta_buf + (own & 1) * 128;
+        bb[tid_wg] = beta_next;
+        named_sync(1 + wg, 128);
+        if (t + 2 < ig.nt) beta_next = beta_of(t + 2);
+        wait_or_abort(s_full + wg, sc & 1, budget, s_abort, hdr, 321);
+        ++sc;
+        tc_fence_after();
+        float x[128];
+        {
+          uint32_t r[32];
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            tmem_ld32(tS[wg] + lane_off + 32 * c, r);
+            tmem_ld_wait(r);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) x[32 * c + e] = __uint_as_float(r[e]);
+          }
+        }
+        const float alpha = ig.pos_side(t) ? a_pos : a_neg;
+        float mt = -INFINITY;
+#pragma unroll
+        for (int j = 0; j < 128; j += 4) {
+          const float4 bv = *reinterpret_cast<const float4*>(bb + j);
+          x[j + 0] = fmaf(x[j + 0], ks, bv.x);
+          x[j + 1] = fmaf(x[j + 1], ks, bv.y);
+          x[j + 2] = fmaf(x[j + 2], ks, bv.z);
+          x[j + 3] = fmaf(x[j + 3], ks, bv.w);
+          mt = fmaxf(mt, fmaxf(fmaxf(x[j], x[j + 1]), fmaxf(x[j + 2], x[j + 3])));
+        }
+        mt += alpha;
+        float scale = 1.f;
+        const bool rebase = mt > m_run + 8.f;
+        if (rebase) {
+          scale = ex2(m_run - mt);
+          m_run = mt;
+          l_run *= scale;
+        }
+        if (o_has && __any_sync(0xffffffffu, rebase)) {
+          uint32_t r[32];
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) {
+            tmem_ld32(tO[wg] + lane_off + 32 * c, r);
+            tmem_ld_wait(r);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * scale);
+            tmem_st32(tO[wg] + lane_off + 32 * c, r);
+          }
+        }
+        // p = 2^(x + alpha - m); with no finite logit yet every p is 0
+        const float shift = m_run == -INFINITY ? INFINITY : m_run - alpha;
+        {
+          uint32_t r[32];
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+              const float p0 = ex2(x[64 * c + 2 * e] - shift);
+              const float p1 = ex2(x[64 * c + 2 * e + 1] - shift);
+              l_run += p0 + p1;
+              r[e] = BF16 ? pack_bf16x2(p0, p1) : pack_f16x2(p0, p1);
+            }
+            tmem_st32(tS[wg] + lane_off + 32 * c, r);
+          }
+          tmem_st_wait();
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(p_full + wg);
+        o_has = true;
+      }
+      // ---- merge the two warpgroups' partial results and write O
+      wait_or_abort(o_final, ic & 1, budget, s_abort, hdr, 322);
+      ++ic;
+      tc_fence_after();
+      sML[wg * 128 + row] = make_float4(m_run, l_run, o_has ? 1.f : 0.f, 0.f);
+      named_sync(3, 256);
+      const float4 mine = sML[wg * 128 + row];
+      const float4 other = sML[(1 - wg) * 128 + row];
+      const float4 a = wg == 0 ? mine : other;   // warpgroup 0's state
+      const float4 b = wg == 0 ? other : mine;   // warpgroup 1's state
+      const bool ha = a.z != 0.f, hb = b.z != 0.f;
+      float m = -INFINITY;
+      if (ha) m = fmaxf(m, a.x);
+      if (hb) m = fmaxf(m, b.x);
+      const float fa = (ha && m != -INFINITY) ? ex2(a.x - m) : 0.f;
+      const float fb = (hb && m != -INFINITY) ? ex2(b.x - m) : 0.f;
+      const float l = a.y * fa + b.y * fb;
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      const bool store = row_out && *s_abort == 0;
+      T* dst = static_cast<T*>(p.out) + (tok * p.H + ig.h) * D;
+#pragma unroll
+      for (int c = 0; c < D / 64; ++c) {
+        const int col = wg * (D / 2) + 32 * c;
+        uint32_t ra[32], rb[32];
+        tmem_ld32(tO[0] + lane_off + col, ra);
+        tmem_ld32(tO[1] + lane_off + col, rb);
+        tmem_ld_wait(ra);
+        tmem_ld_wait(rb);
+        if (store) {
+          uint32_t w[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const float o0 = (__uint_as_float(ra[2 * e]) * fa +
+                              (hb ? __uint_as_float(rb[2 * e]) * fb : 0.f)) * inv;
+            const float o1 = (__uint_as_float(ra[2 * e + 1]) * fa +
+                              (hb ? __uint_as_float(rb[2 * e + 1]) * fb : 0.f)) * inv;
+            w[e] = BF16 ? pack_bf16x2(o0, o1) : pack_f16x2(o0, o1);
+          }
+          uint4* d4 = reinterpret_cast<uint4*>(dst + col);
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            d4[e] = make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
+        }
+      }
+      tc_fence_before();
+      named_sync(3, 256);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, 512);
+}
+
+int far_sm_count() {
+  static int sms = 0;
+  if (!sms) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (sms <= 0) sms = 1;
+  }
+  return sms;
+}
+
+template <int D, bool BF16>
+cudaError_t launch_far_typed(const Problem& p, const TcMaps& maps, cudaStream_t s) {
+  const uint32_t bytes = FarSmem<D>::alloc;
+  cudaError_t e = cudaFuncSetAttribute(tc_far_kernel<D, BF16>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  if (e != cudaSuccess) return e;
+  const int grid = std::min(p.max_items, far_sm_count());
+  tc_far_kernel<D, BF16><<<grid, kFarThreads, bytes, s>>>(p, maps);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_far(const Problem& p, const TcMaps& maps, cudaStream_t s) {
+  const bool bf16 = p.dtype == DF_BF16;
+  if (p.d == 64) return bf16 ? launch_far_typed<64, true>(p, maps, s) : launch_far_typed<64, false>(p, maps, s);
+  return bf16 ? launch_far_typed<128, true>(p, maps, s) : launch_far_typed<128, false>(p, maps, s);
+}
+
+}  // namespace dfa
