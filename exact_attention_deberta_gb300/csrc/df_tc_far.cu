@@ -9,12 +9,16 @@
 // bias:  x_ij = (Q_i.K_j) * log2(e)/sqrt(3d) + alpha_i + beta_j.
 //
 // Warp roles of one CTA (one CTA per SM, persistent over the work list):
-//   warp 0      TMA producer: Q of the item, then K and V of every far tile into
-//               a ring of shared-memory stages;
+//   warp 0      TMA producer: Q of the item (two buffers, so the next item's Q
+//               lands while the current one finishes), then K and V of every
+//               far tile into a ring of shared-memory stages;
 //   warp 1      tcgen05.mma issuer: S = Q.K^T into one of two TMEM score
 //               buffers, then O_b += P.V with P read back from TMEM;
-//   warps 2-5   softmax warpgroup 0: even far tiles, accumulator O_0;
-//   warps 6-9   softmax warpgroup 1: odd far tiles, accumulator O_1.
+//   warps 2-3   idle (they complete the control warpgroup);
+//   warps 4-7   softmax warpgroup 0: even far tiles, accumulator O_0;
+//   warps 8-11  softmax warpgroup 1: odd far tiles, accumulator O_1.
+// The control warpgroup gives registers back (setmaxnreg) so that each softmax
+// thread can hold its 128-score row without spilling.
 // The two warpgroups keep independent running (max, sum, O) so that neither
 // waits for the other while the tensor core alternates between them; the two
 // partial results are merged at the end of the item.  Warpgroup 0 starts from
@@ -30,20 +34,21 @@ namespace {
 
 using namespace ptx;
 
-constexpr int kFarThreads = 320;
+constexpr int kFarThreads = 384;
 
 template <int D>
 struct FarSmem {
   static constexpr int kChunks = D / 64;
   static constexpr int kStages = D == 64 ? 4 : 2;
   static constexpr uint32_t kTileBytes = kChunks * kBoxBytes;
-  static constexpr uint32_t q = 0;
-  static constexpr uint32_t kv = q + kTileBytes;                     // [stage][K | V]
+  static constexpr uint32_t q = 0;                                   // [2][Q tile]
+  static constexpr uint32_t kv = q + 2 * kTileBytes;                 // [stage][K | V]
   static constexpr uint32_t beta = kv + kStages * 2 * kTileBytes;    // float [2 wg][2][128]
   static constexpr uint32_t ml = beta + 2 * 2 * 128 * 4;             // float4 [2 wg][128]
   static constexpr uint32_t bars = ml + 2 * 128 * 16;
-  // q_full, q_empty, kv_full[S], kv_empty[S], s_full[2], p_full[2], o_final, drain
-  static constexpr int kBars = 2 + 2 * kStages + 2 + 2 + 2;
+  // q_full[2], q_empty[2], kv_full[S], kv_empty[S], s_full[2], p_full[2], o_final, drain,
+  // s_cons[2], pv_done[2]
+  static constexpr int kBars = 4 + 2 * kStages + 2 + 2 + 2 + 4;
   static constexpr uint32_t misc = bars + kBars * 8;                 // abort flag, tmem slot
   static constexpr uint32_t bytes = misc + 16;
   static constexpr uint32_t alloc = bytes + 1024;
@@ -111,20 +116,24 @@ __global__ void __launch_bounds__(kFarThreads, 1)
   float4* sML = reinterpret_cast<float4*>(sm + SL::ml);
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + SL::bars);
   uint64_t* q_full = bars;
-  uint64_t* q_empty = bars + 1;
-  uint64_t* kv_full = bars + 2;
-  uint64_t* kv_empty = bars + 2 + S;
-  uint64_t* s_full = bars + 2 + 2 * S;
+  uint64_t* q_empty = bars + 2;
+  uint64_t* kv_full = bars + 4;
+  uint64_t* kv_empty = bars + 4 + S;
+  uint64_t* s_full = bars + 4 + 2 * S;
   uint64_t* p_full = s_full + 2;
   uint64_t* o_final = p_full + 2;
   uint64_t* drain = o_final + 1;
+  uint64_t* s_cons = drain + 1;   // softmax has read S(t) into registers
+  uint64_t* pv_done = s_cons + 2; // P(t).V has completed
   volatile int* s_abort = reinterpret_cast<volatile int*>(sm + SL::misc);
   uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + SL::misc + 4);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
-    mbar_init(q_full, 1);
-    mbar_init(q_empty, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(q_full + b, 1);
+      mbar_init(q_empty + b, 1);
+    }
     for (int s = 0; s < S; ++s) {
       mbar_init(kv_full + s, 1);
       mbar_init(kv_empty + s, 1);
@@ -135,6 +144,10 @@ __global__ void __launch_bounds__(kFarThreads, 1)
     }
     mbar_init(o_final, 1);
     mbar_init(drain, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(s_cons + b, 4);
+      mbar_init(pv_done + b, 1);
+    }
     *s_abort = 0;
     mbar_fence_init();
     tma_prefetch_desc(&maps.q);
@@ -151,6 +164,10 @@ __global__ void __launch_bounds__(kFarThreads, 1)
   const uint32_t tmem = *tslot;
   const uint32_t tS[2] = {tmem, tmem + 128};
   const uint32_t tO[2] = {tmem + 256, tmem + 256 + D};
+  // d = 64 leaves room for a P buffer per warpgroup, so that S can be refilled
+  // as soon as the softmax has read it; at d = 128 P overwrites its S buffer.
+  constexpr bool kSepP = D == 64;
+  const uint32_t tP[2] = {kSepP ? tmem + 384 : tS[0], kSepP ? tmem + 448 : tS[1]};
 
   const int n_items = p.hdr->n_items;
   const int rsp = p.hdr->r_sat_pos, rsn = p.hdr->r_sat_neg;
@@ -159,17 +176,19 @@ __global__ void __launch_bounds__(kFarThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
+    setmaxnreg_dec<56>();
     if (lane == 0) {
-      uint32_t g = 0, qc = 0;
-      int issued[S];
-      for (int s = 0; s < S; ++s) issued[s] = 0;
+      uint32_t g = 0, qc = 0, g_issued = 0, q_issued = 0;  // loads are issued in order
       for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
         const ItemGeom ig = item_geom(p, it, rsp, rsn);
         if (ig.nt == 0) continue;
-        if (wait_or_abort(q_empty, (qc & 1) ^ 1, budget, s_abort, hdr, 301)) {
-          mbar_expect_tx(q_full, SL::kTileBytes);
+        const int qb = qc & 1;
+        if (wait_or_abort(q_empty + qb, ((qc >> 1) & 1) ^ 1, budget, s_abort, hdr, 301)) {
+          mbar_expect_tx(q_full + qb, SL::kTileBytes);
           for (int c = 0; c < kChunks; ++c)
-            tma_load_2d(sQ + c * kBoxBytes, &maps.q, ig.h * D + c * 64, ig.start + ig.i0, q_full);
+            tma_load_2d(sQ + qb * SL::kTileBytes + c * kBoxBytes, &maps.q, ig.h * D + c * 64,
+                        ig.start + ig.i0, q_full + qb);
+          q_issued = qc + 1;
         }
         ++qc;
         for (int t = 0; t < ig.nt; ++t, ++g) {
@@ -183,71 +202,96 @@ __global__ void __launch_bounds__(kFarThreads, 1)
               tma_load_2d(st + SL::kTileBytes + c * kBoxBytes, &maps.v, ig.h * D + c * 64, row,
                           kv_full + s);
             }
-            issued[s] = (int)(g / S) + 1;
+            g_issued = g + 1;
           }
         }
       }
-      // no copy may still be landing when the CTA leaves
-      for (int s = 0; s < S; ++s)
-        if (issued[s] > 0) mbar_wait(kv_full + s, (issued[s] - 1) & 1, kDrainBudget);
-      if (qc > 0) mbar_wait(q_full, (qc - 1) & 1, kDrainBudget);
+      // no copy may still be landing when the CTA leaves: wait for the last load
+      // issued into every stage and into both Q buffers
+      for (uint32_t k = g_issued > (uint32_t)S ? g_issued - S : 0; k < g_issued; ++k)
+        mbar_wait(kv_full + k % S, (k / S) & 1, kDrainBudget);
+      for (uint32_t k = q_issued > 2 ? q_issued - 2 : 0; k < q_issued; ++k)
+        mbar_wait(q_full + (k & 1), (k >> 1) & 1, kDrainBudget);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
+    setmaxnreg_dec<56>();
     if (lane == 0) {
-      uint32_t g = 0, qc = 0, pc[2] = {0, 0};
+      uint32_t g = 0, qc = 0, pc[2] = {0, 0}, cc[2] = {0, 0};
       const uint32_t kv_addr = smem_u32(sKV);
       for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
         const ItemGeom ig = item_geom(p, it, rsp, rsn);
         if (ig.nt == 0) continue;
         const bool has_partial = ig.jhi > ig.jlo;
-        const bool q_ok = wait_or_abort(q_full, qc & 1, budget, s_abort, hdr, 311);
+        const int qb = qc & 1;
+        const uint8_t* sQb = sQ + qb * SL::kTileBytes;
+        const bool q_ok = wait_or_abort(q_full + qb, (qc >> 1) & 1, budget, s_abort, hdr, 311);
         ++qc;
-        for (int t = 0; t <= ig.nt; ++t) {
-          if (t < ig.nt) {
-            const uint32_t gs = g + t;
-            const int s = gs % S;
-            const bool ok = wait_or_abort(kv_full + s, (gs / S) & 1, budget, s_abort, hdr, 312);
-            if (ok && q_ok) {
-              tc_fence_after();
-              const uint8_t* kt = sKV + s * 2 * SL::kTileBytes;
+        auto issue_qk = [&](int t) {
+          const uint32_t gs = g + t;
+          const int s = gs % S;
+          const bool ok = wait_or_abort(kv_full + s, (gs / S) & 1, budget, s_abort, hdr, 312);
+          if (ok && q_ok) {
+            tc_fence_after();
+            const uint8_t* kt = sKV + s * 2 * SL::kTileBytes;
 #pragma unroll
-              for (int k = 0; k < D / 16; ++k)
-                mma_ss(tS[t & 1], kmajor_desc(sQ, k), kmajor_desc(kt, k), kIdescQK, k > 0);
-              mma_commit(s_full + (t & 1));
-            }
+            for (int k = 0; k < D / 16; ++k)
+              mma_ss(tS[t & 1], kmajor_desc(sQb, k), kmajor_desc(kt, k), kIdescQK, k > 0);
+            mma_commit(s_full + (t & 1));
           }
-          if (t >= 1) {
-            const int b = (t - 1) & 1;
-            const bool ok = wait_or_abort(p_full + b, pc[b] & 1, budget, s_abort, hdr, 313);
-            ++pc[b];
-            if (ok) {
-              tc_fence_after();
-              const uint32_t gs = g + t - 1;
-              const int s = gs % S;
-              const uint32_t v_addr = kv_addr + s * 2 * SL::kTileBytes + SL::kTileBytes;
-              const bool carry = (t - 1 >= 2) || (b == 0 && has_partial);
+        };
+        auto issue_pv = [&](int t) {
+          const int b = t & 1;
+          const bool ok = wait_or_abort(p_full + b, pc[b] & 1, budget, s_abort, hdr, 313);
+          ++pc[b];
+          if (ok) {
+            tc_fence_after();
+            const int s = (g + t) % S;
+            const uint32_t v_addr = kv_addr + s * 2 * SL::kTileBytes + SL::kTileBytes;
+            const bool carry = (t >= 2) || (b == 0 && has_partial);
 #pragma unroll
-              for (int k = 0; k < 128 / 16; ++k)
-                mma_ts(tO[b], tS[b] + 8 * k, vtile_desc(v_addr, k), kIdescPV,
-                       (k > 0 || carry) ? 1u : 0u);
-              mma_commit(kv_empty + s);
+            for (int k = 0; k < 128 / 16; ++k)
+              mma_ts(tO[b], tP[b] + 8 * k, vtile_desc(v_addr, k), kIdescPV,
+                     (k > 0 || carry) ? 1u : 0u);
+            mma_commit(kv_empty + s);
+            if (kSepP) mma_commit(pv_done + b);
+          }
+        };
+        if (kSepP) {
+          // QK(t + 2) goes out as soon as warpgroup t % 2 has read S(t)
+          for (int t = 0; t < ig.nt && t < 2; ++t) issue_qk(t);
+          for (int t = 0; t < ig.nt; ++t) {
+            if (t + 2 < ig.nt) {
+              const int b = t & 1;
+              wait_or_abort(s_cons + b, cc[b] & 1, budget, s_abort, hdr, 314);
+              ++cc[b];
+              issue_qk(t + 2);
             }
+            issue_pv(t);
+          }
+        } else {
+          // P overwrites S: QK(t) can only follow PV(t - 2)
+          for (int t = 0; t <= ig.nt; ++t) {
+            if (t < ig.nt) issue_qk(t);
+            if (t >= 1) issue_pv(t - 1);
           }
         }
         g += ig.nt;
-        mma_commit(q_empty);
+        mma_commit(q_empty + qb);
         mma_commit(o_final);
       }
       mma_commit(drain);
       mbar_wait(drain, 0, kDrainBudget);
     }
+  } else if (warp < 4) {
+    setmaxnreg_dec<56>();
   } else {
     // ------------------------------------------------------------ softmax warpgroups
-    const int wg = (warp - 2) >> 2;          // 0 or 1
+    setmaxnreg_inc<224>();
+    const int wg = (warp - 4) >> 2;          // 0 or 1
     const int quad = warp & 3;               // TMEM lane quadrant of this warp
     const int row = quad * 32 + lane;        // query row inside the block
-    const int tid_wg = threadIdx.x - 64 - 128 * wg;
+    const int tid_wg = threadIdx.x - 128 - 128 * wg;
     const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
     const float ks = p.kscale;
     float* beta_buf = sBeta + wg * 256;
@@ -296,12 +340,16 @@ __global__ void __launch_bounds__(kFarThreads, 1)
         if (j >= ig.n) return -INFINITY;
         return scal_h[(ig.pos_side(t) ? 3 : 2) * (size_t)p.t_pad + ig.start + j];
       };
-      float beta_next = wg < ig.nt ? beta_of(wg) : 0.f;
+      // beta values are fetched two own tiles ahead of their use
+      float beta_n1 = wg < ig.nt ? beta_of(wg) : 0.f;
+      float beta_n2 = wg + 2 < ig.nt ? beta_of(wg + 2) : 0.f;
+      const float2 ks2 = make_float2(ks, ks);
       for (int t = wg; t < ig.nt; t += 2, ++own) {
         float* bb = beta_buf + (own & 1) * 128;
-        bb[tid_wg] = beta_next;
+        bb[tid_wg] = beta_n1;
         named_sync(1 + wg, 128);
-        if (t + 2 < ig.nt) beta_next = beta_of(t + 2);
+        beta_n1 = beta_n2;
+        if (t + 4 < ig.nt) beta_n2 = beta_of(t + 4);
         wait_or_abort(s_full + wg, sc & 1, budget, s_abort, hdr, 321);
         ++sc;
         tc_fence_after();
@@ -316,18 +364,26 @@ __global__ void __launch_bounds__(kFarThreads, 1)
             for (int e = 0; e < 32; ++e) x[32 * c + e] = __uint_as_float(r[e]);
           }
         }
+        if (kSepP && t + 2 < ig.nt) {  // S(t) is in registers: the MMA may refill it
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(s_cons + wg);
+        }
         const float alpha = ig.pos_side(t) ? a_pos : a_neg;
-        float mt = -INFINITY;
+        float mt0 = -INFINITY, mt1 = -INFINITY;
 #pragma unroll
         for (int j = 0; j < 128; j += 4) {
           const float4 bv = *reinterpret_cast<const float4*>(bb + j);
-          x[j + 0] = fmaf(x[j + 0], ks, bv.x);
-          x[j + 1] = fmaf(x[j + 1], ks, bv.y);
-          x[j + 2] = fmaf(x[j + 2], ks, bv.z);
-          x[j + 3] = fmaf(x[j + 3], ks, bv.w);
-          mt = fmaxf(mt, fmaxf(fmaxf(x[j], x[j + 1]), fmaxf(x[j + 2], x[j + 3])));
+          const float2 y0 = fma2(make_float2(x[j], x[j + 1]), ks2, make_float2(bv.x, bv.y));
+          const float2 y1 = fma2(make_float2(x[j + 2], x[j + 3]), ks2, make_float2(bv.z, bv.w));
+          x[j] = y0.x;
+          x[j + 1] = y0.y;
+          x[j + 2] = y1.x;
+          x[j + 3] = y1.y;
+          mt0 = fmaxf(mt0, fmaxf(y0.x, y0.y));
+          mt1 = fmaxf(mt1, fmaxf(y1.x, y1.y));
         }
-        mt += alpha;
+        const float mt = fmaxf(mt0, mt1) + alpha;
         float scale = 1.f;
         const bool rebase = mt > m_run + 8.f;
         if (rebase) {
@@ -335,6 +391,29 @@ __global__ void __launch_bounds__(kFarThreads, 1)
           m_run = mt;
           l_run *= scale;
         }
+        // P(t - 2).V must be done before O is rescaled or P is overwritten
+        if (kSepP && own > 0) wait_or_abort(pv_done + wg, (own - 1) & 1, budget, s_abort, hdr, 323);
+        // p = 2^(x + alpha - m); with no finite logit yet every p is 0
+        const float shift = m_run == -INFINITY ? INFINITY : m_run - alpha;
+        const float2 nshift = make_float2(-shift, -shift);
+        {
+          uint32_t r[32];
+          float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+              const float2 z = add2(make_float2(x[64 * c + 2 * e], x[64 * c + 2 * e + 1]), nshift);
+              const float2 pp = make_float2(ex2(z.x), ex2(z.y));
+              acc = add2(acc, pp);
+              r[e] = BF16 ? pack_bf16x2(pp.x, pp.y) : pack_f16x2(pp.x, pp.y);
+            }
+            tmem_st32(tP[wg] + lane_off + 32 * c, r);
+          }
+          l_run += acc.x + acc.y;
+        }
+        // rescale O after the scores are dead (fewer live registers); P(t).V has
+        // not been issued yet, so O still holds the tiles before t
         if (o_has && __any_sync(0xffffffffu, rebase)) {
           uint32_t r[32];
 #pragma unroll
@@ -346,23 +425,7 @@ __global__ void __launch_bounds__(kFarThreads, 1)
             tmem_st32(tO[wg] + lane_off + 32 * c, r);
           }
         }
-        // p = 2^(x + alpha - m); with no finite logit yet every p is 0
-        const float shift = m_run == -INFINITY ? INFINITY : m_run - alpha;
-        {
-          uint32_t r[32];
-#pragma unroll
-          for (int c = 0; c < 2; ++c) {
-#pragma unroll
-            for (int e = 0; e < 32; ++e) {
-              const float p0 = ex2(x[64 * c + 2 * e] - shift);
-              const float p1 = ex2(x[64 * c + 2 * e + 1] - shift);
-              l_run += p0 + p1;
-              r[e] = BF16 ? pack_bf16x2(p0, p1) : pack_f16x2(p0, p1);
-            }
-            tmem_st32(tS[wg] + lane_off + 32 * c, r);
-          }
-          tmem_st_wait();
-        }
+        tmem_st_wait();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(p_full + wg);
