@@ -15,8 +15,12 @@
 // are drained to shared memory, rotated by 4 words per row so that both the
 // drain and the gather are free of bank conflicts, and every score element
 // gathers  C[i][idx(i-j) - lo] + P[j][idx(i-j) - lo].  The online softmax and
-// P.V (P read back from tensor memory) follow.  One warpgroup runs every step
-// of a tile in turn.
+// P.V (P read back from tensor memory) follow.  Two warpgroups share every
+// step of a tile: they split its key columns for the gather and the softmax
+// (exchanging the row maximum through shared memory), warpgroup 0 drains the
+// C band and warpgroup 1 the P band, and thread 0 issues the copies and MMAs.
+// The next tile's K and band rows are fetched while the softmax runs, its V
+// while the current P.V completes.
 //
 // A query block whose key range also has far tiles leaves its un-normalised
 // partial state (O, running max, running sum) in the workspace for the
@@ -34,7 +38,7 @@ namespace {
 
 using namespace ptx;
 
-constexpr int kThreads = 128;
+constexpr int kThreads = 256;
 constexpr int kTile = 128;
 
 // Shared-memory carve-up (offsets from a 1024-byte aligned base).
@@ -46,12 +50,16 @@ struct NearSmem {
   static constexpr uint32_t v = k + kChunks * kBoxBytes;
   static constexpr uint32_t r = v + kChunks * kBoxBytes;  // PK band half, then drained C
   static constexpr uint32_t rp = r + 65536;               // PQ band half, then drained P
-  static constexpr uint32_t tab = rp + 65536;             // int32 [256] local index table
+  // d = 64: the second band half (PK then PQ rows) lands with the first one
+  static constexpr bool kBand1 = D == 64;
+  static constexpr uint32_t br1 = rp + 65536;
+  static constexpr uint32_t tab = br1 + (kBand1 ? 2 * kChunks * kBoxBytes : 0);  // int32 [256]
   static constexpr uint32_t colv = tab + 1024;            // float [128] key bias
-  static constexpr uint32_t bars = colv + 512;
+  static constexpr uint32_t red = colv + 512;             // float [2][128]
+  static constexpr uint32_t bars = red + 1024;
   static constexpr uint32_t tslot = bars + 64;
   static constexpr uint32_t bytes = tslot + 16;
-  static constexpr uint32_t alloc = bytes + 1024;
+  static constexpr uint32_t alloc = bytes;  // the base is 1024-byte aligned (checked)
 };
 
 template <int D, bool BF16>
@@ -63,24 +71,36 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr uint32_t kIdescPV = idesc_f16(128, D, BF16 ? 1 : 0, 0, 1);
   using T = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
 
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* sm = reinterpret_cast<uint8_t*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  // 128-byte swizzled tiles need 1024-byte aligned shared memory; the near-tile
+  // layout uses the whole 227 KB, so there is no slack to realign at run time.
+  if ((smem_u32(smem_raw) & 1023u) != 0) {
+    if (threadIdx.x == 0 && blockIdx.x == 0) raise_device_error(p.hdr, DF_ERR_CUDA, 250);
+    return;
+  }
+  uint8_t* sm = smem_raw;
   uint8_t* sQ = sm + SL::q;
   uint8_t* sK = sm + SL::k;
   uint8_t* sV = sm + SL::v;
   uint8_t* sR = sm + SL::r;
   uint8_t* sRp = sm + SL::rp;
+  uint8_t* sB1 = sm + SL::br1;
   int32_t* sTab = reinterpret_cast<int32_t*>(sm + SL::tab);
   float* sCol = reinterpret_cast<float*>(sm + SL::colv);
-  uint64_t* bar_load = reinterpret_cast<uint64_t*>(sm + SL::bars);
-  uint64_t* bar_mma = bar_load + 1;
+  float* sRed = reinterpret_cast<float*>(sm + SL::red);  // [2][128] cross-warpgroup exchange
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + SL::bars);
+  uint64_t* bar_q = bars;
+  uint64_t* bar_kv = bars + 1;    // K and band half 0
+  uint64_t* bar_v = bars + 2;
+  uint64_t* bar_band = bars + 3;  // band half 1
+  uint64_t* bar_mma = bars + 4;
   uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + SL::tslot);
 
   const int tid = threadIdx.x, warp = tid >> 5;
-  const int row = tid;  // TMEM lane == query row (S, C, O) or key row (P)
+  const int half = warp >> 2;                   // warpgroup: key columns [64 half, 64 half + 64)
+  const int row = (warp & 3) * 32 + (tid & 31);  // TMEM lane: query row (S, C, O) or key row (P)
   if (tid == 0) {
-    mbar_init(bar_load, 1);
-    mbar_init(bar_mma, 1);
+    for (int b = 0; b < 5; ++b) mbar_init(bars + b, 1);
     mbar_fence_init();
     tma_prefetch_desc(&maps.q);
     tma_prefetch_desc(&maps.k);
@@ -96,10 +116,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tslot;
-  const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+  const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
   const uint32_t tS = tmem, tA = tmem + 128, tB = tmem + 256, tO = tmem + 384;
 
-  uint32_t ph_load = 0, ph_mma = 0;
+  uint32_t ph_q = 0, ph_kv = 0, ph_v = 0, ph_band = 0, ph_mma = 0;
   int failed_at = 0;
   const unsigned long long budget = p.wait_budget;
   // Block-uniform bounded wait.  On a timeout the phase is still awaited (with a
@@ -119,6 +139,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int rsp = p.hdr->r_sat_pos, rsn = p.hdr->r_sat_neg;
   const float ks = p.kscale;
   const uint32_t sV_addr = smem_u32(sV);
+  float* Cs = reinterpret_cast<float*>(sR);
+  float* Ps = reinterpret_cast<float*>(sRp);
 
   for (int it = blockIdx.x; it < n_items && failed_at == 0; it += gridDim.x) {
     const int4 item = p.items[it];
@@ -128,40 +150,68 @@ __global__ void __launch_bounds__(kThreads, 1)
     near_block_range(i0, nkb, rsp, rsn, &jlo, &jhi);
     if (jhi <= jlo) continue;  // every tile is far: the far-tile kernel does the block
     const bool has_far = jlo > 0 || jhi < nkb;
-
-    if (tid == 0) {
-      mbar_expect_tx(bar_load, kChunks * kBoxBytes);
+    // K and band half 0 (and, with a dedicated buffer, half 1) of tile jb on one
+    // barrier; lo and hi are idx at the tile's smallest and largest distance
+    auto load_kband = [&](int jb, int lo, int hi) {
+      const bool h1 = SL::kBand1 && hi - lo + 1 > 128;
+      mbar_expect_tx(bar_kv, (h1 ? 5 : 3) * kChunks * kBoxBytes);
+      for (int c = 0; c < kChunks; ++c) {
+        tma_load_2d(sK + c * kBoxBytes, &maps.k, h * D + c * 64, start + jb * kTile, bar_kv);
+        tma_load_2d(sR + c * kBoxBytes, &maps.pk, h * D + c * 64, lo, bar_kv);
+        tma_load_2d(sRp + c * kBoxBytes, &maps.pq, h * D + c * 64, lo, bar_kv);
+        if (h1) {
+          tma_load_2d(sB1 + c * kBoxBytes, &maps.pk, h * D + c * 64, lo + 128, bar_kv);
+          tma_load_2d(sB1 + (kChunks + c) * kBoxBytes, &maps.pq, h * D + c * 64, lo + 128, bar_kv);
+        }
+      }
+    };
+    auto idx_at = [&](int r) { return p.idx[r + p.lt - 1]; };
+    auto load_v = [&](int jb) {
+      mbar_expect_tx(bar_v, kChunks * kBoxBytes);
       for (int c = 0; c < kChunks; ++c)
-        tma_load_2d(sQ + c * kBoxBytes, &maps.q, h * D + c * 64, start + i0, bar_load);
+        tma_load_2d(sV + c * kBoxBytes, &maps.v, h * D + c * 64, start + jb * kTile, bar_v);
+    };
+    if (tid == 0) {
+      mbar_expect_tx(bar_q, kChunks * kBoxBytes);
+      for (int c = 0; c < kChunks; ++c)
+        tma_load_2d(sQ + c * kBoxBytes, &maps.q, h * D + c * 64, start + i0, bar_q);
+      load_kband(jlo, idx_at(i0 - jlo * kTile - (kTile - 1)), idx_at(i0 - jlo * kTile + (kTile - 1)));
+      load_v(jlo);
     }
-    if (!wait_all(bar_load, ph_load, 1)) break;
+    if (!wait_all(bar_q, ph_q, 1)) break;
 
     const int i = i0 + row;
     const size_t tok = (size_t)start + i;
     const bool row_in = i < n;
     const bool row_out = row_in && p.keybias[tok] == 0.f;
-    float m_run = -INFINITY, l_run = 0.f;
+    float m_run = -INFINITY, l_run = 0.f;  // l_run: this warpgroup's columns only
 
+    // raw index-table entries and the key bias of a tile, fetched one tile ahead
+    auto fetch_tab = [&](int jb) -> int {
+      return tid < 2 * kTile - 1 ? idx_at(i0 - jb * kTile - (kTile - 1) + tid) : 0;
+    };
+    auto fetch_col = [&](int jb) -> float {
+      const int j = jb * kTile + tid;
+      return tid < kTile ? (j < n ? p.keybias[(size_t)start + j] : -INFINITY) : 0.f;
+    };
+    int tab_next = fetch_tab(jlo);
+    float col_next = fetch_col(jlo);
     for (int jb = jlo; jb < jhi; ++jb) {
       const int j0 = jb * kTile;
-      const int rlo = i0 - j0 - (kTile - 1), rhi = i0 - j0 + (kTile - 1);
-      const int lo = p.idx[rlo + p.lt - 1];
-      const int W = p.idx[rhi + p.lt - 1] - lo + 1;
-      for (int e = tid; e < 2 * kTile - 1; e += kThreads) sTab[e] = p.idx[rlo + e + p.lt - 1] - lo;
-      {
-        const int j = j0 + tid;
-        sCol[tid] = j < n ? p.keybias[(size_t)start + j] : -INFINITY;
-      }
-      if (tid == 0) {
-        mbar_expect_tx(bar_load, 4 * kChunks * kBoxBytes);
-        for (int c = 0; c < kChunks; ++c) {
-          tma_load_2d(sK + c * kBoxBytes, &maps.k, h * D + c * 64, start + j0, bar_load);
-          tma_load_2d(sV + c * kBoxBytes, &maps.v, h * D + c * 64, start + j0, bar_load);
-          tma_load_2d(sR + c * kBoxBytes, &maps.pk, h * D + c * 64, lo, bar_load);
-          tma_load_2d(sRp + c * kBoxBytes, &maps.pq, h * D + c * 64, lo, bar_load);
+      if (tid < 2 * kTile - 1) sTab[tid] = tab_next;
+      if (tid < kTile) sCol[tid] = col_next;
+      int lo_next = 0, hi_next = 0;
+      if (jb + 1 < jhi) {
+        tab_next = fetch_tab(jb + 1);
+        col_next = fetch_col(jb + 1);
+        if (tid == 0) {
+          lo_next = tab_next;
+          hi_next = idx_at(i0 - (jb + 1) * kTile + (kTile - 1));
         }
       }
-      if (!wait_all(bar_load, ph_load, 2)) break;
+      if (!wait_all(bar_kv, ph_kv, 2)) break;
+      const int lo = sTab[0];
+      const int W = sTab[2 * kTile - 2] - lo + 1;
       if (tid == 0) {
         tc_fence_after();
 #pragma unroll
@@ -178,69 +228,62 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!wait_all(bar_mma, ph_mma, 3)) break;
       tc_fence_after();
 
-      float x[kTile];
+      float x[64];
       {
         uint32_t r[32];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          tmem_ld32(tS + lane_off + 32 * c, r);
+        for (int c = 0; c < 2; ++c) {
+          tmem_ld32(tS + lane_off + 64 * half + 32 * c, r);
           tmem_ld_wait(r);
 #pragma unroll
           for (int e = 0; e < 32; ++e) x[32 * c + e] = __uint_as_float(r[e]);
         }
       }
 
-      float* Cs = reinterpret_cast<float*>(sR);
-      float* Ps = reinterpret_cast<float*>(sRp);
       const int nch = (W + 127) >> 7;
       bool ok = true;
       for (int hc = 0; hc < nch && ok; ++hc) {
         if (hc > 0) {
-          if (tid == 0) {
-            mbar_expect_tx(bar_load, 2 * kChunks * kBoxBytes);
-            for (int c = 0; c < kChunks; ++c) {
-              tma_load_2d(sR + c * kBoxBytes, &maps.pk, h * D + c * 64, lo + 128, bar_load);
-              tma_load_2d(sRp + c * kBoxBytes, &maps.pq, h * D + c * 64, lo + 128, bar_load);
+          const uint8_t* pk1 = SL::kBand1 ? sB1 : sR;
+          const uint8_t* pq1 = SL::kBand1 ? sB1 + kChunks * kBoxBytes : sRp;
+          if (!SL::kBand1) {
+            if (tid == 0) {
+              mbar_expect_tx(bar_band, 2 * kChunks * kBoxBytes);
+              for (int c = 0; c < kChunks; ++c) {
+                tma_load_2d(sR + c * kBoxBytes, &maps.pk, h * D + c * 64, lo + 128, bar_band);
+                tma_load_2d(sRp + c * kBoxBytes, &maps.pq, h * D + c * 64, lo + 128, bar_band);
+              }
             }
+            if (!(ok = wait_all(bar_band, ph_band, 4))) break;
           }
-          if (!(ok = wait_all(bar_load, ph_load, 4))) break;
           if (tid == 0) {
             tc_fence_after();
 #pragma unroll
             for (int k = 0; k < D / 16; ++k)
-              mma_ss(tA, kmajor_desc(sQ, k), kmajor_desc(sR, k), kIdescQK, k > 0);
+              mma_ss(tA, kmajor_desc(sQ, k), kmajor_desc(pk1, k), kIdescQK, k > 0);
 #pragma unroll
             for (int k = 0; k < D / 16; ++k)
-              mma_ss(tB, kmajor_desc(sK, k), kmajor_desc(sRp, k), kIdescQK, k > 0);
+              mma_ss(tB, kmajor_desc(sK, k), kmajor_desc(pq1, k), kIdescQK, k > 0);
             mma_commit(bar_mma);
           }
           if (!(ok = wait_all(bar_mma, ph_mma, 5))) break;
           tc_fence_after();
         }
-        // drain this half of both bands: lane = query row for C, key row for P;
-        // each row is rotated by 4 * (row % 8) words
+        // drain: warpgroup 0 the C band (lane = query row), warpgroup 1 the P band
+        // (lane = key row); every row is rotated by 4 * (row % 8) words
         {
           uint32_t r[32];
           const int rot = 4 * (row & 7);
+          const uint32_t src = (half == 0 ? tA : tB) + lane_off;
+          float* dst = (half == 0 ? Cs : Ps) + row * 128;
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
-            tmem_ld32(tA + lane_off + 32 * c, r);
+            tmem_ld32(src + 32 * c, r);
             tmem_ld_wait(r);
 #pragma unroll
             for (int m = 0; m < 8; ++m) {
               const int col = (32 * c + 4 * m + rot) & 127;
-              *reinterpret_cast<uint4*>(Cs + row * 128 + col) =
-                  make_uint4(r[4 * m], r[4 * m + 1], r[4 * m + 2], r[4 * m + 3]);
-            }
-          }
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            tmem_ld32(tB + lane_off + 32 * c, r);
-            tmem_ld_wait(r);
-#pragma unroll
-            for (int m = 0; m < 8; ++m) {
-              const int col = (32 * c + 4 * m + rot) & 127;
-              *reinterpret_cast<uint4*>(Ps + row * 128 + col) =
+              *reinterpret_cast<uint4*>(dst + col) =
                   make_uint4(r[4 * m], r[4 * m + 1], r[4 * m + 2], r[4 * m + 3]);
             }
           }
@@ -248,34 +291,41 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         __syncthreads();
         {
-          const int base = 128 * hc;
+          const int base = lo + 128 * hc;  // the table holds raw idx values
           const float* crow = Cs + row * 128;
           const int crot = 4 * (row & 7);
+          const int32_t* tab = sTab + row + kTile - 1 - 64 * half;
 #pragma unroll
-          for (int j = 0; j < kTile; ++j) {
-            const int u = sTab[row - j + kTile - 1] - base;
+          for (int jj = 0; jj < 64; ++jj) {
+            const int j = 64 * half + jj;
+            const int u = tab[-jj] - base;
             if ((unsigned)u < 128u)
-              x[j] += crow[(u + crot) & 127] + Ps[j * 128 + ((u + 4 * (j & 7)) & 127)];
+              x[jj] += crow[(u + crot) & 127] + Ps[j * 128 + ((u + 4 * (j & 7)) & 127)];
           }
         }
         fence_proxy_async_smem();
         __syncthreads();
       }
       if (!ok) break;
+      // K and the band buffers are free: the next tile's K and band half 0 can land
+      if (tid == 0 && jb + 1 < jhi) load_kband(jb + 1, lo_next, hi_next);
 
-      // logits in log2 units; masked keys at -inf
+      // logits in log2 units; masked keys at -inf; row maximum over both warpgroups
       float mt = -INFINITY;
 #pragma unroll
-      for (int j = 0; j < kTile; j += 4) {
-        const float4 cv = *reinterpret_cast<const float4*>(sCol + j);
-        x[j + 0] = fmaf(x[j + 0], ks, cv.x);
-        x[j + 1] = fmaf(x[j + 1], ks, cv.y);
-        x[j + 2] = fmaf(x[j + 2], ks, cv.z);
-        x[j + 3] = fmaf(x[j + 3], ks, cv.w);
-        mt = fmaxf(mt, fmaxf(fmaxf(x[j], x[j + 1]), fmaxf(x[j + 2], x[j + 3])));
+      for (int jj = 0; jj < 64; jj += 4) {
+        const float4 cv = *reinterpret_cast<const float4*>(sCol + 64 * half + jj);
+        x[jj + 0] = fmaf(x[jj + 0], ks, cv.x);
+        x[jj + 1] = fmaf(x[jj + 1], ks, cv.y);
+        x[jj + 2] = fmaf(x[jj + 2], ks, cv.z);
+        x[jj + 3] = fmaf(x[jj + 3], ks, cv.w);
+        mt = fmaxf(mt, fmaxf(fmaxf(x[jj], x[jj + 1]), fmaxf(x[jj + 2], x[jj + 3])));
       }
+      sRed[half * 128 + row] = mt;
+      __syncthreads();
+      mt = fmaxf(sRed[row], sRed[128 + row]);
       // Re-base only when the maximum grows by more than 2^8 (exact: numerator and
-      // denominator share the stale base).
+      // denominator share the stale base).  Both warpgroups take the same decision.
       float scale = 1.f;
       const bool rebase = mt > m_run + 8.f;
       if (rebase) {
@@ -286,33 +336,29 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (jb > jlo && __any_sync(0xffffffffu, rebase)) {
         uint32_t r[32];
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          tmem_ld32(tO + lane_off + 32 * c, r);
+        for (int c = 0; c < D / 64; ++c) {
+          const uint32_t a = tO + lane_off + half * (D / 2) + 32 * c;
+          tmem_ld32(a, r);
           tmem_ld_wait(r);
 #pragma unroll
           for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * scale);
-          tmem_st32(tO + lane_off + 32 * c, r);
+          tmem_st32(a, r);
         }
-        tmem_st_wait();
       }
       const float mb = m_run == -INFINITY ? 0.f : m_run;
       {
         uint32_t r[32];
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
-#pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            const float p0 = ex2(x[64 * c + 2 * e] - mb);
-            const float p1 = ex2(x[64 * c + 2 * e + 1] - mb);
-            l_run += p0 + p1;
-            r[e] = BF16 ? pack_bf16x2(p0, p1) : pack_f16x2(p0, p1);
-          }
-          tmem_st32(tS + lane_off + 32 * c, r);
+        for (int e = 0; e < 32; ++e) {
+          const float p0 = ex2(x[2 * e] - mb);
+          const float p1 = ex2(x[2 * e + 1] - mb);
+          l_run += p0 + p1;
+          r[e] = BF16 ? pack_bf16x2(p0, p1) : pack_f16x2(p0, p1);
         }
+        tmem_st32(tS + lane_off + 32 * half, r);
         tmem_st_wait();
       }
-      tc_fence_before();
-      __syncthreads();
+      if (!wait_all(bar_v, ph_v, 6)) break;  // includes the block barrier before P.V
       if (tid == 0) {
         tc_fence_after();
 #pragma unroll
@@ -320,19 +366,23 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_ts(tO, tS + 8 * k, vtile_desc(sV_addr, k), kIdescPV, (jb > jlo || k > 0) ? 1u : 0u);
         mma_commit(bar_mma);
       }
-      if (!wait_all(bar_mma, ph_mma, 6)) break;
+      if (!wait_all(bar_mma, ph_mma, 7)) break;
       tc_fence_after();
+      if (tid == 0 && jb + 1 < jhi) load_v(jb + 1);
     }
     if (failed_at) break;
 
     // epilogue: final rows, or the partial state for the far-tile kernel
+    sRed[half * 128 + row] = l_run;
+    __syncthreads();
+    const float l_tot = sRed[row] + sRed[128 + row];
     {
       uint32_t r[32];
       if (has_far) {
-        float* dst = partial_o(p) + (tok * p.H + h) * D;
+        float* dst = partial_o(p) + (tok * p.H + h) * D + half * (D / 2);
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          tmem_ld32(tO + lane_off + 32 * c, r);
+        for (int c = 0; c < D / 64; ++c) {
+          tmem_ld32(tO + lane_off + half * (D / 2) + 32 * c, r);
           tmem_ld_wait(r);
           if (row_in) {
 #pragma unroll
@@ -340,13 +390,13 @@ __global__ void __launch_bounds__(kThreads, 1)
               *reinterpret_cast<uint4*>(dst + 32 * c + e) = make_uint4(r[e], r[e + 1], r[e + 2], r[e + 3]);
           }
         }
-        if (row_in) partial_ml(p)[tok * p.H + h] = make_float2(m_run, l_run);
+        if (row_in && half == 0) partial_ml(p)[tok * p.H + h] = make_float2(m_run, l_tot);
       } else {
-        const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
-        T* dst = static_cast<T*>(p.out) + (tok * p.H + h) * D;
+        const float inv = l_tot > 0.f ? 1.f / l_tot : 0.f;
+        T* dst = static_cast<T*>(p.out) + (tok * p.H + h) * D + half * (D / 2);
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          tmem_ld32(tO + lane_off + 32 * c, r);
+        for (int c = 0; c < D / 64; ++c) {
+          tmem_ld32(tO + lane_off + half * (D / 2) + 32 * c, r);
           tmem_ld_wait(r);
           if (row_out) {
             uint32_t w[16];
