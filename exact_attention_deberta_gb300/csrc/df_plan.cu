@@ -16,7 +16,6 @@ namespace dfa {
 namespace {
 
 constexpr int kPlanThreads = 256;
-constexpr int kScalarBlocks = 1216;  // 8 x 152 SMs, grid-stride over tokens
 
 // ---- a1: one entry of the index table, plus the two saturation points -------
 // r_sat_pos = smallest r with idx(r) = 2 span - 1, r_sat_neg = largest r with
@@ -38,47 +37,57 @@ __device__ void index_entry(const Problem& p, int e) {
 // ---- per-token position scalars (far tiles) and zeroing of padded rows -------
 // scal[h][0..3][t] = kscale * {Q_t.PK[0], Q_t.PK[top], K_t.PQ[0], K_t.PQ[top]}.
 // A masked (or out-of-range) key gets -inf in both K terms and in keybias.
+// One thread per (head, token); a block covers 256 tokens of one head and keeps
+// that head's four position rows in shared memory.
 template <typename T>
-__device__ void scalar_token(const Problem& p, int t, int lane) {
+__device__ void scalar_block(const Problem& p, int blk) {
+  __shared__ float rows[4][128];
   const int H = p.H, d = p.d, top = 2 * p.span - 1;
-  const bool in_range = t < p.T;
-  const bool valid = in_range && (p.packed || p.key_mask[t] != 0);
-  const T* q = static_cast<const T*>(p.q);
-  const T* k = static_cast<const T*>(p.k);
+  const int tiles = (p.t_pad + kPlanThreads - 1) / kPlanThreads;
+  const int h = blk / tiles;
+  const int t = (blk % tiles) * kPlanThreads + threadIdx.x;
   const T* pk = static_cast<const T*>(p.pk);
   const T* pq = static_cast<const T*>(p.pq);
-  if (lane == 0) p.keybias[t] = valid ? 0.f : -INFINITY;
-  for (int h = 0; h < H; ++h) {
-    float a0 = 0.f, a1 = 0.f, b0 = 0.f, b1 = 0.f;
-    if (valid) {
-      const size_t row = ((size_t)t * H + h) * d;
-      for (int e = lane; e < d; e += 32) {
-        const float qv = IO<T>::load(q + row + e);
-        const float kv = IO<T>::load(k + row + e);
-        a0 = fmaf(qv, IO<T>::load(pk + ((size_t)0 * H + h) * d + e), a0);
-        a1 = fmaf(qv, IO<T>::load(pk + ((size_t)top * H + h) * d + e), a1);
-        b0 = fmaf(kv, IO<T>::load(pq + ((size_t)0 * H + h) * d + e), b0);
-        b1 = fmaf(kv, IO<T>::load(pq + ((size_t)top * H + h) * d + e), b1);
-      }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        a0 += __shfl_xor_sync(0xffffffffu, a0, o);
-        a1 += __shfl_xor_sync(0xffffffffu, a1, o);
-        b0 += __shfl_xor_sync(0xffffffffu, b0, o);
-        b1 += __shfl_xor_sync(0xffffffffu, b1, o);
-      }
-    } else if (in_range) {
-      T* out = static_cast<T*>(p.out) + ((size_t)t * H + h) * d;
-      for (int e = lane; e < d; e += 32) out[e] = IO<T>::from_f(0.f);
-    }
-    if (lane == 0) {
-      const size_t base = (size_t)h * 4 * p.t_pad + t;
-      p.scal[base + 0 * (size_t)p.t_pad] = valid ? a0 * p.kscale : 0.f;
-      p.scal[base + 1 * (size_t)p.t_pad] = valid ? a1 * p.kscale : 0.f;
-      p.scal[base + 2 * (size_t)p.t_pad] = valid ? b0 * p.kscale : -INFINITY;
-      p.scal[base + 3 * (size_t)p.t_pad] = valid ? b1 * p.kscale : -INFINITY;
-    }
+  for (int e = threadIdx.x; e < 4 * d; e += kPlanThreads) {
+    const int which = e / d, c = e % d;
+    const T* src = which < 2 ? pk : pq;
+    const int prow = (which & 1) ? top : 0;
+    rows[which][c] = IO<T>::load(src + ((size_t)prow * H + h) * d + c);
   }
+  __syncthreads();
+  if (t >= p.t_pad) return;
+  const bool in_range = t < p.T;
+  const bool valid = in_range && (p.packed || p.key_mask[t] != 0);
+  if (h == 0) p.keybias[t] = valid ? 0.f : -INFINITY;
+  float a0 = 0.f, a1 = 0.f, b0 = 0.f, b1 = 0.f;
+  const size_t row = ((size_t)t * H + h) * d;
+  if (valid) {
+    constexpr int kVec = 16 / sizeof(T);
+    const uint4* q4 = reinterpret_cast<const uint4*>(static_cast<const T*>(p.q) + row);
+    const uint4* k4 = reinterpret_cast<const uint4*>(static_cast<const T*>(p.k) + row);
+    for (int v = 0; v < d / kVec; ++v) {
+      const uint4 qv = q4[v], kv = k4[v];
+      const T* qe = reinterpret_cast<const T*>(&qv);
+      const T* ke = reinterpret_cast<const T*>(&kv);
+#pragma unroll
+      for (int e = 0; e < kVec; ++e) {
+        const int c = v * kVec + e;
+        const float qf = IO<T>::to_f(qe[e]), kf = IO<T>::to_f(ke[e]);
+        a0 = fmaf(qf, rows[0][c], a0);
+        a1 = fmaf(qf, rows[1][c], a1);
+        b0 = fmaf(kf, rows[2][c], b0);
+        b1 = fmaf(kf, rows[3][c], b1);
+      }
+    }
+  } else if (in_range) {
+    uint4* o4 = reinterpret_cast<uint4*>(static_cast<T*>(p.out) + row);
+    for (int v = 0; v < d * (int)sizeof(T) / 16; ++v) o4[v] = make_uint4(0u, 0u, 0u, 0u);
+  }
+  const size_t base = (size_t)h * 4 * p.t_pad + t;
+  p.scal[base + 0 * (size_t)p.t_pad] = valid ? a0 * p.kscale : 0.f;
+  p.scal[base + 1 * (size_t)p.t_pad] = valid ? a1 * p.kscale : 0.f;
+  p.scal[base + 2 * (size_t)p.t_pad] = valid ? b0 * p.kscale : -INFINITY;
+  p.scal[base + 3 * (size_t)p.t_pad] = valid ? b1 * p.kscale : -INFINITY;
 }
 
 // ---- a2: work list ------------------------------------------------------------
@@ -134,20 +143,18 @@ __device__ void build_worklist(const Problem& p) {
 }
 
 template <typename T>
-__global__ void __launch_bounds__(kPlanThreads) plan_kernel(Problem p, int nb_table) {
-  const int bid = blockIdx.x;
+__global__ void __launch_bounds__(kPlanThreads) plan_kernel(Problem p, int nb_table, int nb_scal) {
+  if (blockIdx.x == 0) {  // the single work-list block starts first
+    build_worklist(p);
+    return;
+  }
+  const int bid = blockIdx.x - 1;
   if (bid < nb_table) {
     const int e = bid * kPlanThreads + threadIdx.x;
     if (e < 2 * p.lt - 1) index_entry(p, e);
     return;
   }
-  if (bid < nb_table + kScalarBlocks) {
-    const int warp = (bid - nb_table) * (kPlanThreads / 32) + threadIdx.x / 32;
-    const int nwarps = kScalarBlocks * (kPlanThreads / 32);
-    for (int t = warp; t < p.t_pad; t += nwarps) scalar_token<T>(p, t, threadIdx.x & 31);
-    return;
-  }
-  build_worklist(p);
+  scalar_block<T>(p, bid - nb_table);
 }
 
 __global__ void __launch_bounds__(kPlanThreads)
@@ -160,11 +167,12 @@ index_table_kernel(int buckets, int max_rel, int span, int max_len, int32_t* idx
 
 cudaError_t launch_plan(const Problem& p, cudaStream_t s) {
   const int nb_table = (2 * p.lt - 1 + kPlanThreads - 1) / kPlanThreads;
-  const int grid = nb_table + kScalarBlocks + 1;
+  const int nb_scal = p.H * ((p.t_pad + kPlanThreads - 1) / kPlanThreads);
+  const int grid = nb_table + nb_scal + 1;
   switch (p.dtype) {
-    case DF_BF16: plan_kernel<__nv_bfloat16><<<grid, kPlanThreads, 0, s>>>(p, nb_table); break;
-    case DF_FP16: plan_kernel<__half><<<grid, kPlanThreads, 0, s>>>(p, nb_table); break;
-    default: plan_kernel<float><<<grid, kPlanThreads, 0, s>>>(p, nb_table); break;
+    case DF_BF16: plan_kernel<__nv_bfloat16><<<grid, kPlanThreads, 0, s>>>(p, nb_table, nb_scal); break;
+    case DF_FP16: plan_kernel<__half><<<grid, kPlanThreads, 0, s>>>(p, nb_table, nb_scal); break;
+    default: plan_kernel<float><<<grid, kPlanThreads, 0, s>>>(p, nb_table, nb_scal); break;
   }
   return cudaGetLastError();
 }

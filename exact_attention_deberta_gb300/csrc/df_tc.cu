@@ -197,7 +197,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     int tab_next = fetch_tab(jlo);
     float col_next = fetch_col(jlo);
     for (int jb = jlo; jb < jhi; ++jb) {
-      const int j0 = jb * kTile;
       if (tid < 2 * kTile - 1) sTab[tid] = tab_next;
       if (tid < kTile) sCol[tid] = col_next;
       int lo_next = 0, hi_next = 0;
@@ -230,13 +229,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 
       float x[64];
       {
-        uint32_t r[32];
+        uint32_t r0[32], r1[32];
+        tmem_ld32(tS + lane_off + 64 * half, r0);
+        tmem_ld32(tS + lane_off + 64 * half + 32, r1);
+        tmem_ld_wait2(r0, r1);
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          tmem_ld32(tS + lane_off + 64 * half + 32 * c, r);
-          tmem_ld_wait(r);
-#pragma unroll
-          for (int e = 0; e < 32; ++e) x[32 * c + e] = __uint_as_float(r[e]);
+        for (int e = 0; e < 32; ++e) {
+          x[e] = __uint_as_float(r0[e]);
+          x[32 + e] = __uint_as_float(r1[e]);
         }
       }
 

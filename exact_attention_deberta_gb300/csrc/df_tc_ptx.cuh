@@ -43,6 +43,18 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
+// Non-blocking test of a phase (never suspends the thread, unlike try_wait).
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
 // Waits for the phase with the given parity to complete; false after `budget`
 // SM cycles without completion.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
@@ -180,6 +192,22 @@ __device__ __forceinline__ void tmem_ld_wait(uint32_t (&r)[32]) {
                :
                : "memory");
 }
+// One wait for several loads in flight (their latencies overlap).
+#define DFA_V8(a, b) "+r"(a[b]), "+r"(a[b + 1]), "+r"(a[b + 2]), "+r"(a[b + 3]), \
+                     "+r"(a[b + 4]), "+r"(a[b + 5]), "+r"(a[b + 6]), "+r"(a[b + 7])
+#define DFA_V32(a) DFA_V8(a, 0), DFA_V8(a, 8), DFA_V8(a, 16), DFA_V8(a, 24)
+__device__ __forceinline__ void tmem_ld_wait2(uint32_t (&a)[32], uint32_t (&b)[32]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" : DFA_V32(a), DFA_V32(b) : : "memory");
+}
+__device__ __forceinline__ void tmem_ld_wait4(uint32_t (&a)[32], uint32_t (&b)[32],
+                                              uint32_t (&c)[32], uint32_t (&d)[32]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : DFA_V32(a), DFA_V32(b), DFA_V32(c), DFA_V32(d)
+               :
+               : "memory");
+}
+#undef DFA_V8
+#undef DFA_V32
 __device__ __forceinline__ void tmem_ld_wait() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
@@ -193,6 +221,26 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
 }
 __device__ __forceinline__ void tmem_st_wait() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// 32 lanes x 32 bit, 16 consecutive columns
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : DFA_R8(0), DFA_R8(8)
+      : "r"(taddr)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_ld_wait(uint32_t (&r)[16]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" : DFA_U8(0), DFA_U8(8) : : "memory");
+}
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+      DFA_W8(0), DFA_W8(8)
+      : "memory");
 }
 
 #undef DFA_R8
