@@ -32,11 +32,50 @@ constexpr unsigned long long kDefaultWaitBudget = 1ull << 31;
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 struct Layout {
-  size_t header, idx, items, seqs, scal, keybias, partial, total;
-  int max_items, t_pad, lt;
+  size_t header, idx, items, seqs, scal, keybias, partial, diag_pk, diag_pq, total;
+  int max_items, t_pad, lt, n_diag, diag_m0;
 };
 
-Layout make_layout(int B, int H, int L, int d) {
+// Host copy of the bucket function (double precision, as on the device); used
+// only to size the diagonal tables.
+int host_rel_index(int r, int buckets, int max_rel, int span) {
+  int b = r;
+  if (buckets > 0) {
+    const int mid = buckets / 2;
+    const int a = r < 0 ? -r : r;
+    if (a > mid) {
+      const double f = log((double)a / (double)mid) / log((double)(max_rel - 1) / (double)mid);
+      const int g = (int)ceil(f * (double)(mid - 1)) + mid;
+      b = r < 0 ? -g : g;
+    }
+  }
+  const int u = b + span;
+  return u < 0 ? 0 : (u > 2 * span - 1 ? 2 * span - 1 : u);
+}
+
+int floor_div(int a, int b) { return a >= 0 ? a / b : -((-a + b - 1) / b); }
+
+// Tile offsets m = query block - key block that can hold a near tile: the tile's
+// distances [128 m - 127, 128 m + 127] are not all saturated.  One offset of
+// slack on each side absorbs a last-ulp difference between host and device logs.
+void near_offsets(int L, int buckets, int max_rel, int span, int lt, int* m0, int* n) {
+  const int top = 2 * span - 1;
+  int rsp = lt + kQBlock, rsn = -(lt + kQBlock);
+  for (int r = 0; r < lt; ++r)
+    if (host_rel_index(r, buckets, max_rel, span) == top) { rsp = r; break; }
+  for (int r = 0; r > -lt; --r)
+    if (host_rel_index(r, buckets, max_rel, span) == 0) { rsn = r; break; }
+  const int nkb = (L + kKBlock - 1) / kKBlock;
+  // strict range: floor((rsn - 127) / 128) + 1 .. ceil((rsp + 127) / 128) - 1
+  int lo = floor_div(rsn - 127, 128);
+  int hi = -floor_div(-(rsp + 127), 128);
+  lo = lo < -(nkb - 1) ? -(nkb - 1) : lo;
+  hi = hi > nkb - 1 ? nkb - 1 : hi;
+  *m0 = lo;
+  *n = hi >= lo ? hi - lo + 1 : 0;
+}
+
+Layout make_layout(int B, int H, int L, int d, int buckets, int max_rel, int span) {
   Layout l{};
   l.lt = ((L + 127) / 128) * 128 + 128;
   const size_t T = (size_t)B * L;
@@ -57,6 +96,12 @@ Layout make_layout(int B, int H, int L, int d) {
   off = align256(off + (size_t)l.t_pad * sizeof(float));
   l.partial = off;
   off = align256(off + T * H * (size_t)(d + 2) * sizeof(float));
+  if (d == 64) near_offsets(L, buckets, max_rel, span, l.lt, &l.diag_m0, &l.n_diag);
+  const size_t diag_bytes = (size_t)l.n_diag * 256 * H * d * 2;
+  l.diag_pk = off;
+  off = align256(off + diag_bytes);
+  l.diag_pq = off;
+  off = align256(off + diag_bytes);
   l.total = off;
   return l;
 }
@@ -91,7 +136,7 @@ df_status build_problem(const void* q, const void* k, const void* v, const void*
   if (!aligned16(q) || !aligned16(k) || !aligned16(pk) || !aligned16(pq) || !aligned16(out) ||
       (need_v && !aligned16(v)))
     return DF_ERR_ALIGNMENT;
-  const Layout lay = make_layout(B, H, L, d);
+  const Layout lay = make_layout(B, H, L, d, buckets, max_rel, span);
   if (!ws || ws_bytes < lay.total) return DF_ERR_WORKSPACE;
   if (((uintptr_t)ws & 255) != 0) return DF_ERR_ALIGNMENT;
   char* base = static_cast<char*>(ws);
@@ -113,6 +158,10 @@ df_status build_problem(const void* q, const void* k, const void* v, const void*
   P.max_items = lay.max_items;
   P.t_pad = lay.t_pad;
   P.lt = lay.lt;
+  P.diag_pk = base + lay.diag_pk;
+  P.diag_pq = base + lay.diag_pq;
+  P.n_diag = lay.n_diag;
+  P.diag_m0 = lay.diag_m0;
   const unsigned long long wb = g_wait_budget.load();
   P.wait_budget = wb ? wb : kDefaultWaitBudget;
   return DF_OK;
@@ -142,7 +191,7 @@ df_status df_attn_supported(int H, int L, int d, df_dtype dtype, int buckets, in
 
 size_t df_attn_workspace_size(int B, int H, int L, int d, int buckets, int max_rel, int span) {
   if (B < 0 || check_params(H, L, d, DF_BF16, buckets, max_rel, span) != DF_OK) return 0;
-  return make_layout(B, H, L, d).total;
+  return make_layout(B, H, L, d, buckets, max_rel, span).total;
 }
 
 df_status df_attn_workspace_layout(int B, int H, int L, int d, int buckets, int max_rel, int span,
@@ -150,7 +199,7 @@ df_status df_attn_workspace_layout(int B, int H, int L, int d, int buckets, int 
   if (!layout || B < 0) return DF_ERR_INVALID_ARG;
   const df_status st = check_params(H, L, d, DF_BF16, buckets, max_rel, span);
   if (st != DF_OK) return st;
-  const Layout l = make_layout(B, H, L, d);
+  const Layout l = make_layout(B, H, L, d, buckets, max_rel, span);
   layout->header = l.header;
   layout->idx_table = l.idx;
   layout->items = l.items;
@@ -161,6 +210,10 @@ df_status df_attn_workspace_layout(int B, int H, int L, int d, int buckets, int 
   layout->max_items = l.max_items;
   layout->t_pad = l.t_pad;
   layout->table_half = l.lt;
+  layout->diag_pk = l.diag_pk;
+  layout->diag_pq = l.diag_pq;
+  layout->n_diag = l.n_diag;
+  layout->diag_m0 = l.diag_m0;
   return DF_OK;
 }
 

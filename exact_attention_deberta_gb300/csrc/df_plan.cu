@@ -142,8 +142,28 @@ __device__ void build_worklist(const Problem& p) {
   }
 }
 
+// ---- diagonal position tables (near tiles of the d = 64 tensor-core kernel) ----
+// For tile offset m and diagonal t, row (m - diag_m0) * 256 + t of each table is
+// the PK (PQ) row at idx(128 m - 127 + t): with them the position products of a
+// near tile come out of the MMA already indexed by diagonal.  One thread copies
+// 16 bytes of one row.
+__device__ void diag_chunk(const Problem& p, int g) {
+  const int cpr = p.H * p.d * 2 / 16;  // 16-byte chunks per row (16-bit types)
+  const int rows = p.n_diag * 256;
+  const int chunk = g % cpr;
+  const int row = (g / cpr) % rows;
+  const int which = g / (cpr * rows);
+  if (which >= 2) return;
+  const int m = p.diag_m0 + row / 256;
+  const int u = rel_index(128 * m - 127 + row % 256, p.buckets, p.max_rel, p.span);
+  const uint4* src = static_cast<const uint4*>(which ? p.pq : p.pk);
+  uint4* dst = static_cast<uint4*>(which ? p.diag_pq : p.diag_pk);
+  dst[(size_t)row * cpr + chunk] = src[(size_t)u * cpr + chunk];
+}
+
 template <typename T>
-__global__ void __launch_bounds__(kPlanThreads) plan_kernel(Problem p, int nb_table, int nb_scal) {
+__global__ void __launch_bounds__(kPlanThreads)
+    plan_kernel(Problem p, int nb_table, int nb_scal, int nb_diag) {
   if (blockIdx.x == 0) {  // the single work-list block starts first
     build_worklist(p);
     return;
@@ -154,7 +174,11 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(Problem p, int nb_ta
     if (e < 2 * p.lt - 1) index_entry(p, e);
     return;
   }
-  scalar_block<T>(p, bid - nb_table);
+  if (bid < nb_table + nb_scal) {
+    scalar_block<T>(p, bid - nb_table);
+    return;
+  }
+  diag_chunk(p, (bid - nb_table - nb_scal) * kPlanThreads + threadIdx.x);
 }
 
 __global__ void __launch_bounds__(kPlanThreads)
@@ -168,11 +192,19 @@ index_table_kernel(int buckets, int max_rel, int span, int max_len, int32_t* idx
 cudaError_t launch_plan(const Problem& p, cudaStream_t s) {
   const int nb_table = (2 * p.lt - 1 + kPlanThreads - 1) / kPlanThreads;
   const int nb_scal = p.H * ((p.t_pad + kPlanThreads - 1) / kPlanThreads);
-  const int grid = nb_table + nb_scal + 1;
+  // diagonal tables: 16-bit I/O types only (the strict-fp32 kernel does not use them)
+  const long long diag_chunks =
+      p.dtype == DF_FP32 ? 0 : 2LL * p.n_diag * 256 * (p.H * p.d * 2 / 16);
+  const int nb_diag = (int)((diag_chunks + kPlanThreads - 1) / kPlanThreads);
+  const int grid = nb_table + nb_scal + nb_diag + 1;
   switch (p.dtype) {
-    case DF_BF16: plan_kernel<__nv_bfloat16><<<grid, kPlanThreads, 0, s>>>(p, nb_table, nb_scal); break;
-    case DF_FP16: plan_kernel<__half><<<grid, kPlanThreads, 0, s>>>(p, nb_table, nb_scal); break;
-    default: plan_kernel<float><<<grid, kPlanThreads, 0, s>>>(p, nb_table, nb_scal); break;
+    case DF_BF16:
+      plan_kernel<__nv_bfloat16><<<grid, kPlanThreads, 0, s>>>(p, nb_table, nb_scal, nb_diag);
+      break;
+    case DF_FP16:
+      plan_kernel<__half><<<grid, kPlanThreads, 0, s>>>(p, nb_table, nb_scal, nb_diag);
+      break;
+    default: plan_kernel<float><<<grid, kPlanThreads, 0, s>>>(p, nb_table, nb_scal, nb_diag); break;
   }
   return cudaGetLastError();
 }

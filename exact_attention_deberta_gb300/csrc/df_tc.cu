@@ -491,10 +491,18 @@ cudaError_t launch_tc(const Problem& p, cudaStream_t s, cudaEvent_t ev0, cudaEve
       !encode_rows(&maps.pk, p.pk, 2LL * p.span, row, bf16) ||
       !encode_rows(&maps.pq, p.pq, 2LL * p.span, row, bf16))
     return cudaErrorInvalidValue;
+  if (p.d == 64) {
+    if (p.n_diag < 1 || !encode_rows(&maps.dpk, p.diag_pk, 256LL * p.n_diag, row, bf16) ||
+        !encode_rows(&maps.dpq, p.diag_pq, 256LL * p.n_diag, row, bf16))
+      return cudaErrorInvalidValue;
+  } else {
+    maps.dpk = maps.pk;
+    maps.dpq = maps.pq;
+  }
   if (ev0) cudaEventRecord(ev0, s);
   cudaError_t e;
   if (p.d == 64)
-    e = bf16 ? launch_near_typed<64, true>(p, maps, s) : launch_near_typed<64, false>(p, maps, s);
+    e = launch_near64(p, maps, s);
   else
     e = bf16 ? launch_near_typed<128, true>(p, maps, s) : launch_near_typed<128, false>(p, maps, s);
   if (e == cudaSuccess) e = launch_far(p, maps, s);

@@ -13,6 +13,7 @@ constexpr unsigned long long kDrainBudget = 1ull << 31;
 
 struct TcMaps {
   CUtensorMap q, k, v, pk, pq;
+  CUtensorMap dpk, dpq;  // diagonal position tables (d = 64)
 };
 
 // K step ks (16 elements) of a K-major 128-row tile stored as 64-column,
@@ -57,5 +58,32 @@ __device__ __forceinline__ float ex2(float x) {
 }
 
 cudaError_t launch_far(const Problem& p, const TcMaps& maps, cudaStream_t s);
+cudaError_t launch_near64(const Problem& p, const TcMaps& maps, cudaStream_t s);
+
+// Bounded wait that also gives up as soon as another role of the CTA has
+// aborted.  On a timeout it records DF_ERR_DEVICE_TIMEOUT and raises the CTA's
+// abort flag.  Callers keep their control flow identical after a failure (no
+// early exit), so that warp-collective instructions and named barriers stay
+// matched.
+__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity,
+                                              unsigned long long budget, volatile int* abort,
+                                              df_ws_header* hdr, int where) {
+  if (*abort) return false;
+  if (ptx::mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  for (;;) {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    if (*abort) return false;
+    if ((unsigned long long)(clock64() - t0) > budget) {
+      *abort = 1;
+      raise_device_error(hdr, DF_ERR_DEVICE_TIMEOUT, where);
+      return false;
+    }
+  }
+}
+
+__device__ __forceinline__ void named_sync(int id, int count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
 
 }  // namespace dfa

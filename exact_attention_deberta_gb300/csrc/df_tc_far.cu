@@ -54,31 +54,6 @@ struct FarSmem {
   static constexpr uint32_t alloc = bytes + 1024;
 };
 
-// Bounded wait that also gives up as soon as another role has aborted.  On a
-// timeout it records DF_ERR_DEVICE_TIMEOUT and raises the CTA's abort flag.
-// Callers keep their control flow identical after a failure (no early exit), so
-// that warp-collective instructions and named barriers stay matched.
-__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity,
-                                              unsigned long long budget, volatile int* abort,
-                                              df_ws_header* hdr, int where) {
-  if (*abort) return false;
-  if (mbar_try_wait(bar, parity)) return true;
-  const long long t0 = clock64();
-  for (;;) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if (*abort) return false;
-    if ((unsigned long long)(clock64() - t0) > budget) {
-      *abort = 1;
-      raise_device_error(hdr, DF_ERR_DEVICE_TIMEOUT, where);
-      return false;
-    }
-  }
-}
-
-__device__ __forceinline__ void named_sync(int id, int count) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
-}
-
 struct ItemGeom {
   int start, n, h, i0, nkb, jlo, jhi, nt;
   __device__ __forceinline__ int block_of(int t) const { return t < jlo ? t : jhi + (t - jlo); }

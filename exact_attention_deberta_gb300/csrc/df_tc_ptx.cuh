@@ -276,6 +276,26 @@ __device__ __forceinline__ float2 mul2(float2 a, float2 b) {
   return d;
 }
 
+// 16-bit shared-memory access at a 32-bit shared address.
+__device__ __forceinline__ void sts16(uint32_t addr, uint16_t v) {
+  asm volatile("st.shared.b16 [%0], %1;" ::"r"(addr), "h"(v) : "memory");
+}
+__device__ __forceinline__ uint16_t lds16(uint32_t addr) {
+  uint16_t v;
+  asm volatile("ld.shared.b16 %0, [%1];" : "=h"(v) : "r"(addr) : "memory");
+  return v;
+}
+// fp32 -> fp16, round to nearest even, clamped to the finite range.
+__device__ __forceinline__ uint16_t f16_satfinite(float x) {
+  uint16_t v;
+  asm("cvt.rn.satfinite.f16.f32 %0, %1;" : "=h"(v) : "f"(x));
+  return v;
+}
+// fp32 value of the fp16 sum a + b.
+__device__ __forceinline__ float f16_sum_f32(uint16_t a, uint16_t b) {
+  return __half2float(__hadd(__ushort_as_half(a), __ushort_as_half(b)));
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);

@@ -6,6 +6,7 @@ import ctypes
 import os
 import re
 
+import numpy as np
 import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
@@ -70,6 +71,31 @@ def test_workspace_size_and_layout(binding):
     assert lay["max_items"] == 16 * 12 * 64
     assert lay["table_half"] == 8192 + 128
     assert binding.df_attn_workspace_size(16, 12, 8192, 48) == 0
+
+
+@pytest.mark.parametrize("buckets,max_rel,span,L", [
+    (256, 512, 256, 8192), (256, 512, 256, 300), (0, 512, 512, 2048), (64, 128, 64, 1000),
+    (8, 16, 8, 100), (256, 4096, 256, 65536)])
+def test_diagonal_table_range(binding, buckets, max_rel, span, L):
+    """The diagonal tables cover every tile offset m whose distances
+    [128 m - 127, 128 m + 127] are not all saturated (checked with the oracle's
+    index function), with at most one offset of slack on each side."""
+    from oracle import rel_index
+    lay = binding.df_attn_workspace_layout(3, 4, L, 64, buckets=buckets, max_rel=max_rel, span=span)
+    nkb = (L + 127) // 128
+    top = 2 * span - 1
+    near = []
+    for m in range(-(nkb - 1), nkb):
+        u = rel_index(np.arange(128 * m - 127, 128 * m + 128), buckets, max_rel, span)
+        if not (np.all(u == top) or np.all(u == 0)):
+            near.append(m)
+    m0, n = lay["diag_m0"], lay["n_diag"]
+    assert m0 <= min(near) and m0 + n - 1 >= max(near)
+    assert n <= len(near) + 2
+    rows = n * 256 * 4 * 64 * 2
+    assert lay["diag_pq"] - lay["diag_pk"] >= rows and lay["total"] - lay["diag_pq"] >= rows
+    assert binding.df_attn_workspace_layout(3, 4, L, 128, buckets=buckets, max_rel=max_rel,
+                                            span=span)["n_diag"] == 0
 
 
 def _fwd_raw(binding, **over):

@@ -89,6 +89,33 @@ def test_plan_worklist_and_scalars(lib, name):
         assert torch.all(o == 0)
 
 
+@pytest.mark.parametrize("name", ["v3base_padded_bf16", "packed_varlen_h12d64"])
+def test_plan_diagonal_tables(lib, name):
+    """Row (m - diag_m0) * 256 + t of the diagonal tables is PK / PQ at
+    idx(128 m - 127 + t), byte for byte."""
+    x = synth.make_inputs(name)
+    dev = {n: None if getattr(x, n) is None else getattr(x, n).cuda()
+           for n in ("q", "k", "pk", "pq", "key_mask", "cu_seqlens")}
+    kw = dict(buckets=x.w.buckets, max_rel=x.w.max_rel, span=x.w.span)
+    if x.w.layout == "padded":
+        _, ws = lib.df_attn_plan(dev["q"], dev["k"], dev["pk"], dev["pq"], key_mask=dev["key_mask"], **kw)
+        B, L = x.key_mask.shape
+    else:
+        _, ws = lib.df_attn_plan(dev["q"], dev["k"], dev["pk"], dev["pq"], cu_seqlens=dev["cu_seqlens"],
+                                 max_seqlen=x.w.L, **kw)
+        B, L = x.cu_seqlens.numel() - 1, x.w.L
+    torch.cuda.synchronize()
+    lay = lib.df_attn_workspace_layout(B, x.w.H, L, x.w.d, **kw)
+    n, m0 = lay["n_diag"], lay["diag_m0"]
+    assert n > 0
+    r = (128 * (m0 + np.arange(n))[:, None] - 127 + np.arange(256)[None, :]).reshape(-1)
+    u = torch.from_numpy(rel_index(r, **kw).astype(np.int64))
+    for name_t, src in (("diag_pk", x.pk), ("diag_pq", x.pq)):
+        got = _read_ws(ws, lay, name_t, torch.int16, n * 256 * x.w.H * x.w.d).view(n * 256, x.w.H, x.w.d)
+        want = src.view(torch.int16)[u]
+        assert torch.equal(got, want), name_t
+
+
 FULL = ["tiny_fp32", "tiny_fp32_pad97", "v3base_padded_bf16", "v2xl_heavypad_fp16"]
 
 
