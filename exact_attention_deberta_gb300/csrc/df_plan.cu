@@ -145,20 +145,29 @@ __device__ void build_worklist(const Problem& p) {
 // ---- diagonal position tables (near tiles of the d = 64 tensor-core kernel) ----
 // For tile offset m and diagonal t, row (m - diag_m0) * 256 + t of each table is
 // the PK (PQ) row at idx(128 m - 127 + t): with them the position products of a
-// near tile come out of the MMA already indexed by diagonal.  One thread copies
-// 16 bytes of one row.
-__device__ void diag_chunk(const Problem& p, int g) {
-  const int cpr = p.H * p.d * 2 / 16;  // 16-byte chunks per row (16-bit types)
+// near tile come out of the MMA already indexed by diagonal.  A block copies
+// kDiagRows rows of one table in 16-byte pieces; their source rows are looked
+// up once.
+constexpr int kDiagRows = 8;
+
+__device__ void diag_rows(const Problem& p, int blk) {
+  __shared__ int src_row[kDiagRows];
+  const int cpr = p.H * p.d * 2 / 16;  // 16-byte pieces per row (16-bit types)
   const int rows = p.n_diag * 256;
-  const int chunk = g % cpr;
-  const int row = (g / cpr) % rows;
-  const int which = g / (cpr * rows);
-  if (which >= 2) return;
-  const int m = p.diag_m0 + row / 256;
-  const int u = rel_index(128 * m - 127 + row % 256, p.buckets, p.max_rel, p.span);
+  const int which = blk / (rows / kDiagRows);
+  const int row0 = (blk % (rows / kDiagRows)) * kDiagRows;
+  if (threadIdx.x < kDiagRows) {
+    const int row = row0 + threadIdx.x;
+    const int m = p.diag_m0 + row / 256;
+    src_row[threadIdx.x] = rel_index(128 * m - 127 + row % 256, p.buckets, p.max_rel, p.span);
+  }
+  __syncthreads();
   const uint4* src = static_cast<const uint4*>(which ? p.pq : p.pk);
   uint4* dst = static_cast<uint4*>(which ? p.diag_pq : p.diag_pk);
-  dst[(size_t)row * cpr + chunk] = src[(size_t)u * cpr + chunk];
+  for (int e = threadIdx.x; e < kDiagRows * cpr; e += kPlanThreads) {
+    const int r = e / cpr, c = e % cpr;
+    dst[(size_t)(row0 + r) * cpr + c] = src[(size_t)src_row[r] * cpr + c];
+  }
 }
 
 template <typename T>
@@ -178,7 +187,7 @@ __global__ void __launch_bounds__(kPlanThreads)
     scalar_block<T>(p, bid - nb_table);
     return;
   }
-  diag_chunk(p, (bid - nb_table - nb_scal) * kPlanThreads + threadIdx.x);
+  diag_rows(p, bid - nb_table - nb_scal);
 }
 
 __global__ void __launch_bounds__(kPlanThreads)
@@ -193,9 +202,7 @@ cudaError_t launch_plan(const Problem& p, cudaStream_t s) {
   const int nb_table = (2 * p.lt - 1 + kPlanThreads - 1) / kPlanThreads;
   const int nb_scal = p.H * ((p.t_pad + kPlanThreads - 1) / kPlanThreads);
   // diagonal tables: 16-bit I/O types only (the strict-fp32 kernel does not use them)
-  const long long diag_chunks =
-      p.dtype == DF_FP32 ? 0 : 2LL * p.n_diag * 256 * (p.H * p.d * 2 / 16);
-  const int nb_diag = (int)((diag_chunks + kPlanThreads - 1) / kPlanThreads);
+  const int nb_diag = p.dtype == DF_FP32 ? 0 : 2 * p.n_diag * 256 / kDiagRows;
   const int grid = nb_table + nb_scal + nb_diag + 1;
   switch (p.dtype) {
     case DF_BF16:

@@ -22,6 +22,13 @@ __device__ __forceinline__ uint64_t kmajor_desc(const uint8_t* tile, int ks) {
   return ptx::sdesc_sw128(ptx::smem_u32(tile + (ks >> 2) * kBoxBytes + (ks & 3) * 32), 16, 1024);
 }
 
+// Offset of K step ks from step 0 in a descriptor's 16-byte address field, so
+// that the descriptors of one tile are a base plus compile-time constants.
+__host__ __device__ constexpr uint64_t kmajor_step(int ks) {
+  return (uint64_t)(((ks >> 2) * kBoxBytes + (ks & 3) * 32) >> 4);
+}
+__host__ __device__ constexpr uint64_t vtile_step(int ks) { return (uint64_t)(ks * 2048 >> 4); }
+
 // K step ks (16 key rows) of a 128-row V tile used as the MN-major B operand of
 // P.V: 16 rows x 128 B = 2048 B per step, 64-column boxes kBoxBytes apart.
 __device__ __forceinline__ uint64_t vtile_desc(uint32_t v_addr, int ks) {

@@ -9,12 +9,16 @@
 // bias:  x_ij = (Q_i.K_j) * log2(e)/sqrt(3d) + alpha_i + beta_j.
 //
 // Warp roles of one CTA (one CTA per SM, persistent over the work list):
-//   warp 0      TMA producer: Q of the item (two buffers, so the next item's Q
-//               lands while the current one finishes), then K and V of every
-//               far tile into a ring of shared-memory stages;
-//   warp 1      tcgen05.mma issuer: S = Q.K^T into one of two TMEM score
-//               buffers, then O_b += P.V with P read back from TMEM;
-//   warps 2-3   idle (they complete the control warpgroup);
+//   warp 0      TMA producer of Q (two buffers, so the next item's Q lands
+//               while the current one finishes) and of K for every far tile;
+//   warp 2      TMA producer of V; K and V have separate stage barriers, a K
+//               stage is free once its QK has completed, a V stage once its
+//               P.V has, so K loads run further ahead;
+//   warp 1      tcgen05.mma issuer of S = Q.K^T into one of two TMEM score
+//               buffers (and, at d = 128, of the P.V products too);
+//   warp 3      at d = 64 the issuer of O_b += P.V with P read back from TMEM,
+//               so that QK never queues behind a blocking P.V issue; idle at
+//               d = 128;
 //   warps 4-7   softmax warpgroup 0: even far tiles, accumulator O_0;
 //   warps 8-11  softmax warpgroup 1: odd far tiles, accumulator O_1.
 // The control warpgroup gives registers back (setmaxnreg) so that each softmax
@@ -43,12 +47,12 @@ struct FarSmem {
   static constexpr uint32_t kTileBytes = kChunks * kBoxBytes;
   static constexpr uint32_t q = 0;                                   // [2][Q tile]
   static constexpr uint32_t kv = q + 2 * kTileBytes;                 // [stage][K | V]
-  static constexpr uint32_t beta = kv + kStages * 2 * kTileBytes;    // float [2 wg][2][128]
-  static constexpr uint32_t ml = beta + 2 * 2 * 128 * 4;             // float4 [2 wg][128]
+  static constexpr uint32_t beta = kv + kStages * 2 * kTileBytes;    // float [8 warps][128]
+  static constexpr uint32_t ml = beta + 8 * 128 * 4;                 // float4 [2 wg][128]
   static constexpr uint32_t bars = ml + 2 * 128 * 16;
-  // q_full[2], q_empty[2], kv_full[S], kv_empty[S], s_full[2], p_full[2], o_final, drain,
-  // s_cons[2], pv_done[2]
-  static constexpr int kBars = 4 + 2 * kStages + 2 + 2 + 2 + 4;
+  // q_full[2], q_empty[2], k_full[S], k_empty[S], v_full[S], v_empty[S], s_full[2],
+  // p_full[2], o_final, drain[2], s_cons[2], pv_done[2]
+  static constexpr int kBars = 4 + 4 * kStages + 2 + 2 + 3 + 4;
   static constexpr uint32_t misc = bars + kBars * 8;                 // abort flag, tmem slot
   static constexpr uint32_t bytes = misc + 16;
   static constexpr uint32_t alloc = bytes + 1024;
@@ -92,13 +96,15 @@ __global__ void __launch_bounds__(kFarThreads, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + SL::bars);
   uint64_t* q_full = bars;
   uint64_t* q_empty = bars + 2;
-  uint64_t* kv_full = bars + 4;
-  uint64_t* kv_empty = bars + 4 + S;
-  uint64_t* s_full = bars + 4 + 2 * S;
+  uint64_t* k_full = bars + 4;
+  uint64_t* k_empty = bars + 4 + S;      // K(t) read: QK(t) has completed
+  uint64_t* v_full = bars + 4 + 2 * S;
+  uint64_t* v_empty = bars + 4 + 3 * S;  // V(t) read: P(t).V has completed
+  uint64_t* s_full = bars + 4 + 4 * S;
   uint64_t* p_full = s_full + 2;
   uint64_t* o_final = p_full + 2;
-  uint64_t* drain = o_final + 1;
-  uint64_t* s_cons = drain + 1;   // softmax has read S(t) into registers
+  uint64_t* drain = o_final + 1;         // [2]: one per MMA-issuing thread
+  uint64_t* s_cons = drain + 2;   // softmax has read S(t) into registers
   uint64_t* pv_done = s_cons + 2; // P(t).V has completed
   volatile int* s_abort = reinterpret_cast<volatile int*>(sm + SL::misc);
   uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + SL::misc + 4);
@@ -109,16 +115,14 @@ __global__ void __launch_bounds__(kFarThreads, 1)
       mbar_init(q_full + b, 1);
       mbar_init(q_empty + b, 1);
     }
-    for (int s = 0; s < S; ++s) {
-      mbar_init(kv_full + s, 1);
-      mbar_init(kv_empty + s, 1);
-    }
+    for (int s = 0; s < 4 * S; ++s) mbar_init(k_full + s, 1);
     for (int b = 0; b < 2; ++b) {
       mbar_init(s_full + b, 1);
       mbar_init(p_full + b, 4);
     }
     mbar_init(o_final, 1);
     mbar_init(drain, 1);
+    mbar_init(drain + 1, 1);
     for (int b = 0; b < 2; ++b) {
       mbar_init(s_cons + b, 4);
       mbar_init(pv_done + b, 1);
@@ -137,46 +141,56 @@ __global__ void __launch_bounds__(kFarThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tslot;
-  const uint32_t tS[2] = {tmem, tmem + 128};
-  const uint32_t tO[2] = {tmem + 256, tmem + 256 + D};
+  // TMEM columns of buffer b
+  const uint32_t tSa[2] = {tmem, tmem + 128};
+  const uint32_t tOa[2] = {tmem + 256, tmem + 256 + D};
+  auto tS = [&](int b) { return tSa[b]; };
+  auto tO = [&](int b) { return tOa[b]; };
   // d = 64 leaves room for a P buffer per warpgroup, so that S can be refilled
   // as soon as the softmax has read it; at d = 128 P overwrites its S buffer.
   constexpr bool kSepP = D == 64;
-  const uint32_t tP[2] = {kSepP ? tmem + 384 : tS[0], kSepP ? tmem + 448 : tS[1]};
+  const uint32_t tPa[2] = {kSepP ? tmem + 384 : tSa[0], kSepP ? tmem + 448 : tSa[1]};
+  auto tP = [&](int b) { return tPa[b]; };
 
   const int n_items = p.hdr->n_items;
   const int rsp = p.hdr->r_sat_pos, rsn = p.hdr->r_sat_neg;
   const unsigned long long budget = p.wait_budget;
   df_ws_header* hdr = p.hdr;
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ TMA producer
+  if (warp == 0 || warp == 2) {
+    // ------------------------------------------------------------ TMA producers
+    // warp 0: Q of every item and K of every far tile; warp 2: V.  K stages are
+    // released when QK has read them, V stages when P.V has, so K runs ahead.
     setmaxnreg_dec<56>();
     if (lane == 0) {
+      const bool is_k = warp == 0;
+      uint64_t* full = is_k ? k_full : v_full;
+      uint64_t* empty = is_k ? k_empty : v_empty;
+      const uint32_t off = is_k ? 0u : SL::kTileBytes;
+      const CUtensorMap* map = is_k ? &maps.k : &maps.v;
       uint32_t g = 0, qc = 0, g_issued = 0, q_issued = 0;  // loads are issued in order
       for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
         const ItemGeom ig = item_geom(p, it, rsp, rsn);
         if (ig.nt == 0) continue;
-        const int qb = qc & 1;
-        if (wait_or_abort(q_empty + qb, ((qc >> 1) & 1) ^ 1, budget, s_abort, hdr, 301)) {
-          mbar_expect_tx(q_full + qb, SL::kTileBytes);
-          for (int c = 0; c < kChunks; ++c)
-            tma_load_2d(sQ + qb * SL::kTileBytes + c * kBoxBytes, &maps.q, ig.h * D + c * 64,
-                        ig.start + ig.i0, q_full + qb);
-          q_issued = qc + 1;
+        if (is_k) {
+          const int qb = qc & 1;
+          if (wait_or_abort(q_empty + qb, ((qc >> 1) & 1) ^ 1, budget, s_abort, hdr, 301)) {
+            mbar_expect_tx(q_full + qb, SL::kTileBytes);
+            for (int c = 0; c < kChunks; ++c)
+              tma_load_2d(sQ + qb * SL::kTileBytes + c * kBoxBytes, &maps.q, ig.h * D + c * 64,
+                          ig.start + ig.i0, q_full + qb);
+            q_issued = qc + 1;
+          }
+          ++qc;
         }
-        ++qc;
         for (int t = 0; t < ig.nt; ++t, ++g) {
           const int s = g % S;
           const int row = ig.start + ig.block_of(t) * 128;
-          if (wait_or_abort(kv_empty + s, ((g / S) & 1) ^ 1, budget, s_abort, hdr, 302)) {
-            uint8_t* st = sKV + s * 2 * SL::kTileBytes;
-            mbar_expect_tx(kv_full + s, 2 * SL::kTileBytes);
-            for (int c = 0; c < kChunks; ++c) {
-              tma_load_2d(st + c * kBoxBytes, &maps.k, ig.h * D + c * 64, row, kv_full + s);
-              tma_load_2d(st + SL::kTileBytes + c * kBoxBytes, &maps.v, ig.h * D + c * 64, row,
-                          kv_full + s);
-            }
+          if (wait_or_abort(empty + s, ((g / S) & 1) ^ 1, budget, s_abort, hdr, is_k ? 302 : 303)) {
+            uint8_t* st = sKV + s * 2 * SL::kTileBytes + off;
+            mbar_expect_tx(full + s, SL::kTileBytes);
+            for (int c = 0; c < kChunks; ++c)
+              tma_load_2d(st + c * kBoxBytes, map, ig.h * D + c * 64, row, full + s);
             g_issued = g + 1;
           }
         }
@@ -184,15 +198,23 @@ __global__ void __launch_bounds__(kFarThreads, 1)
       // no copy may still be landing when the CTA leaves: wait for the last load
       // issued into every stage and into both Q buffers
       for (uint32_t k = g_issued > (uint32_t)S ? g_issued - S : 0; k < g_issued; ++k)
-        mbar_wait(kv_full + k % S, (k / S) & 1, kDrainBudget);
+        mbar_wait(full + k % S, (k / S) & 1, kDrainBudget);
       for (uint32_t k = q_issued > 2 ? q_issued - 2 : 0; k < q_issued; ++k)
         mbar_wait(q_full + (k & 1), (k >> 1) & 1, kDrainBudget);
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
+  } else if (warp == 1 || (kSepP && warp == 3)) {
+    // ------------------------------------------------------------ MMA issuers
+    // d = 64: warp 1 issues S = Q.K^T, warp 3 issues O += P.V, so that neither
+    // chain waits behind the other's blocking issue; every commit is made by the
+    // thread whose MMAs it covers.  d = 128 (P overwrites S): warp 1 issues both
+    // in order.
     setmaxnreg_dec<56>();
     if (lane == 0) {
-      uint32_t g = 0, qc = 0, pc[2] = {0, 0}, cc[2] = {0, 0};
+      const bool qk_role = warp == 1;
+      const bool pv_role = warp == 3 || !kSepP;
+      uint32_t g = 0, qc = 0;
+      uint32_t pbits = 0, cbits = 0;  // bit b: parity of the next p_full[b] / s_cons[b] phase
+      uint32_t s_used = 0;            // bit b: score buffer b has been written before
       const uint32_t kv_addr = smem_u32(sKV);
       for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
         const ItemGeom ig = item_geom(p, it, rsp, rsn);
@@ -200,49 +222,56 @@ __global__ void __launch_bounds__(kFarThreads, 1)
         const bool has_partial = ig.jhi > ig.jlo;
         const int qb = qc & 1;
         const uint8_t* sQb = sQ + qb * SL::kTileBytes;
-        const bool q_ok = wait_or_abort(q_full + qb, (qc >> 1) & 1, budget, s_abort, hdr, 311);
+        const bool q_ok = qk_role && wait_or_abort(q_full + qb, (qc >> 1) & 1, budget, s_abort, hdr, 311);
         ++qc;
         auto issue_qk = [&](int t) {
           const uint32_t gs = g + t;
           const int s = gs % S;
-          const bool ok = wait_or_abort(kv_full + s, (gs / S) & 1, budget, s_abort, hdr, 312);
+          const bool ok = wait_or_abort(k_full + s, (gs / S) & 1, budget, s_abort, hdr, 312);
           if (ok && q_ok) {
+            const uint64_t dq = kmajor_desc(sQb, 0);
+            const uint64_t dk = kmajor_desc(sKV + s * 2 * SL::kTileBytes, 0);
             tc_fence_after();
-            const uint8_t* kt = sKV + s * 2 * SL::kTileBytes;
 #pragma unroll
             for (int k = 0; k < D / 16; ++k)
-              mma_ss(tS[t & 1], kmajor_desc(sQb, k), kmajor_desc(kt, k), kIdescQK, k > 0);
+              mma_ss(tS(t & 1), dq + kmajor_step(k), dk + kmajor_step(k), kIdescQK, k > 0);
             mma_commit(s_full + (t & 1));
+            mma_commit(k_empty + s);
           }
         };
         auto issue_pv = [&](int t) {
           const int b = t & 1;
-          const bool ok = wait_or_abort(p_full + b, pc[b] & 1, budget, s_abort, hdr, 313);
-          ++pc[b];
+          const uint32_t gs = g + t;
+          const int s = gs % S;
+          bool ok = wait_or_abort(p_full + b, (pbits >> b) & 1, budget, s_abort, hdr, 313);
+          pbits ^= 1u << b;
+          ok = wait_or_abort(v_full + s, (gs / S) & 1, budget, s_abort, hdr, 315) && ok;
           if (ok) {
+            const uint64_t dv = vtile_desc(kv_addr + s * 2 * SL::kTileBytes + SL::kTileBytes, 0);
             tc_fence_after();
-            const int s = (g + t) % S;
-            const uint32_t v_addr = kv_addr + s * 2 * SL::kTileBytes + SL::kTileBytes;
             const bool carry = (t >= 2) || (b == 0 && has_partial);
 #pragma unroll
             for (int k = 0; k < 128 / 16; ++k)
-              mma_ts(tO[b], tP[b] + 8 * k, vtile_desc(v_addr, k), kIdescPV,
-                     (k > 0 || carry) ? 1u : 0u);
-            mma_commit(kv_empty + s);
+              mma_ts(tO(b), tP(b) + 8 * k, dv + vtile_step(k), kIdescPV, (k > 0 || carry) ? 1u : 0u);
+            mma_commit(v_empty + s);
             if (kSepP) mma_commit(pv_done + b);
           }
         };
         if (kSepP) {
-          // QK(t + 2) goes out as soon as warpgroup t % 2 has read S(t)
-          for (int t = 0; t < ig.nt && t < 2; ++t) issue_qk(t);
-          for (int t = 0; t < ig.nt; ++t) {
-            if (t + 2 < ig.nt) {
+          if (qk_role) {
+            // QK(t) goes out as soon as warpgroup t % 2 has read the score
+            // buffer's previous contents (also across items)
+            for (int t = 0; t < ig.nt; ++t) {
               const int b = t & 1;
-              wait_or_abort(s_cons + b, cc[b] & 1, budget, s_abort, hdr, 314);
-              ++cc[b];
-              issue_qk(t + 2);
+              if (s_used & (1u << b)) {
+                wait_or_abort(s_cons + b, (cbits >> b) & 1, budget, s_abort, hdr, 314);
+                cbits ^= 1u << b;
+              }
+              s_used |= 1u << b;
+              issue_qk(t);
             }
-            issue_pv(t);
+          } else {
+            for (int t = 0; t < ig.nt; ++t) issue_pv(t);
           }
         } else {
           // P overwrites S: QK(t) can only follow PV(t - 2)
@@ -252,13 +281,14 @@ __global__ void __launch_bounds__(kFarThreads, 1)
           }
         }
         g += ig.nt;
-        mma_commit(q_empty + qb);
-        mma_commit(o_final);
+        if (qk_role) mma_commit(q_empty + qb);
+        if (pv_role) mma_commit(o_final);
       }
-      mma_commit(drain);
-      mbar_wait(drain, 0, kDrainBudget);
+      uint64_t* my_drain = drain + (warp == 3 ? 1 : 0);
+      mma_commit(my_drain);
+      mbar_wait(my_drain, 0, kDrainBudget);
     }
-  } else if (warp < 4) {
+  } else if (warp == 3) {  // d = 128: idle
     setmaxnreg_dec<56>();
   } else {
     // ------------------------------------------------------------ softmax warpgroups
@@ -266,10 +296,9 @@ __global__ void __launch_bounds__(kFarThreads, 1)
     const int wg = (warp - 4) >> 2;          // 0 or 1
     const int quad = warp & 3;               // TMEM lane quadrant of this warp
     const int row = quad * 32 + lane;        // query row inside the block
-    const int tid_wg = threadIdx.x - 128 - 128 * wg;
     const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
     const float ks = p.kscale;
-    float* beta_buf = sBeta + wg * 256;
+    float* bw = sBeta + (warp - 4) * 128;  // this warp's copy of the tile's key terms
     uint32_t sc = 0, ic = 0, own = 0;
     for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
       const ItemGeom ig = item_geom(p, it, rsp, rsn);
@@ -304,61 +333,72 @@ __global__ void __launch_bounds__(kFarThreads, 1)
             r[e + 2] = __float_as_uint(v.z);
             r[e + 3] = __float_as_uint(v.w);
           }
-          tmem_st32(tO[0] + lane_off + 32 * c, r);
+          tmem_st32(tO(0) + lane_off + 32 * c, r);
         }
         tmem_st_wait();
         o_has = true;
       }
-      // beta of a tile: one value per thread, shared through shared memory
-      auto beta_of = [&](int t) -> float {
-        const int j = ig.block_of(t) * 128 + tid_wg;
-        if (j >= ig.n) return -INFINITY;
-        return scal_h[(ig.pos_side(t) ? 3 : 2) * (size_t)p.t_pad + ig.start + j];
+      // key terms beta_j of a tile, four per lane (keys 4 lane .. 4 lane + 3);
+      // every warp stages its own copy, so no warp waits for another
+      auto beta_of = [&](int t) -> float4 {
+        const int j0 = ig.block_of(t) * 128 + 4 * lane;
+        const float* src = scal_h + (ig.pos_side(t) ? 3 : 2) * (size_t)p.t_pad + ig.start;
+        float v[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) v[e] = j0 + e < ig.n ? src[j0 + e] : -INFINITY;
+        return make_float4(v[0], v[1], v[2], v[3]);
       };
-      // beta values are fetched two own tiles ahead of their use
-      float beta_n1 = wg < ig.nt ? beta_of(wg) : 0.f;
-      float beta_n2 = wg + 2 < ig.nt ? beta_of(wg + 2) : 0.f;
+      float4 beta_next = wg < ig.nt ? beta_of(wg) : make_float4(0.f, 0.f, 0.f, 0.f);
       const float2 ks2 = make_float2(ks, ks);
       for (int t = wg; t < ig.nt; t += 2, ++own) {
-        float* bb = beta_buf + (own & 1) * 128;
-        bb[tid_wg] = beta_n1;
-        named_sync(1 + wg, 128);
-        beta_n1 = beta_n2;
-        if (t + 4 < ig.nt) beta_n2 = beta_of(t + 4);
+        __syncwarp();  // every lane has finished reading the previous tile's copy
+        *reinterpret_cast<float4*>(bw + 4 * lane) = beta_next;
+        __syncwarp();
+        if (t + 2 < ig.nt) beta_next = beta_of(t + 2);
         wait_or_abort(s_full + wg, sc & 1, budget, s_abort, hdr, 321);
         ++sc;
         tc_fence_after();
         float x[128];
         {
-          uint32_t r[32];
+          uint32_t r0[32], r1[32], r2[32], r3[32];
+          tmem_ld32(tS(wg) + lane_off, r0);
+          tmem_ld32(tS(wg) + lane_off + 32, r1);
+          tmem_ld32(tS(wg) + lane_off + 64, r2);
+          tmem_ld32(tS(wg) + lane_off + 96, r3);
+          tmem_ld_wait4(r0, r1, r2, r3);
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            tmem_ld32(tS[wg] + lane_off + 32 * c, r);
-            tmem_ld_wait(r);
-#pragma unroll
-            for (int e = 0; e < 32; ++e) x[32 * c + e] = __uint_as_float(r[e]);
+          for (int e = 0; e < 32; ++e) {
+            x[e] = __uint_as_float(r0[e]);
+            x[32 + e] = __uint_as_float(r1[e]);
+            x[64 + e] = __uint_as_float(r2[e]);
+            x[96 + e] = __uint_as_float(r3[e]);
           }
         }
-        if (kSepP && t + 2 < ig.nt) {  // S(t) is in registers: the MMA may refill it
+        if (kSepP) {  // S(t) is in registers: the MMA may refill the buffer
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(s_cons + wg);
         }
         const float alpha = ig.pos_side(t) ? a_pos : a_neg;
-        float mt0 = -INFINITY, mt1 = -INFINITY;
+        // logits in log2 units; eight independent maximum chains
+        float mx[8];
+#pragma unroll
+        for (int a = 0; a < 8; ++a) mx[a] = -INFINITY;
 #pragma unroll
         for (int j = 0; j < 128; j += 4) {
-          const float4 bv = *reinterpret_cast<const float4*>(bb + j);
+          const float4 bv = *reinterpret_cast<const float4*>(bw + j);
           const float2 y0 = fma2(make_float2(x[j], x[j + 1]), ks2, make_float2(bv.x, bv.y));
           const float2 y1 = fma2(make_float2(x[j + 2], x[j + 3]), ks2, make_float2(bv.z, bv.w));
           x[j] = y0.x;
           x[j + 1] = y0.y;
           x[j + 2] = y1.x;
           x[j + 3] = y1.y;
-          mt0 = fmaxf(mt0, fmaxf(y0.x, y0.y));
-          mt1 = fmaxf(mt1, fmaxf(y1.x, y1.y));
+          const int a = (j >> 2) & 3;
+          mx[2 * a] = fmaxf(mx[2 * a], fmaxf(y0.x, y0.y));
+          mx[2 * a + 1] = fmaxf(mx[2 * a + 1], fmaxf(y1.x, y1.y));
         }
-        const float mt = fmaxf(mt0, mt1) + alpha;
+        const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                               fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) + alpha;
         float scale = 1.f;
         const bool rebase = mt > m_run + 8.f;
         if (rebase) {
@@ -373,19 +413,22 @@ __global__ void __launch_bounds__(kFarThreads, 1)
         const float2 nshift = make_float2(-shift, -shift);
         {
           uint32_t r[32];
-          float2 acc = make_float2(0.f, 0.f);
+          float2 acc[4];  // four independent sum chains
+#pragma unroll
+          for (int a = 0; a < 4; ++a) acc[a] = make_float2(0.f, 0.f);
 #pragma unroll
           for (int c = 0; c < 2; ++c) {
 #pragma unroll
             for (int e = 0; e < 32; ++e) {
               const float2 z = add2(make_float2(x[64 * c + 2 * e], x[64 * c + 2 * e + 1]), nshift);
               const float2 pp = make_float2(ex2(z.x), ex2(z.y));
-              acc = add2(acc, pp);
+              acc[e & 3] = add2(acc[e & 3], pp);
               r[e] = BF16 ? pack_bf16x2(pp.x, pp.y) : pack_f16x2(pp.x, pp.y);
             }
-            tmem_st32(tP[wg] + lane_off + 32 * c, r);
+            tmem_st32(tP(wg) + lane_off + 32 * c, r);
           }
-          l_run += acc.x + acc.y;
+          const float2 s01 = add2(acc[0], acc[1]), s23 = add2(acc[2], acc[3]);
+          l_run += (s01.x + s23.x) + (s01.y + s23.y);
         }
         // rescale O after the scores are dead (fewer live registers); P(t).V has
         // not been issued yet, so O still holds the tiles before t
@@ -393,11 +436,11 @@ __global__ void __launch_bounds__(kFarThreads, 1)
           uint32_t r[32];
 #pragma unroll
           for (int c = 0; c < D / 32; ++c) {
-            tmem_ld32(tO[wg] + lane_off + 32 * c, r);
+            tmem_ld32(tO(wg) + lane_off + 32 * c, r);
             tmem_ld_wait(r);
 #pragma unroll
             for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * scale);
-            tmem_st32(tO[wg] + lane_off + 32 * c, r);
+            tmem_st32(tO(wg) + lane_off + 32 * c, r);
           }
         }
         tmem_st_wait();
@@ -430,8 +473,8 @@ __global__ void __launch_bounds__(kFarThreads, 1)
       for (int c = 0; c < D / 64; ++c) {
         const int col = wg * (D / 2) + 32 * c;
         uint32_t ra[32], rb[32];
-        tmem_ld32(tO[0] + lane_off + col, ra);
-        tmem_ld32(tO[1] + lane_off + col, rb);
+        tmem_ld32(tO(0) + lane_off + col, ra);
+        tmem_ld32(tO(1) + lane_off + col, rb);
         tmem_ld_wait(ra);
         tmem_ld_wait(rb);
         if (store) {

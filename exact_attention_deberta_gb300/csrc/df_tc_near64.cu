@@ -21,9 +21,9 @@
 //     Pw[j'][i']     = P[j'][t]  with i' = t - 127 + j'
 // so element (i', j') reads Cw[127 - j'][i'] and Pw[j'][i'].  Both stores and
 // loads are 16-bit and bank-conflict free (row strides 262 and 258 bytes).  The
-// terms are stored already scaled to log2 units, rounded to fp16 (saturating);
-// the upper triangle j' >= i' needs only the first half, so it is summed while
-// the second half is in the tensor core.
+// terms are rounded to fp16 (saturating) and scaled to log2 units when they
+// are added; the upper triangle j' >= i' needs only the first half, so it is
+// summed while the second half is in the tensor core.
 //
 // Roles (one CTA per SM, persistent over the work list):
 //   warps 0-15  compute: warp w owns TMEM lanes 32 (w % 4) .. +31 (query rows
@@ -56,8 +56,8 @@ constexpr int kTile = 128;
 constexpr int kComputeWarps = 16;
 constexpr int kComputeThreads = kComputeWarps * 32;
 constexpr int kThreads = kComputeThreads + 32;
-constexpr uint32_t kCwStride = 262;  // bytes per Cw row (128 fp16 + 6 B)
-constexpr uint32_t kPwStride = 258;  // bytes per Pw row (128 fp16 + 2 B)
+constexpr int kCwRow = 131;  // fp16 elements per Cw row (262 B: conflict-free skew)
+constexpr int kPwRow = 129;  // fp16 elements per Pw row (258 B)
 
 struct Smem {
   static constexpr uint32_t q = 0;                       // Q tile
@@ -66,8 +66,8 @@ struct Smem {
   static constexpr uint32_t e1 = e0 + 2 * kBoxBytes;     // diagonal rows 128-255: PK | PQ
   static constexpr uint32_t v = e1 + 2 * kBoxBytes;      // V tiles [2]
   static constexpr uint32_t cw = v + 2 * kBoxBytes;      // fp16 [128][131]
-  static constexpr uint32_t pw = cw + 128 * kCwStride;   // fp16 [128][129]
-  static constexpr uint32_t col = pw + 128 * kPwStride;  // float [2][128] key bias
+  static constexpr uint32_t pw = cw + 128 * kCwRow * 2;  // fp16 [128][129]
+  static constexpr uint32_t col = pw + 128 * kPwRow * 2; // float [2][128] key bias
   static constexpr uint32_t red = col + 2 * 128 * 4;     // float [4][128]
   static constexpr uint32_t bars = red + 4 * 128 * 4;
   static constexpr int kBars = 15;
@@ -152,6 +152,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t q_n = 0, k_n = 0, e0_n = 0, e1_n = 0, v_n = 0;
       uint32_t q_w = 0, k_w = 0, e0_w = 0, e1_w = 0, v_w = 0;
       uint32_t ph_c1 = 0, ph_c2 = 0, ph_c3 = 0, ph_d0 = 0, ph_d1 = 0, ph_pr = 0;
+      // step-0 descriptors of the fixed buffers (K steps add kmajor_step)
+      const uint64_t dq = kmajor_desc(sQ, 0);
+      const uint64_t de0k = kmajor_desc(sE0, 0), de0q = kmajor_desc(sE0 + kBoxBytes, 0);
+      const uint64_t de1k = kmajor_desc(sE1, 0), de1q = kmajor_desc(sE1 + kBoxBytes, 0);
       for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
         const int4 item = p.items[it];
         const int start = item.x, n = item.y, h = item.z, ib = item.w;
@@ -216,17 +220,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t kbuf0 = k_n & 1;  // buffer of tile 0's K (tiles alternate)
         const uint32_t vbuf0 = v_n & 1;
         auto issue_mma1 = [&](int t) {
-          const uint8_t* kt = sK + ((kbuf0 + t) & 1) * kBoxBytes;
+          const uint64_t dk = kmajor_desc(sK + ((kbuf0 + t) & 1) * kBoxBytes, 0);
           tc_fence_after();
 #pragma unroll
           for (int k = 0; k < kD / 16; ++k)
-            mma_ss(tS, kmajor_desc(sQ, k), kmajor_desc(kt, k), kIdescQK, k > 0);
+            mma_ss(tS, dq + kmajor_step(k), dk + kmajor_step(k), kIdescQK, k > 0);
 #pragma unroll
           for (int k = 0; k < kD / 16; ++k)
-            mma_ss(tA, kmajor_desc(sQ, k), kmajor_desc(sE0, k), kIdescQK, k > 0);
+            mma_ss(tA, dq + kmajor_step(k), de0k + kmajor_step(k), kIdescQK, k > 0);
 #pragma unroll
           for (int k = 0; k < kD / 16; ++k)
-            mma_ss(tB, kmajor_desc(kt, k), kmajor_desc(sE0 + kBoxBytes, k), kIdescQK, k > 0);
+            mma_ss(tB, dk + kmajor_step(k), de0q + kmajor_step(k), kIdescQK, k > 0);
           mma_commit(bar_c1);
         };
 
@@ -254,14 +258,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = wait_ph(bar_d0, ph_d0, 274);
           ok = wait_e(1, 275) && ok;
           if (ok) {
-            const uint8_t* kt = sK + ((kbuf0 + t) & 1) * kBoxBytes;
+            const uint64_t dk = kmajor_desc(sK + ((kbuf0 + t) & 1) * kBoxBytes, 0);
             tc_fence_after();
 #pragma unroll
             for (int k = 0; k < kD / 16; ++k)
-              mma_ss(tA, kmajor_desc(sQ, k), kmajor_desc(sE1, k), kIdescQK, k > 0);
+              mma_ss(tA, dq + kmajor_step(k), de1k + kmajor_step(k), kIdescQK, k > 0);
 #pragma unroll
             for (int k = 0; k < kD / 16; ++k)
-              mma_ss(tB, kmajor_desc(kt, k), kmajor_desc(sE1 + kBoxBytes, k), kIdescQK, k > 0);
+              mma_ss(tB, dk + kmajor_step(k), de1q + kmajor_step(k), kIdescQK, k > 0);
             mma_commit(bar_c2);
           }
           // (3) K(t) and diagonal half 1 are free; tile t + 1's first MMAs go out
@@ -279,11 +283,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = wait_ph(bar_pr, ph_pr, 280);
           ok = wait_v(281) && ok;
           if (ok) {
-            const uint32_t v_a = smem_u32(sV + ((vbuf0 + t) & 1) * kBoxBytes);
+            const uint64_t dv = vtile_desc(smem_u32(sV + ((vbuf0 + t) & 1) * kBoxBytes), 0);
             tc_fence_after();
 #pragma unroll
             for (int k = 0; k < kTile / 16; ++k)
-              mma_ts(tO, tP + 8 * k, vtile_desc(v_a, k), kIdescPV, (t > 0 || k > 0) ? 1u : 0u);
+              mma_ts(tO, tP + 8 * k, dv + vtile_step(k), kIdescPV, (t > 0 || k > 0) ? 1u : 0u);
             mma_commit(bar_c3);
           }
           // (5) V(t)'s buffer takes V(t + 2) once P(t).V is done
@@ -307,13 +311,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int rho = qd * 32 + lane;      // TMEM lane: query row (S, C, O) or key row (P)
     const uint32_t lane_off = (uint32_t)(qd * 32) << 16;
     const float ks = p.kscale;
-    const uint32_t cw_a = smem_u32(sm + SL::cw), pw_a = smem_u32(sm + SL::pw);
+    // 32-bit shared addresses of the fp16 buffers (row strides kCwRow, kPwRow elements)
+    const uint32_t cw = smem_u32(sm + SL::cw), pw = smem_u32(sm + SL::pw);
     // drain: C[rho][t] -> Cw[t - rho][rho];  P[rho][t] -> Pw[rho][t - 127 + rho]
-    const uint32_t dC = cw_a + 2u * rho - kCwStride * rho;            // + kCwStride * t
-    const uint32_t dP = pw_a + (kPwStride + 2u) * rho - 254u;          // + 2 t
+    const uint32_t dC = cw - 2u * (kCwRow - 1) * rho;         // + 2 kCwRow t
+    const uint32_t dP = pw + 2u * (kPwRow + 1) * rho - 254u;   // + 2 t
     // gather of element (rho, j' = 32 g + jj): Cw[127 - j'][rho] and Pw[j'][rho]
-    const uint32_t gC = cw_a + 127u * kCwStride + 2u * rho - kCwStride * 32u * g;  // - kCwStride jj
-    const uint32_t gP = pw_a + 2u * rho + kPwStride * 32u * g;                     // + kPwStride jj
+    const uint32_t gC = cw + 2u * (kCwRow * (96 - 32 * g) + rho);  // + 2 kCwRow (31 - jj)
+    const uint32_t gP = pw + 2u * (kPwRow * 32 * g + rho);          // + 2 kPwRow jj
 
     uint32_t ph_c1 = 0, ph_c2 = 0, ph_c3 = 0, gt = 0;
     auto wait_ph = [&](uint64_t* bar, uint32_t& ph, int where) {
@@ -321,27 +326,39 @@ __global__ void __launch_bounds__(kThreads, 1)
       ph ^= 1;
       return ok;
     };
-    // drain one 32-column chunk: side 0 = C (A columns), 1 = P (B columns)
-    auto drain = [&](int side, int t0) {
+    // Drain the 32 columns t0 .. t0 + 31 of A (side 0, C) or B (side 1, P) as
+    // fp16.  Only the chunk on the window's edge needs a per-lane test.
+    auto drain = [&](int side, int t0, bool edge) {
       uint32_t r[32];
       tmem_ld32((side ? tB : tA) + lane_off + (t0 & 127), r);
       tmem_ld_wait(r);
       if (side == 0) {
-        const uint32_t base = dC + kCwStride * (uint32_t)t0;
+        const uint32_t dst = dC + 2u * kCwRow * t0;
+        if (!edge) {
 #pragma unroll
-        for (int e = 0; e < 32; ++e)
-          if ((unsigned)(t0 + e - rho) < 128u)
-            sts16(base + kCwStride * e, f16_satfinite(__uint_as_float(r[e]) * ks));
+          for (int e = 0; e < 32; ++e) sts16(dst + 2 * kCwRow * e, f16_satfinite(__uint_as_float(r[e])));
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e)
+            if ((unsigned)(t0 + e - rho) < 128u)
+              sts16(dst + 2 * kCwRow * e, f16_satfinite(__uint_as_float(r[e])));
+        }
       } else {
-        const uint32_t base = dP + 2u * (uint32_t)t0;
+        const uint32_t dst = dP + 2u * t0;
+        if (!edge) {
 #pragma unroll
-        for (int e = 0; e < 32; ++e)
-          if ((unsigned)(t0 + e - 127 + rho) < 128u)
-            sts16(base + 2 * e, f16_satfinite(__uint_as_float(r[e]) * ks));
+          for (int e = 0; e < 32; ++e) sts16(dst + 2 * e, f16_satfinite(__uint_as_float(r[e])));
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e)
+            if ((unsigned)(t0 + e - 127 + rho) < 128u)
+              sts16(dst + 2 * e, f16_satfinite(__uint_as_float(r[e])));
+        }
       }
     };
     // the five chunks a lane quarter needs from one half, shared by its 4 warps
     //   half 0: C chunks qd..3, P chunks 3-qd..3;  half 1: C chunks 0..qd, P chunks 0..3-qd
+    //   the edge chunks: C chunk qd and P chunk 3 - qd of either half
     auto drain_half = [&](int half) {
       for (int item = g; item < 5; item += 4) {
         int side, c;
@@ -352,7 +369,25 @@ __global__ void __launch_bounds__(kThreads, 1)
           side = item <= qd ? 0 : 1;
           c = side == 0 ? item : item - (qd + 1);
         }
-        drain(side, 128 * half + 32 * c);
+        drain(side, 128 * half + 32 * c, c == (side == 0 ? qd : 3 - qd));
+      }
+    };
+    // Add the position terms of this thread's 32 elements: the upper triangle
+    // j' >= rho (first halves) or the lower one (second halves).  Whole 32 x 32
+    // blocks off the diagonal belong to one triangle.
+    auto gather = [&](float (&x)[32], bool upper) {
+      const bool all = upper ? g > qd : g < qd;
+      if (all) {
+#pragma unroll
+        for (int jj = 0; jj < 32; ++jj)
+          x[jj] = fmaf(f16_sum_f32(lds16(gC + 2 * kCwRow * (31 - jj)), lds16(gP + 2 * kPwRow * jj)),
+                       ks, x[jj]);
+      } else if (g == qd) {
+#pragma unroll
+        for (int jj = 0; jj < 32; ++jj)
+          if ((jj >= lane) == upper)
+            x[jj] = fmaf(f16_sum_f32(lds16(gC + 2 * kCwRow * (31 - jj)), lds16(gP + 2 * kPwRow * jj)),
+                         ks, x[jj]);
       }
     };
 
@@ -403,11 +438,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(bar_d0);
         named_sync(1, kComputeThreads);
-        // upper triangle (t <= 127): first halves only
-#pragma unroll
-        for (int jj = 0; jj < 32; ++jj)
-          if (32 * g + jj >= rho)
-            x[jj] += f16_sum_f32(lds16(gC - kCwStride * jj), lds16(gP + kPwStride * jj));
+        gather(x, true);
         // ---- second halves
         wait_ph(bar_c2, ph_c2, 291);
         tc_fence_after();
@@ -416,10 +447,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(bar_d1);
         named_sync(1, kComputeThreads);
-#pragma unroll
-        for (int jj = 0; jj < 32; ++jj)
-          if (32 * g + jj < rho)
-            x[jj] += f16_sum_f32(lds16(gC - kCwStride * jj), lds16(gP + kPwStride * jj));
+        gather(x, false);
 
         // ---- online softmax (log2 units); row maximum over the four column groups
         float mt = -INFINITY;
