@@ -38,7 +38,7 @@ PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 def parse_args(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
@@ -70,6 +70,28 @@ def algorithmic_flops(lengths, H, d, span):
     return float(sum(H * (4.0 * n * n * d + 8.0 * n * span * d) for n in lengths))
 
 
+def tile_flops(lengths, H, d, span, rsp, rsn):
+    """Algorithmic flops per launch of the near-tile and far-tile kernels: Q.K^T and
+    P.V over the valid (query, key) pairs of every 128 x 128 tile (4 rows keys d),
+    split by the tile's class (far: every distance saturated, r - 127 >= r_sat_pos
+    or r + 127 <= r_sat_neg for the tile offset r); the two relative-position
+    projections (8 n span d per sequence and head) belong to the near-tile kernel."""
+    near = far = 0.0
+    for n in lengths:
+        nb = (n + 127) // 128
+        rows = [min(128, n - 128 * b) for b in range(nb)]
+        for ib in range(nb):
+            for jb in range(nb):
+                off = 128 * (ib - jb)
+                f = 4.0 * rows[ib] * rows[jb] * d
+                if off - 127 >= rsp or off + 127 <= rsn:
+                    far += f
+                else:
+                    near += f
+        near += 8.0 * n * span * d
+    return H * near, H * far
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -96,7 +118,7 @@ class ClockSampler:
             os.close(fd)
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.QUERY}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "25"],
                 stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
         except (OSError, FileNotFoundError):
             self.proc = None
@@ -265,11 +287,10 @@ def main(argv=None):
     assert binding.df_attn_get_device_status(ws) == binding.DF_OK
     launches_per_step = binding.df_attn_last_launch_count()
 
-    kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(args.steps)]
-    for a, b in kev:  # torch creates the CUDA events lazily, at their first record
-        a.record(stream)
-        b.record(stream)
+    kev = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(3)) for _ in range(args.steps)]
+    for evs in kev:  # torch creates the CUDA events lazily, at their first record
+        for e in evs:
+            e.record(stream)
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if dist is not None:
         dist.barrier()
@@ -277,15 +298,20 @@ def main(argv=None):
     with ClockSampler(local) as clk:
         t0.record(stream)
         for i in range(args.steps):
-            binding.df_attn_set_profile_events(*kev[i])
+            binding.df_attn_set_profile_events(kev[i][0], kev[i][2])
+            binding.df_attn_set_profile_split(kev[i][1])
             step(dev, out)
         t1.record(stream)
         torch.cuda.synchronize()
     binding.df_attn_set_profile_events(None, None)
+    binding.df_attn_set_profile_split(None)
     if dist is not None:
         dist.barrier()
     ms = t0.elapsed_time(t1) / args.steps
-    kern_ms = sum(a.elapsed_time(b) for a, b in kev) / args.steps
+    near_ms = sum(a.elapsed_time(m) for a, m, _ in kev) / args.steps
+    far_ms = sum(m.elapsed_time(b) for _, m, b in kev) / args.steps
+    hdr = ws[:64].view(torch.int32).cpu()
+    rsp, rsn = int(hdr[3]), int(hdr[4])
     assert binding.df_attn_get_device_status(ws) == binding.DF_OK
 
     e2e = None
@@ -314,26 +340,34 @@ def main(argv=None):
         e2e = (e2e_ms, h2d, d2h)
 
     # max over ranks
-    times = torch.tensor([ms, kern_ms, e2e[0] if e2e else 0.0], dtype=torch.float64, device="cuda")
+    times = torch.tensor([ms, near_ms, far_ms, e2e[0] if e2e else 0.0], dtype=torch.float64,
+                         device="cuda")
     if dist is not None:
         dist.all_reduce(times, op=dist.ReduceOp.MAX)
-    ms, kern_ms, e2e_ms = (float(t) for t in times.cpu())
+    ms, near_ms, far_ms, e2e_ms = (float(t) for t in times.cpu())
 
     flops_rank = metric_flops(lengths, H, d)
     tokens_rank = float(sum(lengths))
     value = world * flops_rank / (ms * 1e-3) / 1e12
     peaks, peak_src = load_peaks()
     tc = x.w.dtype in ("bf16", "fp16")
-    algo = algorithmic_flops(lengths, H, d, span)
     if tc:
+        # kernels timed inside a multi-millisecond step: the sustained dense rate
+        # (fp16 has the same dense rate as bf16)
         bound, peak, unit = "tensor", float(peaks["bf16_tflops_sustained"]), "TFLOP/s"
-        if x.w.dtype == "fp16":
-            peak = float(peaks["bf16_tflops_sustained"])  # same dense rate as bf16
-        kernel_file = "df_tc.cu"
+        near_algo, far_algo = tile_flops(lengths, H, d, span, rsp, rsn)
+        near_file = "df_tc_near64.cu" if d == 64 else "df_tc.cu"
+        if far_ms >= near_ms:
+            kernel_file, kname, algo, kern_ms = "df_tc_far.cu", "tc_far_kernel", far_algo, far_ms
+            other = ("tc_near_kernel", near_algo, near_ms)
+        else:
+            kernel_file, kname, algo, kern_ms = near_file, "tc_near_kernel", near_algo, near_ms
+            other = ("tc_far_kernel", far_algo, far_ms)
     else:
         # FP32 FFMA: 152 SMs x 128 lanes x 2 flop x 2.07 GHz
         bound, peak, unit = "alu", 152 * 128 * 2 * 2.07e9 / 1e12, "TFLOP/s"
-        kernel_file = "df_simt.cu"
+        kernel_file, kname = "df_simt.cu", "simt_fwd_kernel"
+        algo, kern_ms, other = algorithmic_flops(lengths, H, d, span), far_ms, None
     achieved = algo / (kern_ms * 1e-3) / 1e12
     tr = traffic_record(kernel_file)
     line = {
@@ -359,9 +393,15 @@ def main(argv=None):
         "gpu_launches": launches_per_step * args.steps,
         "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
                      "frac": achieved / peak, "traffic": tr.get("dram_bytes_per_launch") if tr else None,
-                     "kernel_ms": kern_ms, "peak_source": peak_src if bound == "tensor" else
+                     "kernel": kname, "kernel_ms": kern_ms, "algorithmic_flops": algo,
+                     "peak_source": (peak_src + " bf16_tflops_sustained") if bound == "tensor" else
                      "derived: 152 SM x 128 FP32 lanes x 2 x 2.07 GHz"},
     }
+    if other is not None:
+        oname, oalgo, oms = other
+        line["roofline"]["other_kernel"] = {"kernel": oname, "kernel_ms": oms, "algorithmic_flops": oalgo,
+                                            "achieved": oalgo / (oms * 1e-3) / 1e12,
+                                            "frac": oalgo / (oms * 1e-3) / 1e12 / peak}
     if e2e:
         line["e2e"] = {"value": world * flops_rank / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                        "h2d_bytes_per_step": e2e[1], "d2h_bytes_per_step": e2e[2]}

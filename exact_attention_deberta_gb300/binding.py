@@ -62,6 +62,8 @@ _lib.df_attn_workspace_layout.argtypes = [_i] * 7 + [ctypes.POINTER(_Layout)]
 _lib.df_attn_workspace_layout.restype = _i
 _lib.df_attn_set_profile_events.argtypes = [_vp, _vp]
 _lib.df_attn_set_profile_events.restype = None
+_lib.df_attn_set_profile_split.argtypes = [_vp]
+_lib.df_attn_set_profile_split.restype = None
 _lib.df_attn_set_wait_budget.argtypes = [ctypes.c_ulonglong]
 _lib.df_attn_set_wait_budget.restype = None
 _lib.df_attn_last_launch_count.argtypes = []
@@ -210,6 +212,10 @@ def df_rel_index_table(buckets, max_rel, span, max_len, out=None, stream=None, d
 def df_attn_set_profile_events(start=None, stop=None):
     h = lambda e: None if e is None else ctypes.c_void_p(e.cuda_event)  # noqa: E731
     _lib.df_attn_set_profile_events(h(start), h(stop))
+
+
+def df_attn_set_profile_split(mid=None):
+    _lib.df_attn_set_profile_split(None if mid is None else ctypes.c_void_p(mid.cuda_event))
 
 
 def df_attn_set_wait_budget(cycles: int):

@@ -13,8 +13,8 @@
 #include <atomic>
 
 namespace dfa {
-cudaError_t launch_tc(const Problem& p, cudaStream_t s, cudaEvent_t ev0, cudaEvent_t ev1,
-                      int* launches);
+cudaError_t launch_tc(const Problem& p, cudaStream_t s, cudaEvent_t ev0, cudaEvent_t ev_mid,
+                      cudaEvent_t ev1, int* launches);
 bool tc_enabled();
 }  // namespace dfa
 
@@ -25,6 +25,7 @@ using namespace dfa;
 std::atomic<unsigned long long> g_wait_budget{0};
 cudaEvent_t g_prof_start = nullptr;
 cudaEvent_t g_prof_stop = nullptr;
+cudaEvent_t g_prof_mid = nullptr;
 std::atomic<int> g_last_launches{0};
 
 constexpr unsigned long long kDefaultWaitBudget = 1ull << 31;
@@ -245,9 +246,10 @@ df_status df_attn_fwd(const void* q, const void* k, const void* v, const void* p
   int launches = 0;
   cudaError_t e;
   if (dtype != DF_FP32 && tc_enabled()) {
-    e = launch_tc(p, s, g_prof_start, g_prof_stop, &launches);
+    e = launch_tc(p, s, g_prof_start, g_prof_mid, g_prof_stop, &launches);
   } else {
     if (g_prof_start) cudaEventRecord(g_prof_start, s);
+    if (g_prof_mid) cudaEventRecord(g_prof_mid, s);
     e = launch_simt(p, s, &launches);
     if (g_prof_stop) cudaEventRecord(g_prof_stop, s);
   }
@@ -283,6 +285,8 @@ void df_attn_set_profile_events(df_event_t start, df_event_t stop) {
   g_prof_start = (cudaEvent_t)start;
   g_prof_stop = (cudaEvent_t)stop;
 }
+
+void df_attn_set_profile_split(df_event_t mid) { g_prof_mid = (cudaEvent_t)mid; }
 
 void df_attn_set_wait_budget(unsigned long long cycles) { g_wait_budget.store(cycles); }
 

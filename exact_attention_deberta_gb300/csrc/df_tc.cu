@@ -479,8 +479,8 @@ cudaError_t launch_near_typed(const Problem& p, const TcMaps& maps, cudaStream_t
 
 bool tc_enabled() { return true; }
 
-cudaError_t launch_tc(const Problem& p, cudaStream_t s, cudaEvent_t ev0, cudaEvent_t ev1,
-                      int* launches) {
+cudaError_t launch_tc(const Problem& p, cudaStream_t s, cudaEvent_t ev0, cudaEvent_t ev_mid,
+                      cudaEvent_t ev1, int* launches) {
   *launches = 0;
   if (p.T == 0 || p.max_items == 0) return cudaSuccess;
   const bool bf16 = p.dtype == DF_BF16;
@@ -505,6 +505,7 @@ cudaError_t launch_tc(const Problem& p, cudaStream_t s, cudaEvent_t ev0, cudaEve
     e = launch_near64(p, maps, s);
   else
     e = bf16 ? launch_near_typed<128, true>(p, maps, s) : launch_near_typed<128, false>(p, maps, s);
+  if (ev_mid) cudaEventRecord(ev_mid, s);
   if (e == cudaSuccess) e = launch_far(p, maps, s);
   if (ev1) cudaEventRecord(ev1, s);
   *launches = 2;

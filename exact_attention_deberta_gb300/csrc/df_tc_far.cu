@@ -299,6 +299,10 @@ __global__ void __launch_bounds__(kFarThreads, 1)
     const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
     const float ks = p.kscale;
     float* bw = sBeta + (warp - 4) * 128;  // this warp's copy of the tile's key terms
+    // this warpgroup's TMEM buffers, in registers
+    const uint32_t tSw = tmem + 128u * wg + lane_off;
+    const uint32_t tPw = (kSepP ? tmem + 384u + 64u * wg : tmem + 128u * wg) + lane_off;
+    const uint32_t tOw = tmem + 256u + (uint32_t)D * wg + lane_off;
     uint32_t sc = 0, ic = 0, own = 0;
     for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
       const ItemGeom ig = item_geom(p, it, rsp, rsn);
@@ -361,10 +365,10 @@ __global__ void __launch_bounds__(kFarThreads, 1)
         float x[128];
         {
           uint32_t r0[32], r1[32], r2[32], r3[32];
-          tmem_ld32(tS(wg) + lane_off, r0);
-          tmem_ld32(tS(wg) + lane_off + 32, r1);
-          tmem_ld32(tS(wg) + lane_off + 64, r2);
-          tmem_ld32(tS(wg) + lane_off + 96, r3);
+          tmem_ld32(tSw, r0);
+          tmem_ld32(tSw + 32, r1);
+          tmem_ld32(tSw + 64, r2);
+          tmem_ld32(tSw + 96, r3);
           tmem_ld_wait4(r0, r1, r2, r3);
 #pragma unroll
           for (int e = 0; e < 32; ++e) {
@@ -425,7 +429,7 @@ __global__ void __launch_bounds__(kFarThreads, 1)
               acc[e & 3] = add2(acc[e & 3], pp);
               r[e] = BF16 ? pack_bf16x2(pp.x, pp.y) : pack_f16x2(pp.x, pp.y);
             }
-            tmem_st32(tP(wg) + lane_off + 32 * c, r);
+            tmem_st32(tPw + 32 * c, r);
           }
           const float2 s01 = add2(acc[0], acc[1]), s23 = add2(acc[2], acc[3]);
           l_run += (s01.x + s23.x) + (s01.y + s23.y);
@@ -436,11 +440,11 @@ __global__ void __launch_bounds__(kFarThreads, 1)
           uint32_t r[32];
 #pragma unroll
           for (int c = 0; c < D / 32; ++c) {
-            tmem_ld32(tO(wg) + lane_off + 32 * c, r);
+            tmem_ld32(tOw + 32 * c, r);
             tmem_ld_wait(r);
 #pragma unroll
             for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * scale);
-            tmem_st32(tO(wg) + lane_off + 32 * c, r);
+            tmem_st32(tOw + 32 * c, r);
           }
         }
         tmem_st_wait();

@@ -185,6 +185,13 @@ df_status df_attn_plan(const void* q, const void* k, const void* pos_key, const 
  * caller. */
 void df_attn_set_profile_events(df_event_t start, df_event_t stop);
 
+/* Profiling hook (process-wide, not thread-safe), used with the one above: while
+ * set, the tensor-core path also records `mid` between its near-tile and
+ * far-tile kernels, so that each can be timed alone; the strict-fp32 path (one
+ * fused kernel) records it right after `start`.  Pass NULL to clear.  Owned by
+ * the caller.  No counterpart in the pages: a measurement aid. */
+void df_attn_set_profile_split(df_event_t mid);
+
 /* Upper bound, in SM clock cycles, of every spin-wait on an mbarrier inside the
  * kernels (process-wide; 0 restores the default of about 2^31 cycles, ~1 s).
  * When a wait runs out the kernel records DF_ERR_DEVICE_TIMEOUT in the
