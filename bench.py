@@ -60,6 +60,22 @@ def shard_sequences(lengths, rank: int, world: int):
     return list(lengths)
 
 
+def max_over_ranks(values, dist=None, device="cpu"):
+    """Element-wise maximum of per-rank timings (the slowest rank decides the
+    step time); identity with one rank."""
+    import torch
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    if dist is not None:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t.cpu()]
+
+
+def job_throughput(world: int, units_per_rank: float, ms: float) -> float:
+    """Whole-job rate: every rank processes units_per_rank per step (weak scaling,
+    replicas), the step takes the maximum over ranks."""
+    return world * units_per_rank / (ms * 1e-3)
+
+
 def metric_flops(lengths, H, d):
     return float(sum(8.0 * n * n * d * H for n in lengths))
 
@@ -340,15 +356,12 @@ def main(argv=None):
         e2e = (e2e_ms, h2d, d2h)
 
     # max over ranks
-    times = torch.tensor([ms, near_ms, far_ms, e2e[0] if e2e else 0.0], dtype=torch.float64,
-                         device="cuda")
-    if dist is not None:
-        dist.all_reduce(times, op=dist.ReduceOp.MAX)
-    ms, near_ms, far_ms, e2e_ms = (float(t) for t in times.cpu())
+    ms, near_ms, far_ms, e2e_ms = max_over_ranks([ms, near_ms, far_ms, e2e[0] if e2e else 0.0],
+                                                 dist, device="cuda")
 
     flops_rank = metric_flops(lengths, H, d)
     tokens_rank = float(sum(lengths))
-    value = world * flops_rank / (ms * 1e-3) / 1e12
+    value = job_throughput(world, flops_rank, ms) / 1e12
     peaks, peak_src = load_peaks()
     tc = x.w.dtype in ("bf16", "fp16")
     if tc:
@@ -388,7 +401,7 @@ def main(argv=None):
                    "buckets": x.w.buckets, "max_rel": x.w.max_rel, "span": span,
                    "l2": "inputs larger than L2 (q,k,v,out %.0f MB)" % (
                        4 * out.numel() * out.element_size() / 1e6)},
-        "tokens_per_s": world * tokens_rank / (ms * 1e-3),
+        "tokens_per_s": job_throughput(world, tokens_rank, ms),
         "pct_bf16_peak_metric": value / world / float(peaks["bf16_tflops_sustained"]) * 100.0,
         "gpu_launches": launches_per_step * args.steps,
         "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
@@ -403,7 +416,7 @@ def main(argv=None):
                                             "achieved": oalgo / (oms * 1e-3) / 1e12,
                                             "frac": oalgo / (oms * 1e-3) / 1e12 / peak}
     if e2e:
-        line["e2e"] = {"value": world * flops_rank / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+        line["e2e"] = {"value": job_throughput(world, flops_rank, e2e_ms) / 1e12, "unit": "TFLOP/s",
                        "h2d_bytes_per_step": e2e[1], "d2h_bytes_per_step": e2e[2]}
     clocks = clk.summary()
     line["clocks"] = clocks
