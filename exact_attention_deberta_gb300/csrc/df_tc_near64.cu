@@ -326,69 +326,62 @@ __global__ void __launch_bounds__(kThreads, 1)
       ph ^= 1;
       return ok;
     };
-    // Drain the 32 columns t0 .. t0 + 31 of A (side 0, C) or B (side 1, P) as
-    // fp16.  Only the chunk on the window's edge needs a per-lane test.
-    auto drain = [&](int side, int t0, bool edge) {
-      uint32_t r[32];
-      tmem_ld32((side ? tB : tA) + lane_off + (t0 & 127), r);
+    // Drain NC columns t0 .. t0 + NC - 1 of A (side 0, C) or B (side 1, P) as
+    // fp16.  Chunks on the window's edge test every lane; the rest store all.
+    auto drain = [&](auto nc_tag, int side, int t0, bool edge) {
+      constexpr int NC = decltype(nc_tag)::value;
+      uint32_t r[NC];
+      const uint32_t src = (side ? tB : tA) + lane_off + (t0 & 127);
+      if constexpr (NC == 32) {
+        tmem_ld32(src, r);
+      } else {
+        tmem_ld8(src, r);
+      }
       tmem_ld_wait(r);
       if (side == 0) {
         const uint32_t dst = dC + 2u * kCwRow * t0;
-        if (!edge) {
 #pragma unroll
-          for (int e = 0; e < 32; ++e) sts16(dst + 2 * kCwRow * e, f16_satfinite(__uint_as_float(r[e])));
-        } else {
-#pragma unroll
-          for (int e = 0; e < 32; ++e)
-            if ((unsigned)(t0 + e - rho) < 128u)
-              sts16(dst + 2 * kCwRow * e, f16_satfinite(__uint_as_float(r[e])));
-        }
+        for (int e = 0; e < NC; ++e)
+          if (!edge || (unsigned)(t0 + e - rho) < 128u)
+            sts16(dst + 2 * kCwRow * e, f16_satfinite(__uint_as_float(r[e])));
       } else {
         const uint32_t dst = dP + 2u * t0;
-        if (!edge) {
 #pragma unroll
-          for (int e = 0; e < 32; ++e) sts16(dst + 2 * e, f16_satfinite(__uint_as_float(r[e])));
-        } else {
-#pragma unroll
-          for (int e = 0; e < 32; ++e)
-            if ((unsigned)(t0 + e - 127 + rho) < 128u)
-              sts16(dst + 2 * e, f16_satfinite(__uint_as_float(r[e])));
-        }
+        for (int e = 0; e < NC; ++e)
+          if (!edge || (unsigned)(t0 + e - 127 + rho) < 128u)
+            sts16(dst + 2 * e, f16_satfinite(__uint_as_float(r[e])));
       }
     };
-    // the five chunks a lane quarter needs from one half, shared by its 4 warps
+    // The five 32-column chunks a lane quarter needs from one half:
     //   half 0: C chunks qd..3, P chunks 3-qd..3;  half 1: C chunks 0..qd, P chunks 0..3-qd
-    //   the edge chunks: C chunk qd and P chunk 3 - qd of either half
+    //   (edge chunks: C chunk qd and P chunk 3 - qd of either half).
+    // Warp g drains chunk g whole and 8 columns of the fifth one.
     auto drain_half = [&](int half) {
-      for (int item = g; item < 5; item += 4) {
-        int side, c;
+      auto chunk = [&](int item, int* side, int* c) {
         if (half == 0) {
-          side = item < 4 - qd ? 0 : 1;
-          c = side == 0 ? qd + item : 3 - qd + (item - (4 - qd));
+          *side = item < 4 - qd ? 0 : 1;
+          *c = *side == 0 ? qd + item : 3 - qd + (item - (4 - qd));
         } else {
-          side = item <= qd ? 0 : 1;
-          c = side == 0 ? item : item - (qd + 1);
+          *side = item <= qd ? 0 : 1;
+          *c = *side == 0 ? item : item - (qd + 1);
         }
-        drain(side, 128 * half + 32 * c, c == (side == 0 ? qd : 3 - qd));
-      }
+      };
+      int side, c;
+      chunk(g, &side, &c);
+      drain(std::integral_constant<int, 32>{}, side, 128 * half + 32 * c,
+            c == (side == 0 ? qd : 3 - qd));
+      chunk(4, &side, &c);
+      drain(std::integral_constant<int, 8>{}, side, 128 * half + 32 * c + 8 * g,
+            c == (side == 0 ? qd : 3 - qd));
     };
-    // Add the position terms of this thread's 32 elements: the upper triangle
-    // j' >= rho (first halves) or the lower one (second halves).  Whole 32 x 32
-    // blocks off the diagonal belong to one triangle.
-    auto gather = [&](float (&x)[32], bool upper) {
-      const bool all = upper ? g > qd : g < qd;
-      if (all) {
+    // Add the position terms of this thread's 32 elements.  Blocks wholly in the
+    // upper triangle (j' >= rho: first halves only) are summed while the second
+    // halves are in the tensor core; the rest, diagonal blocks included, after.
+    auto gather = [&](float (&x)[32]) {
 #pragma unroll
-        for (int jj = 0; jj < 32; ++jj)
-          x[jj] = fmaf(f16_sum_f32(lds16(gC + 2 * kCwRow * (31 - jj)), lds16(gP + 2 * kPwRow * jj)),
-                       ks, x[jj]);
-      } else if (g == qd) {
-#pragma unroll
-        for (int jj = 0; jj < 32; ++jj)
-          if ((jj >= lane) == upper)
-            x[jj] = fmaf(f16_sum_f32(lds16(gC + 2 * kCwRow * (31 - jj)), lds16(gP + 2 * kPwRow * jj)),
-                         ks, x[jj]);
-      }
+      for (int jj = 0; jj < 32; ++jj)
+        x[jj] = fmaf(f16_sum_f32(lds16(gC + 2 * kCwRow * (31 - jj)), lds16(gP + 2 * kPwRow * jj)), ks,
+                     x[jj]);
     };
 
     for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
@@ -438,7 +431,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(bar_d0);
         named_sync(1, kComputeThreads);
-        gather(x, true);
+        if (g > qd) gather(x);
         // ---- second halves
         wait_ph(bar_c2, ph_c2, 291);
         tc_fence_after();
@@ -447,7 +440,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(bar_d1);
         named_sync(1, kComputeThreads);
-        gather(x, false);
+        if (g <= qd) gather(x);
 
         // ---- online softmax (log2 units); row maximum over the four column groups
         float mt = -INFINITY;
