@@ -33,7 +33,7 @@ constexpr unsigned long long kDefaultWaitBudget = 1ull << 31;
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 struct Layout {
-  size_t header, idx, items, seqs, scal, keybias, partial, diag_pk, diag_pq, total;
+  size_t header, idx, items, seqs, scal, keybias, partial, diag_pk, diag_pq, kaug, kaug_sel, total;
   int max_items, t_pad, lt, n_diag, diag_m0;
 };
 
@@ -103,6 +103,10 @@ Layout make_layout(int B, int H, int L, int d, int buckets, int max_rel, int spa
   off = align256(off + diag_bytes);
   l.diag_pq = off;
   off = align256(off + diag_bytes);
+  l.kaug = off;
+  off = align256(off + (size_t)l.t_pad * H * 16 * 2);
+  l.kaug_sel = off;
+  off = align256(off + 256 * 16 * 2);
   l.total = off;
   return l;
 }
@@ -161,6 +165,8 @@ df_status build_problem(const void* q, const void* k, const void* v, const void*
   P.lt = lay.lt;
   P.diag_pk = base + lay.diag_pk;
   P.diag_pq = base + lay.diag_pq;
+  P.kaug = base + lay.kaug;
+  P.kaug_sel = base + lay.kaug_sel;
   P.n_diag = lay.n_diag;
   P.diag_m0 = lay.diag_m0;
   const unsigned long long wb = g_wait_budget.load();
@@ -215,6 +221,8 @@ df_status df_attn_workspace_layout(int B, int H, int L, int d, int buckets, int 
   layout->diag_pq = l.diag_pq;
   layout->n_diag = l.n_diag;
   layout->diag_m0 = l.diag_m0;
+  layout->kaug = l.kaug;
+  layout->kaug_sel = l.kaug_sel;
   return DF_OK;
 }
 

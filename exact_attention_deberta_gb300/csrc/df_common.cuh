@@ -20,6 +20,9 @@ namespace dfa {
 constexpr int kQBlock = 128;
 // Keys per far tile of the tensor-core path.
 constexpr int kKBlock = 128;
+// Stand-in for -inf in the key-term block (raw score units): it must stay
+// finite because the MMA multiplies the unused side's terms by 0.
+constexpr float kMaskedKeyTerm = -30000.f;
 
 // Workspace views and call parameters handed to every kernel.
 struct Problem {
@@ -51,6 +54,10 @@ struct Problem {
   // PK / PQ[idx(128 m - 127 + t)], [rows][H][d] in the I/O type
   void* diag_pk;
   void* diag_pq;
+  // far tiles: per (key, head) 16 values (beta_neg hi, lo, beta_pos hi, lo, 0...)
+  // in the I/O type, and the two selector blocks [256][16]
+  void* kaug;
+  void* kaug_sel;
   int n_diag;
   int diag_m0;
   unsigned long long wait_budget;

@@ -83,6 +83,21 @@ __device__ void scalar_block(const Problem& p, int blk) {
     uint4* o4 = reinterpret_cast<uint4*>(static_cast<T*>(p.out) + row);
     for (int v = 0; v < d * (int)sizeof(T) / 16; ++v) o4[v] = make_uint4(0u, 0u, 0u, 0u);
   }
+  if constexpr (sizeof(T) == 2) {
+    // key-term block of far tiles: raw p2c products as hi + lo, masked keys finite
+    T v[16];
+    const float c0 = valid ? b0 : kMaskedKeyTerm, c1 = valid ? b1 : kMaskedKeyTerm;
+    const T h0 = IO<T>::from_f(c0), h1 = IO<T>::from_f(c1);
+    v[0] = h0;
+    v[1] = IO<T>::from_f(valid ? c0 - IO<T>::to_f(h0) : 0.f);
+    v[2] = h1;
+    v[3] = IO<T>::from_f(valid ? c1 - IO<T>::to_f(h1) : 0.f);
+#pragma unroll
+    for (int e = 4; e < 16; ++e) v[e] = IO<T>::from_f(0.f);
+    uint4* dst = reinterpret_cast<uint4*>(static_cast<T*>(p.kaug) + ((size_t)t * H + h) * 16);
+    dst[0] = *reinterpret_cast<const uint4*>(v);
+    dst[1] = *reinterpret_cast<const uint4*>(v + 8);
+  }
   const size_t base = (size_t)h * 4 * p.t_pad + t;
   p.scal[base + 0 * (size_t)p.t_pad] = valid ? a0 * p.kscale : 0.f;
   p.scal[base + 1 * (size_t)p.t_pad] = valid ? a1 * p.kscale : 0.f;
@@ -96,6 +111,18 @@ __device__ void scalar_block(const Problem& p, int blk) {
 // {start, n, head, query block} are laid out sequence by sequence in
 // non-increasing nblk order (ties keep the sequence order), head-major inside a
 // sequence so that blocks sharing K/V run next to each other.
+template <typename T>
+__device__ void write_kaug_selectors(const Problem& p) {
+  if constexpr (sizeof(T) == 2) {
+    T* sel = static_cast<T*>(p.kaug_sel);
+    for (int e = threadIdx.x; e < 256 * 16; e += blockDim.x) {
+      const int row = e >> 4, c = e & 15;
+      const bool one = row < 128 ? c < 2 : (c == 2 || c == 3);
+      sel[e] = IO<T>::from_f(one ? 1.f : 0.f);
+    }
+  }
+}
+
 __device__ void build_worklist(const Problem& p) {
   const int B = p.B, L = p.L;
   // The status word reports the latest call: this block is the only one of the
@@ -174,6 +201,7 @@ template <typename T>
 __global__ void __launch_bounds__(kPlanThreads)
     plan_kernel(Problem p, int nb_table, int nb_scal, int nb_diag) {
   if (blockIdx.x == 0) {  // the single work-list block starts first
+    write_kaug_selectors<T>(p);
     build_worklist(p);
     return;
   }

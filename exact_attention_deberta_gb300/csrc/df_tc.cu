@@ -440,17 +440,20 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 }
 
 // Row-major [rows][row_elems] 16-bit matrix, 64 x 128 boxes, 128-byte swizzle.
-bool encode_rows(CUtensorMap* m, const void* base, long long rows, long long row_elems, bool bf16) {
+// Row-major [rows][row_elems] 16-bit matrix in boxes of `inner` x 128 elements:
+// 64-element boxes with the 128-byte swizzle, 16-element boxes with the 32-byte one.
+bool encode_rows(CUtensorMap* m, const void* base, long long rows, long long row_elems, bool bf16,
+                 int inner = 64) {
   auto enc = tensor_map_encoder();
   if (!enc) return false;
   const cuuint64_t dims[2] = {(cuuint64_t)row_elems, (cuuint64_t)rows};
   const cuuint64_t strides[1] = {(cuuint64_t)row_elems * 2};
-  const cuuint32_t box[2] = {64, 128};
+  const cuuint32_t box[2] = {(cuuint32_t)inner, 128};
   const cuuint32_t es[2] = {1, 1};
   return enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
              const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+             inner == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_32B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 int sm_count() {
@@ -490,6 +493,9 @@ cudaError_t launch_tc(const Problem& p, cudaStream_t s, cudaEvent_t ev0, cudaEve
       !encode_rows(&maps.v, p.v, p.T, row, bf16) ||
       !encode_rows(&maps.pk, p.pk, 2LL * p.span, row, bf16) ||
       !encode_rows(&maps.pq, p.pq, 2LL * p.span, row, bf16))
+    return cudaErrorInvalidValue;
+  if (!encode_rows(&maps.kaug, p.kaug, p.T, 16LL * p.H, bf16, 16) ||
+      !encode_rows(&maps.kaug_sel, p.kaug_sel, 256, 16, bf16, 16))
     return cudaErrorInvalidValue;
   if (p.d == 64) {
     if (p.n_diag < 1 || !encode_rows(&maps.dpk, p.diag_pk, 256LL * p.n_diag, row, bf16) ||

@@ -13,8 +13,22 @@ constexpr unsigned long long kDrainBudget = 1ull << 31;
 
 struct TcMaps {
   CUtensorMap q, k, v, pk, pq;
-  CUtensorMap dpk, dpq;  // diagonal position tables (d = 64)
+  CUtensorMap dpk, dpq;        // diagonal position tables (d = 64)
+  CUtensorMap kaug, kaug_sel;  // far tiles: key-term block and selector rows (16 wide)
 };
+
+constexpr uint32_t kAugBytes = 128 * 16 * 2;  // one 128-row x 16-column 16-bit box
+
+// Descriptor of a K-major 128-row operand with 16 elements (32 bytes) per row,
+// 32-byte swizzle: 8-row groups 256 bytes apart.
+__device__ __forceinline__ uint64_t aug_desc(const uint8_t* tile) {
+  uint64_t d = (uint64_t)((ptx::smem_u32(tile) >> 4) & 0x3FFFu);
+  d |= (uint64_t)1 << 16;           // leading byte offset (unused by a single K step)
+  d |= (uint64_t)(256 >> 4) << 32;  // stride byte offset
+  d |= (uint64_t)1 << 46;           // descriptor version of tcgen05
+  d |= (uint64_t)6 << 61;           // 32-byte swizzle
+  return d;
+}
 
 // K step ks (16 elements) of a K-major 128-row tile stored as 64-column,
 // 128-byte-swizzled boxes: box ks/4, 32-byte offset inside it.

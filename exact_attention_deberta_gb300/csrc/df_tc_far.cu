@@ -6,7 +6,10 @@
 // (DisentangledFlash README, "Status": C2P/P2C disentangled attention; the
 // kernels-community "DisentangledFlash" discussion, "Motivation": exact,
 // tiled, streaming).  What remains per tile is flash attention with a rank-1
-// bias:  x_ij = (Q_i.K_j) * log2(e)/sqrt(3d) + alpha_i + beta_j.
+// bias:  x_ij = (Q_i.K_j + beta_j) * log2(e)/sqrt(3d) + alpha_i.  beta_j enters
+// the score MMA as a fifth K step: a selector block (1, 1, 0, 0, ...) or
+// (0, 0, 1, 1, ...) for the tile's side times the keys' block of raw p2c terms
+// (K.PQ[0] and K.PQ[top], each split into a 16-bit high and low part).
 //
 // Warp roles of one CTA (one CTA per SM, persistent over the work list):
 //   warp 0      TMA producer of Q (two buffers, so the next item's Q lands
@@ -45,14 +48,15 @@ struct FarSmem {
   static constexpr int kChunks = D / 64;
   static constexpr int kStages = D == 64 ? 4 : 2;
   static constexpr uint32_t kTileBytes = kChunks * kBoxBytes;
+  static constexpr uint32_t kStageBytes = 2 * kTileBytes + kAugBytes;
   static constexpr uint32_t q = 0;                                   // [2][Q tile]
-  static constexpr uint32_t kv = q + 2 * kTileBytes;                 // [stage][K | V]
-  static constexpr uint32_t beta = kv + kStages * 2 * kTileBytes;    // float [8 warps][128]
-  static constexpr uint32_t ml = beta + 8 * 128 * 4;                 // float4 [2 wg][128]
+  static constexpr uint32_t kv = q + 2 * kTileBytes;                 // [stage][K | V | key terms]
+  static constexpr uint32_t sel = kv + kStages * kStageBytes;        // [2] selector blocks
+  static constexpr uint32_t ml = sel + 2 * kAugBytes;                // float4 [2 wg][128]
   static constexpr uint32_t bars = ml + 2 * 128 * 16;
   // q_full[2], q_empty[2], k_full[S], k_empty[S], v_full[S], v_empty[S], s_full[2],
-  // p_full[2], o_final, drain[2], s_cons[2], pv_done[2]
-  static constexpr int kBars = 4 + 4 * kStages + 2 + 2 + 3 + 4;
+  // p_full[2], o_final, drain[2], s_cons[2], pv_done[2], sel_full
+  static constexpr int kBars = 4 + 4 * kStages + 2 + 2 + 3 + 4 + 1;
   static constexpr uint32_t misc = bars + kBars * 8;                 // abort flag, tmem slot
   static constexpr uint32_t bytes = misc + 16;
   static constexpr uint32_t alloc = bytes + 1024;
@@ -91,7 +95,7 @@ __global__ void __launch_bounds__(kFarThreads, 1)
   uint8_t* sm = reinterpret_cast<uint8_t*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   uint8_t* sQ = sm + SL::q;
   uint8_t* sKV = sm + SL::kv;
-  float* sBeta = reinterpret_cast<float*>(sm + SL::beta);
+  uint8_t* sSel = sm + SL::sel;
   float4* sML = reinterpret_cast<float4*>(sm + SL::ml);
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + SL::bars);
   uint64_t* q_full = bars;
@@ -106,6 +110,7 @@ __global__ void __launch_bounds__(kFarThreads, 1)
   uint64_t* drain = o_final + 1;         // [2]: one per MMA-issuing thread
   uint64_t* s_cons = drain + 2;   // softmax has read S(t) into registers
   uint64_t* pv_done = s_cons + 2; // P(t).V has completed
+  uint64_t* sel_full = pv_done + 2;  // selector blocks landed
   volatile int* s_abort = reinterpret_cast<volatile int*>(sm + SL::misc);
   uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + SL::misc + 4);
 
@@ -127,11 +132,13 @@ __global__ void __launch_bounds__(kFarThreads, 1)
       mbar_init(s_cons + b, 4);
       mbar_init(pv_done + b, 1);
     }
+    mbar_init(sel_full, 1);
     *s_abort = 0;
     mbar_fence_init();
     tma_prefetch_desc(&maps.q);
     tma_prefetch_desc(&maps.k);
     tma_prefetch_desc(&maps.v);
+    tma_prefetch_desc(&maps.kaug);
   }
   if (warp == 1) {
     tmem_alloc(tslot, 512);
@@ -169,6 +176,11 @@ __global__ void __launch_bounds__(kFarThreads, 1)
       const uint32_t off = is_k ? 0u : SL::kTileBytes;
       const CUtensorMap* map = is_k ? &maps.k : &maps.v;
       uint32_t g = 0, qc = 0, g_issued = 0, q_issued = 0;  // loads are issued in order
+      if (is_k) {  // the two selector blocks, once
+        mbar_expect_tx(sel_full, 2 * kAugBytes);
+        tma_load_2d(sSel, &maps.kaug_sel, 0, 0, sel_full);
+        tma_load_2d(sSel + kAugBytes, &maps.kaug_sel, 0, 128, sel_full);
+      }
       for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
         const ItemGeom ig = item_geom(p, it, rsp, rsn);
         if (ig.nt == 0) continue;
@@ -187,10 +199,13 @@ __global__ void __launch_bounds__(kFarThreads, 1)
           const int s = g % S;
           const int row = ig.start + ig.block_of(t) * 128;
           if (wait_or_abort(empty + s, ((g / S) & 1) ^ 1, budget, s_abort, hdr, is_k ? 302 : 303)) {
-            uint8_t* st = sKV + s * 2 * SL::kTileBytes + off;
-            mbar_expect_tx(full + s, SL::kTileBytes);
+            uint8_t* st = sKV + s * SL::kStageBytes + off;
+            mbar_expect_tx(full + s, SL::kTileBytes + (is_k ? kAugBytes : 0u));
             for (int c = 0; c < kChunks; ++c)
               tma_load_2d(st + c * kBoxBytes, map, ig.h * D + c * 64, row, full + s);
+            if (is_k)  // the keys' p2c terms, 16 values per key
+              tma_load_2d(sKV + s * SL::kStageBytes + 2 * SL::kTileBytes, &maps.kaug, ig.h * 16, row,
+                          full + s);
             g_issued = g + 1;
           }
         }
@@ -201,6 +216,7 @@ __global__ void __launch_bounds__(kFarThreads, 1)
         mbar_wait(full + k % S, (k / S) & 1, kDrainBudget);
       for (uint32_t k = q_issued > 2 ? q_issued - 2 : 0; k < q_issued; ++k)
         mbar_wait(q_full + (k & 1), (k >> 1) & 1, kDrainBudget);
+      if (is_k) mbar_wait(sel_full, 0, kDrainBudget);
     }
   } else if (warp == 1 || (kSepP && warp == 3)) {
     // ------------------------------------------------------------ MMA issuers
@@ -215,6 +231,7 @@ __global__ void __launch_bounds__(kFarThreads, 1)
       uint32_t g = 0, qc = 0;
       uint32_t pbits = 0, cbits = 0;  // bit b: parity of the next p_full[b] / s_cons[b] phase
       uint32_t s_used = 0;            // bit b: score buffer b has been written before
+      const bool sel_ok = !qk_role || wait_or_abort(sel_full, 0, budget, s_abort, hdr, 316);
       const uint32_t kv_addr = smem_u32(sKV);
       for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
         const ItemGeom ig = item_geom(p, it, rsp, rsn);
@@ -228,13 +245,16 @@ __global__ void __launch_bounds__(kFarThreads, 1)
           const uint32_t gs = g + t;
           const int s = gs % S;
           const bool ok = wait_or_abort(k_full + s, (gs / S) & 1, budget, s_abort, hdr, 312);
-          if (ok && q_ok) {
+          if (ok && q_ok && sel_ok) {
             const uint64_t dq = kmajor_desc(sQb, 0);
-            const uint64_t dk = kmajor_desc(sKV + s * 2 * SL::kTileBytes, 0);
+            const uint64_t dk = kmajor_desc(sKV + s * SL::kStageBytes, 0);
             tc_fence_after();
 #pragma unroll
             for (int k = 0; k < D / 16; ++k)
               mma_ss(tS(t & 1), dq + kmajor_step(k), dk + kmajor_step(k), kIdescQK, k > 0);
+            // S += selector . key terms: the p2c term of the tile's side (hi + lo)
+            mma_ss(tS(t & 1), aug_desc(sSel + (ig.pos_side(t) ? kAugBytes : 0u)),
+                   aug_desc(sKV + s * SL::kStageBytes + 2 * SL::kTileBytes), kIdescQK, 1u);
             mma_commit(s_full + (t & 1));
             mma_commit(k_empty + s);
           }
@@ -247,7 +267,7 @@ __global__ void __launch_bounds__(kFarThreads, 1)
           pbits ^= 1u << b;
           ok = wait_or_abort(v_full + s, (gs / S) & 1, budget, s_abort, hdr, 315) && ok;
           if (ok) {
-            const uint64_t dv = vtile_desc(kv_addr + s * 2 * SL::kTileBytes + SL::kTileBytes, 0);
+            const uint64_t dv = vtile_desc(kv_addr + s * SL::kStageBytes + SL::kTileBytes, 0);
             tc_fence_after();
             const bool carry = (t >= 2) || (b == 0 && has_partial);
 #pragma unroll
@@ -298,7 +318,6 @@ __global__ void __launch_bounds__(kFarThreads, 1)
     const int row = quad * 32 + lane;        // query row inside the block
     const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
     const float ks = p.kscale;
-    float* bw = sBeta + (warp - 4) * 128;  // this warp's copy of the tile's key terms
     // this warpgroup's TMEM buffers, in registers
     const uint32_t tSw = tmem + 128u * wg + lane_off;
     const uint32_t tPw = (kSepP ? tmem + 384u + 64u * wg : tmem + 128u * wg) + lane_off;
@@ -342,23 +361,8 @@ __global__ void __launch_bounds__(kFarThreads, 1)
         tmem_st_wait();
         o_has = true;
       }
-      // key terms beta_j of a tile, four per lane (keys 4 lane .. 4 lane + 3);
-      // every warp stages its own copy, so no warp waits for another
-      auto beta_of = [&](int t) -> float4 {
-        const int j0 = ig.block_of(t) * 128 + 4 * lane;
-        const float* src = scal_h + (ig.pos_side(t) ? 3 : 2) * (size_t)p.t_pad + ig.start;
-        float v[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) v[e] = j0 + e < ig.n ? src[j0 + e] : -INFINITY;
-        return make_float4(v[0], v[1], v[2], v[3]);
-      };
-      float4 beta_next = wg < ig.nt ? beta_of(wg) : make_float4(0.f, 0.f, 0.f, 0.f);
       const float2 ks2 = make_float2(ks, ks);
       for (int t = wg; t < ig.nt; t += 2, ++own) {
-        __syncwarp();  // every lane has finished reading the previous tile's copy
-        *reinterpret_cast<float4*>(bw + 4 * lane) = beta_next;
-        __syncwarp();
-        if (t + 2 < ig.nt) beta_next = beta_of(t + 2);
         wait_or_abort(s_full + wg, sc & 1, budget, s_abort, hdr, 321);
         ++sc;
         tc_fence_after();
@@ -384,15 +388,24 @@ __global__ void __launch_bounds__(kFarThreads, 1)
           if (lane == 0) mbar_arrive(s_cons + wg);
         }
         const float alpha = ig.pos_side(t) ? a_pos : a_neg;
-        // logits in log2 units; eight independent maximum chains
+        // Keys past the sequence end (only in its last key block) belong to the
+        // next sequence or to nothing: their scores become -inf.
+        const int kb = ig.block_of(t);
+        if (kb == ig.nkb - 1 && (ig.n & 127) != 0) {
+          const int valid = ig.n - 128 * kb;
+#pragma unroll
+          for (int j = 0; j < 128; ++j)
+            if (j >= valid) x[j] = -INFINITY;
+        }
+        // logits in log2 units (the key term came with S); eight independent
+        // maximum chains
         float mx[8];
 #pragma unroll
         for (int a = 0; a < 8; ++a) mx[a] = -INFINITY;
 #pragma unroll
         for (int j = 0; j < 128; j += 4) {
-          const float4 bv = *reinterpret_cast<const float4*>(bw + j);
-          const float2 y0 = fma2(make_float2(x[j], x[j + 1]), ks2, make_float2(bv.x, bv.y));
-          const float2 y1 = fma2(make_float2(x[j + 2], x[j + 3]), ks2, make_float2(bv.z, bv.w));
+          const float2 y0 = mul2(make_float2(x[j], x[j + 1]), ks2);
+          const float2 y1 = mul2(make_float2(x[j + 2], x[j + 3]), ks2);
           x[j] = y0.x;
           x[j + 1] = y0.y;
           x[j + 2] = y1.x;

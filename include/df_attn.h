@@ -152,6 +152,12 @@ typedef struct {
   size_t diag_pq;
   int n_diag;
   int diag_m0;
+  /* Key-term block of far tiles (16-bit I/O types): [Tpad][H][16] in the I/O
+   * type, per key the raw p2c products K.PQ[0] and K.PQ[2span-1], each as a
+   * high and a low part (hi + lo), then zeros; masked keys hold -30000.  Below
+   * it, kaug_sel: [256][16] selector rows (1, 1, 0, ...) and (0, 0, 1, 1, ...). */
+  size_t kaug;
+  size_t kaug_sel;
 } df_ws_layout;
 
 /* Header at workspace offset 0, written on the device by every call. */
