@@ -397,25 +397,19 @@ __global__ void __launch_bounds__(kFarThreads, 1)
           for (int j = 0; j < 128; ++j)
             if (j >= valid) x[j] = -INFINITY;
         }
-        // logits in log2 units (the key term came with S); eight independent
-        // maximum chains
+        // row maximum of the raw scores (the key term came with S; the log2
+        // scale is positive), eight independent chains
         float mx[8];
 #pragma unroll
         for (int a = 0; a < 8; ++a) mx[a] = -INFINITY;
 #pragma unroll
         for (int j = 0; j < 128; j += 4) {
-          const float2 y0 = mul2(make_float2(x[j], x[j + 1]), ks2);
-          const float2 y1 = mul2(make_float2(x[j + 2], x[j + 3]), ks2);
-          x[j] = y0.x;
-          x[j + 1] = y0.y;
-          x[j + 2] = y1.x;
-          x[j + 3] = y1.y;
           const int a = (j >> 2) & 3;
-          mx[2 * a] = fmaxf(mx[2 * a], fmaxf(y0.x, y0.y));
-          mx[2 * a + 1] = fmaxf(mx[2 * a + 1], fmaxf(y1.x, y1.y));
+          mx[2 * a] = fmaxf(mx[2 * a], fmaxf(x[j], x[j + 1]));
+          mx[2 * a + 1] = fmaxf(mx[2 * a + 1], fmaxf(x[j + 2], x[j + 3]));
         }
         const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                               fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) + alpha;
+                               fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * ks + alpha;
         float scale = 1.f;
         const bool rebase = mt > m_run + 8.f;
         if (rebase) {
@@ -425,7 +419,8 @@ __global__ void __launch_bounds__(kFarThreads, 1)
         }
         // P(t - 2).V must be done before O is rescaled or P is overwritten
         if (kSepP && own > 0) wait_or_abort(pv_done + wg, (own - 1) & 1, budget, s_abort, hdr, 323);
-        // p = 2^(x + alpha - m); with no finite logit yet every p is 0
+        // p = 2^(S ks + alpha - m), one FMA per pair; with no finite logit yet
+        // every p is 0
         const float shift = m_run == -INFINITY ? INFINITY : m_run - alpha;
         const float2 nshift = make_float2(-shift, -shift);
         {
@@ -437,7 +432,7 @@ __global__ void __launch_bounds__(kFarThreads, 1)
           for (int c = 0; c < 2; ++c) {
 #pragma unroll
             for (int e = 0; e < 32; ++e) {
-              const float2 z = add2(make_float2(x[64 * c + 2 * e], x[64 * c + 2 * e + 1]), nshift);
+              const float2 z = fma2(make_float2(x[64 * c + 2 * e], x[64 * c + 2 * e + 1]), ks2, nshift);
               const float2 pp = make_float2(ex2(z.x), ex2(z.y));
               acc[e & 3] = add2(acc[e & 3], pp);
               r[e] = BF16 ? pack_bf16x2(pp.x, pp.y) : pack_f16x2(pp.x, pp.y);
