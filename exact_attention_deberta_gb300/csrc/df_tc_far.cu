@@ -46,7 +46,7 @@ constexpr int kFarThreads = 384;
 template <int D>
 struct FarSmem {
   static constexpr int kChunks = D / 64;
-  static constexpr int kStages = D == 64 ? 4 : 2;
+  static constexpr int kStages = D == 64 ? 5 : 2;
   static constexpr uint32_t kTileBytes = kChunks * kBoxBytes;
   static constexpr uint32_t kStageBytes = 2 * kTileBytes + kAugBytes;
   static constexpr uint32_t q = 0;                                   // [2][Q tile]
@@ -405,8 +405,8 @@ __global__ void __launch_bounds__(kFarThreads, 1)
 #pragma unroll
         for (int j = 0; j < 128; j += 4) {
           const int a = (j >> 2) & 3;
-          mx[2 * a] = fmaxf(mx[2 * a], fmaxf(x[j], x[j + 1]));
-          mx[2 * a + 1] = fmaxf(mx[2 * a + 1], fmaxf(x[j + 2], x[j + 3]));
+          mx[2 * a] = fmax3(mx[2 * a], x[j], x[j + 1]);
+          mx[2 * a + 1] = fmax3(mx[2 * a + 1], x[j + 2], x[j + 3]);
         }
         const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
                                fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * ks + alpha;
