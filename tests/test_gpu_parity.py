@@ -184,6 +184,27 @@ def test_arbitrary_mask_pattern(lib, dtype):
     assert_close(out.double().cpu().numpy(), ref, dtype, "holes")
 
 
+@pytest.mark.parametrize("dtype,d", [("bf16", 64), ("fp16", 64), ("bf16", 128)])
+def test_mask_holes_in_far_tiles(lib, dtype, d):
+    """Long padded rows (far tiles exist: 13 key blocks) with key-mask holes in
+    both near and far tiles, a row whose valid keys are all far from it, and a
+    ragged last key block; checked on every row."""
+    L = 1600
+    x = synth.custom_inputs(layout="padded", dtype=dtype, H=2, d=d, lengths=[L, L, 1500], L=L, seed=17)
+    m = x.key_mask.clone()
+    g = torch.Generator().manual_seed(3)
+    m[0] = (torch.rand(L, generator=g) < 0.6).to(torch.uint8)
+    m[1] = 0
+    m[1, 1200:1210] = 1          # rows 0..700 see only far keys
+    m[1, 1599] = 1
+    m[2, 1400:1500] = 0          # a hole at the end of a ragged sequence
+    m[2, 0:40] = 0
+    x.key_mask = m
+    out = run_gpu(lib, x)
+    ref = oracle_full(x)
+    assert_close(out.double().cpu().numpy(), ref, dtype, f"far-holes-{dtype}-d{d}")
+
+
 @pytest.mark.parametrize("buckets,max_rel,span", [(0, 300, 300), (32, 64, 32), (256, 512, 128), (16, 4096, 16)])
 def test_other_position_parameters(lib, buckets, max_rel, span):
     x = synth.custom_inputs(layout="packed", dtype="bf16", H=2, d=64, lengths=[900, 64, 1500], L=1500,
