@@ -17,8 +17,9 @@
 //   warp 2      TMA producer of V; K and V have separate stage barriers, a K
 //               stage is free once its QK has completed, a V stage once its
 //               P.V has, so K loads run further ahead;
-//   warp 1      tcgen05.mma issuer of S = Q.K^T into one of two TMEM score
-//               buffers (and, at d = 128, of the P.V products too);
+//   warp 1      tcgen05.mma issuer of S = Q.K^T into a TMEM score buffer
+//               (three at d = 64, P overwriting its S, so QK(G) waits only
+//               for P(G - 3).V; at d = 128 this warp also issues the P.V);
 //   warp 3      at d = 64 the issuer of O_b += P.V with P read back from TMEM,
 //               so that QK never queues behind a blocking P.V issue; idle at
 //               d = 128;
@@ -54,9 +55,9 @@ struct FarSmem {
   static constexpr uint32_t sel = kv + kStages * kStageBytes;        // [2] selector blocks
   static constexpr uint32_t ml = sel + 2 * kAugBytes;                // float4 [2 wg][128]
   static constexpr uint32_t bars = ml + 2 * 128 * 16;
-  // q_full[2], q_empty[2], k_full[S], k_empty[S], v_full[S], v_empty[S], s_full[2],
-  // p_full[2], o_final, drain[2], s_cons[2], pv_done[2], sel_full
-  static constexpr int kBars = 4 + 4 * kStages + 2 + 2 + 3 + 4 + 1;
+  // q_full[2], q_empty[2], k_full[S], k_empty[S], v_full[S], v_empty[S], s_full[3],
+  // p_full[2][2], o_final, drain[2], buf_free[3], sel_full
+  static constexpr int kBars = 4 + 4 * kStages + 3 + 4 + 3 + 3 + 1;
   static constexpr uint32_t misc = bars + kBars * 8;                 // abort flag, tmem slot
   static constexpr uint32_t bytes = misc + 16;
   static constexpr uint32_t alloc = bytes + 1024;
@@ -104,13 +105,16 @@ __global__ void __launch_bounds__(kFarThreads, 1)
   uint64_t* k_empty = bars + 4 + S;      // K(t) read: QK(t) has completed
   uint64_t* v_full = bars + 4 + 2 * S;
   uint64_t* v_empty = bars + 4 + 3 * S;  // V(t) read: P(t).V has completed
-  uint64_t* s_full = bars + 4 + 4 * S;
-  uint64_t* p_full = s_full + 2;
-  uint64_t* o_final = p_full + 2;
+  uint64_t* s_full = bars + 4 + 4 * S;   // [3] S of the buffer computed
+  // [wg][k & 1]: the four warps of warpgroup wg stored P of its k-th tile.  Two
+  // per warpgroup because a warp may finish its next tile before a sibling
+  // warp has stored the current one; it is never two tiles ahead, since its
+  // next S waits for a P.V issued after this phase.
+  uint64_t* p_full = s_full + 3;
+  uint64_t* o_final = p_full + 4;
   uint64_t* drain = o_final + 1;         // [2]: one per MMA-issuing thread
-  uint64_t* s_cons = drain + 2;   // softmax has read S(t) into registers
-  uint64_t* pv_done = s_cons + 2; // P(t).V has completed
-  uint64_t* sel_full = pv_done + 2;  // selector blocks landed
+  uint64_t* buf_free = drain + 2;  // [3] d = 64: the P.V that read the buffer is done
+  uint64_t* sel_full = buf_free + 3;  // selector blocks landed
   volatile int* s_abort = reinterpret_cast<volatile int*>(sm + SL::misc);
   uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + SL::misc + 4);
 
@@ -121,17 +125,14 @@ __global__ void __launch_bounds__(kFarThreads, 1)
       mbar_init(q_empty + b, 1);
     }
     for (int s = 0; s < 4 * S; ++s) mbar_init(k_full + s, 1);
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < 3; ++b) {
       mbar_init(s_full + b, 1);
-      mbar_init(p_full + b, 4);
+      mbar_init(buf_free + b, 1);
     }
+    for (int b = 0; b < 4; ++b) mbar_init(p_full + b, 4);
     mbar_init(o_final, 1);
     mbar_init(drain, 1);
     mbar_init(drain + 1, 1);
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(s_cons + b, 4);
-      mbar_init(pv_done + b, 1);
-    }
     mbar_init(sel_full, 1);
     *s_abort = 0;
     mbar_fence_init();
@@ -149,15 +150,14 @@ __global__ void __launch_bounds__(kFarThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tslot;
   // TMEM columns of buffer b
-  const uint32_t tSa[2] = {tmem, tmem + 128};
-  const uint32_t tOa[2] = {tmem + 256, tmem + 256 + D};
-  auto tS = [&](int b) { return tSa[b]; };
-  auto tO = [&](int b) { return tOa[b]; };
-  // d = 64 leaves room for a P buffer per warpgroup, so that S can be refilled
-  // as soon as the softmax has read it; at d = 128 P overwrites its S buffer.
-  constexpr bool kSepP = D == 64;
-  const uint32_t tPa[2] = {kSepP ? tmem + 384 : tSa[0], kSepP ? tmem + 448 : tSa[1]};
-  auto tP = [&](int b) { return tPa[b]; };
+  // d = 64: three score buffers (tile G of the CTA uses buffer G % 3) and the
+  // two warpgroups' O; P(G) overwrites its own S once the softmax has read it,
+  // so neither the softmax nor QK(G + 2) waits for a P.V.  d = 128: one score
+  // buffer per warpgroup (P overwrites it) and the two O.
+  constexpr bool kTriS = D == 64;
+  const uint32_t tO_base = tmem + (kTriS ? 384u : 256u);
+  auto tS = [&](int b) { return tmem + 128u * b; };
+  auto tO = [&](int b) { return tO_base + (uint32_t)D * b; };
 
   const int n_items = p.hdr->n_items;
   const int rsp = p.hdr->r_sat_pos, rsn = p.hdr->r_sat_neg;
@@ -218,7 +218,7 @@ __global__ void __launch_bounds__(kFarThreads, 1)
         mbar_wait(q_full + (k & 1), (k >> 1) & 1, kDrainBudget);
       if (is_k) mbar_wait(sel_full, 0, kDrainBudget);
     }
-  } else if (warp == 1 || (kSepP && warp == 3)) {
+  } else if (warp == 1 || (kTriS && warp == 3)) {
     // ------------------------------------------------------------ MMA issuers
     // d = 64: warp 1 issues S = Q.K^T, warp 3 issues O += P.V, so that neither
     // chain waits behind the other's blocking issue; every commit is made by the
@@ -227,10 +227,9 @@ __global__ void __launch_bounds__(kFarThreads, 1)
     setmaxnreg_dec<56>();
     if (lane == 0) {
       const bool qk_role = warp == 1;
-      const bool pv_role = warp == 3 || !kSepP;
+      const bool pv_role = warp == 3 || !kTriS;
       uint32_t g = 0, qc = 0;
-      uint32_t pbits = 0, cbits = 0;  // bit b: parity of the next p_full[b] / s_cons[b] phase
-      uint32_t s_used = 0;            // bit b: score buffer b has been written before
+      uint32_t pn[2] = {0, 0};  // tiles of warpgroup b whose P has been consumed
       const bool sel_ok = !qk_role || wait_or_abort(sel_full, 0, budget, s_abort, hdr, 316);
       const uint32_t kv_addr = smem_u32(sKV);
       for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
@@ -244,18 +243,23 @@ __global__ void __launch_bounds__(kFarThreads, 1)
         auto issue_qk = [&](int t) {
           const uint32_t gs = g + t;
           const int s = gs % S;
-          const bool ok = wait_or_abort(k_full + s, (gs / S) & 1, budget, s_abort, hdr, 312);
+          // score buffer: G % 3 at d = 64 (free once P(G - 3).V is done), else t % 2
+          const int sb = kTriS ? (int)(gs % 3) : (t & 1);
+          bool ok = true;
+          if (kTriS && gs >= 3)
+            ok = wait_or_abort(buf_free + sb, ((gs - 3) / 3) & 1, budget, s_abort, hdr, 314);
+          ok = wait_or_abort(k_full + s, (gs / S) & 1, budget, s_abort, hdr, 312) && ok;
           if (ok && q_ok && sel_ok) {
             const uint64_t dq = kmajor_desc(sQb, 0);
             const uint64_t dk = kmajor_desc(sKV + s * SL::kStageBytes, 0);
             tc_fence_after();
 #pragma unroll
             for (int k = 0; k < D / 16; ++k)
-              mma_ss(tS(t & 1), dq + kmajor_step(k), dk + kmajor_step(k), kIdescQK, k > 0);
+              mma_ss(tS(sb), dq + kmajor_step(k), dk + kmajor_step(k), kIdescQK, k > 0);
             // S += selector . key terms: the p2c term of the tile's side (hi + lo)
-            mma_ss(tS(t & 1), aug_desc(sSel + (ig.pos_side(t) ? kAugBytes : 0u)),
+            mma_ss(tS(sb), aug_desc(sSel + (ig.pos_side(t) ? kAugBytes : 0u)),
                    aug_desc(sKV + s * SL::kStageBytes + 2 * SL::kTileBytes), kIdescQK, 1u);
-            mma_commit(s_full + (t & 1));
+            mma_commit(s_full + sb);
             mma_commit(k_empty + s);
           }
         };
@@ -263,33 +267,24 @@ __global__ void __launch_bounds__(kFarThreads, 1)
           const int b = t & 1;
           const uint32_t gs = g + t;
           const int s = gs % S;
-          bool ok = wait_or_abort(p_full + b, (pbits >> b) & 1, budget, s_abort, hdr, 313);
-          pbits ^= 1u << b;
+          const uint32_t k = pn[b]++;
+          bool ok = wait_or_abort(p_full + 2 * b + (k & 1), (k >> 1) & 1, budget, s_abort, hdr, 313);
           ok = wait_or_abort(v_full + s, (gs / S) & 1, budget, s_abort, hdr, 315) && ok;
           if (ok) {
             const uint64_t dv = vtile_desc(kv_addr + s * SL::kStageBytes + SL::kTileBytes, 0);
             tc_fence_after();
             const bool carry = (t >= 2) || (b == 0 && has_partial);
+            const uint32_t tP = tS(kTriS ? (int)(gs % 3) : b);  // P(t) overwrote its S
 #pragma unroll
             for (int k = 0; k < 128 / 16; ++k)
-              mma_ts(tO(b), tP(b) + 8 * k, dv + vtile_step(k), kIdescPV, (k > 0 || carry) ? 1u : 0u);
+              mma_ts(tO(b), tP + 8 * k, dv + vtile_step(k), kIdescPV, (k > 0 || carry) ? 1u : 0u);
             mma_commit(v_empty + s);
-            if (kSepP) mma_commit(pv_done + b);
+            if (kTriS) mma_commit(buf_free + (gs % 3));
           }
         };
-        if (kSepP) {
+        if (kTriS) {
           if (qk_role) {
-            // QK(t) goes out as soon as warpgroup t % 2 has read the score
-            // buffer's previous contents (also across items)
-            for (int t = 0; t < ig.nt; ++t) {
-              const int b = t & 1;
-              if (s_used & (1u << b)) {
-                wait_or_abort(s_cons + b, (cbits >> b) & 1, budget, s_abort, hdr, 314);
-                cbits ^= 1u << b;
-              }
-              s_used |= 1u << b;
-              issue_qk(t);
-            }
+            for (int t = 0; t < ig.nt; ++t) issue_qk(t);
           } else {
             for (int t = 0; t < ig.nt; ++t) issue_pv(t);
           }
@@ -318,11 +313,9 @@ __global__ void __launch_bounds__(kFarThreads, 1)
     const int row = quad * 32 + lane;        // query row inside the block
     const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
     const float ks = p.kscale;
-    // this warpgroup's TMEM buffers, in registers
-    const uint32_t tSw = tmem + 128u * wg + lane_off;
-    const uint32_t tPw = (kSepP ? tmem + 384u + 64u * wg : tmem + 128u * wg) + lane_off;
-    const uint32_t tOw = tmem + 256u + (uint32_t)D * wg + lane_off;
-    uint32_t sc = 0, ic = 0, own = 0;
+    // this warpgroup's O, in a register
+    const uint32_t tOw = tO_base + (uint32_t)D * wg + lane_off;
+    uint32_t sc = 0, ic = 0, own = 0, gbase = 0;  // gbase: CTA tiles before the item
     for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
       const ItemGeom ig = item_geom(p, it, rsp, rsn);
       if (ig.nt == 0) continue;
@@ -363,7 +356,11 @@ __global__ void __launch_bounds__(kFarThreads, 1)
       }
       const float2 ks2 = make_float2(ks, ks);
       for (int t = wg; t < ig.nt; t += 2, ++own) {
-        wait_or_abort(s_full + wg, sc & 1, budget, s_abort, hdr, 321);
+        // score buffer of the tile: G % 3 (d = 64) or the warpgroup's own (d = 128)
+        const uint32_t G = gbase + t;
+        const int sb = kTriS ? (int)(G % 3) : wg;
+        const uint32_t tSw = tmem + 128u * sb + lane_off;
+        wait_or_abort(s_full + sb, kTriS ? (G / 3) & 1 : sc & 1, budget, s_abort, hdr, 321);
         ++sc;
         tc_fence_after();
         float x[128];
@@ -381,11 +378,6 @@ __global__ void __launch_bounds__(kFarThreads, 1)
             x[64 + e] = __uint_as_float(r2[e]);
             x[96 + e] = __uint_as_float(r3[e]);
           }
-        }
-        if (kSepP) {  // S(t) is in registers: the MMA may refill the buffer
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(s_cons + wg);
         }
         const float alpha = ig.pos_side(t) ? a_pos : a_neg;
         // Keys past the sequence end (only in its last key block) belong to the
@@ -417,8 +409,6 @@ __global__ void __launch_bounds__(kFarThreads, 1)
           m_run = mt;
           l_run *= scale;
         }
-        // P(t - 2).V must be done before O is rescaled or P is overwritten
-        if (kSepP && own > 0) wait_or_abort(pv_done + wg, (own - 1) & 1, budget, s_abort, hdr, 323);
         // p = 2^(S ks + alpha - m), one FMA per pair; with no finite logit yet
         // every p is 0
         const float shift = m_run == -INFINITY ? INFINITY : m_run - alpha;
@@ -437,7 +427,7 @@ __global__ void __launch_bounds__(kFarThreads, 1)
               acc[e & 3] = add2(acc[e & 3], pp);
               r[e] = BF16 ? pack_bf16x2(pp.x, pp.y) : pack_f16x2(pp.x, pp.y);
             }
-            tmem_st32(tPw + 32 * c, r);
+            tmem_st32(tSw + 32 * c, r);  // P(t) overwrites the S it came from
           }
           const float2 s01 = add2(acc[0], acc[1]), s23 = add2(acc[2], acc[3]);
           l_run += (s01.x + s23.x) + (s01.y + s23.y);
@@ -445,6 +435,12 @@ __global__ void __launch_bounds__(kFarThreads, 1)
         // rescale O after the scores are dead (fewer live registers); P(t).V has
         // not been issued yet, so O still holds the tiles before t
         if (o_has && __any_sync(0xffffffffu, rebase)) {
+          // d = 64: P(t - 2).V, this warpgroup's previous one, must be done (at
+          // d = 128 the score MMA of t already followed it in the same pipe)
+          if (kTriS && t >= 2) {
+            wait_or_abort(buf_free + (G - 2) % 3, ((G - 2) / 3) & 1, budget, s_abort, hdr, 323);
+            tc_fence_after();
+          }
           uint32_t r[32];
 #pragma unroll
           for (int c = 0; c < D / 32; ++c) {
@@ -458,7 +454,7 @@ __global__ void __launch_bounds__(kFarThreads, 1)
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(p_full + wg);
+        if (lane == 0) mbar_arrive(p_full + 2 * wg + (own & 1));
         o_has = true;
       }
       // ---- merge the two warpgroups' partial results and write O
@@ -507,6 +503,7 @@ __global__ void __launch_bounds__(kFarThreads, 1)
       }
       tc_fence_before();
       named_sync(3, 256);
+      gbase += ig.nt;
     }
   }
 
