@@ -15,15 +15,20 @@
 // fixed skew, with no index lookups.  The 256 diagonal columns come in two MMA
 // halves (t < 128, t >= 128) that share the tensor-memory columns A and B.
 //
-// Skew through shared memory.  Each drained value lands where the gather reads
-// it as a unit-stride row of query indices:
-//     Cw[t - i'][i'] = C[i'][t]  (kept for 0 <= t - i' < 128)
-//     Pw[j'][i']     = P[j'][t]  with i' = t - 127 + j'
-// so element (i', j') reads Cw[127 - j'][i'] and Pw[j'][i'].  Both stores and
-// loads are 16-bit and bank-conflict free (row strides 262 and 258 bytes).  The
-// terms are rounded to fp16 (saturating) and scaled to log2 units when they
-// are added; the upper triangle j' >= i' needs only the first half, so it is
-// summed while the second half is in the tensor core.
+// Skew through shared memory.  Both terms are stored by query row, in the
+// order the score row reads them:
+//     Cw[i'][j'] = C[i'][i' - j' + 127]      Pw[i'][j'] = P[j'][i' - j' + 127]
+// A lane of C drains its own query row, where consecutive diagonals are
+// consecutive keys (descending): it converts two values per instruction and
+// stores them as 32-bit words (rows of odd lanes start one key late, so their
+// pairs are re-formed with a byte permute and the two end values go alone).  A
+// lane of P (a key row) writes one 16-bit value into each query row.  The
+// gather then reads 32 keys of each term as four 16-byte vectors and adds the
+// two as fp16x2.  Rows are 272 bytes (16-byte aligned, 8 keys of padding): the
+// vector loads are conflict free, the drains' stores at most 2-way.  The terms
+// are rounded to fp16 (saturating) and scaled to log2 units when they are
+// added; the upper triangle j' >= i' needs only the first half, so it is summed
+// while the second half is in the tensor core.
 //
 // Roles (one CTA per SM, persistent over the work list):
 //   warps 0-15  compute: warp w owns TMEM lanes 32 (w % 4) .. +31 (query rows
@@ -56,8 +61,8 @@ constexpr int kTile = 128;
 constexpr int kComputeWarps = 16;
 constexpr int kComputeThreads = kComputeWarps * 32;
 constexpr int kThreads = kComputeThreads + 32;
-constexpr int kCwRow = 131;  // fp16 elements per Cw row (262 B: conflict-free skew)
-constexpr int kPwRow = 129;  // fp16 elements per Pw row (258 B)
+constexpr uint32_t kRowB = 272;    // bytes per Cw / Pw row: 128 keys + 8 of padding
+constexpr uint32_t kRowLead = 16;  // Cw lead: words written just before row 0 land here
 
 struct Smem {
   static constexpr uint32_t q = 0;                       // Q tile
@@ -65,9 +70,9 @@ struct Smem {
   static constexpr uint32_t e0 = k + 2 * kBoxBytes;      // diagonal rows 0-127: PK | PQ
   static constexpr uint32_t e1 = e0 + 2 * kBoxBytes;     // diagonal rows 128-255: PK | PQ
   static constexpr uint32_t v = e1 + 2 * kBoxBytes;      // V tiles [2]
-  static constexpr uint32_t cw = v + 2 * kBoxBytes;      // fp16 [128][131]
-  static constexpr uint32_t pw = cw + 128 * kCwRow * 2;  // fp16 [128][129]
-  static constexpr uint32_t col = pw + 128 * kPwRow * 2; // float [2][128] key bias
+  static constexpr uint32_t cw = v + 2 * kBoxBytes;      // lead + fp16 [128][136]
+  static constexpr uint32_t pw = cw + kRowLead + 128 * kRowB;  // fp16 [128][136]
+  static constexpr uint32_t col = pw + 128 * kRowB;      // float [2][128] key bias
   static constexpr uint32_t red = col + 2 * 128 * 4;     // float [4][128]
   static constexpr uint32_t bars = red + 4 * 128 * 4;
   static constexpr int kBars = 15;
@@ -311,14 +316,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int rho = qd * 32 + lane;      // TMEM lane: query row (S, C, O) or key row (P)
     const uint32_t lane_off = (uint32_t)(qd * 32) << 16;
     const float ks = p.kscale;
-    // 32-bit shared addresses of the fp16 buffers (row strides kCwRow, kPwRow elements)
-    const uint32_t cw = smem_u32(sm + SL::cw), pw = smem_u32(sm + SL::pw);
-    // drain: C[rho][t] -> Cw[t - rho][rho];  P[rho][t] -> Pw[rho][t - 127 + rho]
-    const uint32_t dC = cw - 2u * (kCwRow - 1) * rho;         // + 2 kCwRow t
-    const uint32_t dP = pw + 2u * (kPwRow + 1) * rho - 254u;   // + 2 t
-    // gather of element (rho, j' = 32 g + jj): Cw[127 - j'][rho] and Pw[j'][rho]
-    const uint32_t gC = cw + 2u * (kCwRow * (96 - 32 * g) + rho);  // + 2 kCwRow (31 - jj)
-    const uint32_t gP = pw + 2u * (kPwRow * 32 * g + rho);          // + 2 kPwRow jj
+    // 32-bit shared addresses of the fp16 rows (kRowB bytes each)
+    const uint32_t cw = smem_u32(sm + SL::cw) + kRowLead, pw = smem_u32(sm + SL::pw);
+    const uint32_t cw_row = cw + kRowB * rho;                       // C: lane rho's own row
+    const uint32_t dP = pw + (uint32_t)((int)kRowB * (rho - 127) + 2 * rho);  // + kRowB t
+    // gather of (rho, 32 g .. 32 g + 31): 64 bytes of each term's row
+    const uint32_t gC = cw_row + 64u * g, gP = pw + kRowB * rho + 64u * g;
 
     uint32_t ph_c1 = 0, ph_c2 = 0, ph_c3 = 0, gt = 0;
     auto wait_ph = [&](uint64_t* bar, uint32_t& ph, int where) {
@@ -326,8 +329,45 @@ __global__ void __launch_bounds__(kThreads, 1)
       ph ^= 1;
       return ok;
     };
-    // Drain NC columns t0 .. t0 + NC - 1 of A (side 0, C) or B (side 1, P) as
-    // fp16.  Chunks on the window's edge test every lane; the rest store all.
+    // Store NC drained columns t0 .. t0 + NC - 1 (t0 even) as fp16.  q[k] holds
+    // columns t0 + 2k (bits 16-31) and t0 + 2k + 1 (bits 0-15).  EDGE chunks
+    // reach outside the lane's window and test each store.
+    auto store_c = [&](auto nc_tag, auto edge_tag, int t0, const uint32_t* q) {
+      constexpr int NC = decltype(nc_tag)::value;
+      constexpr bool EDGE = decltype(edge_tag)::value;
+      // key u = rho + 127 - t of column t: the chunk covers keys a .. a + NC - 1,
+      // column t0 + NC - 1 - (u - a) at key u.  Words at even keys; an odd row
+      // (a odd) shifts every pair by one key.  A word written next to the row's
+      // keys 0..127 lands in padding (keys -8..-1 and 128..135).
+      const int a = rho + 128 - t0 - NC;
+      const int odd = rho & 1;
+      const uint32_t sel = odd ? 0x5432u : 0x3210u;
+      const uint32_t base = cw_row + 2u * (uint32_t)(a + odd);
+#pragma unroll
+      for (int m = 0; m < NC / 2 - 1; ++m) {
+        const uint32_t w = prmt(q[NC / 2 - 1 - m], q[NC / 2 - 2 - m], sel);
+        if (!EDGE || (unsigned)(a + odd + 2 * m + 8) < 143u) sts32(base + 4u * m, w);
+      }
+      if (!odd) {
+        if (!EDGE || (unsigned)(a + NC - 2 + 8) < 143u) sts32(base + 4u * (NC / 2 - 1), q[0]);
+      } else {
+        if (!EDGE || (unsigned)(a + 8) < 143u) sts16_lo(cw_row + 2u * (uint32_t)a, q[NC / 2 - 1]);
+        if (!EDGE || (unsigned)(a + NC - 1 + 8) < 143u)
+          sts16_lo(cw_row + 2u * (uint32_t)(a + NC - 1), q[0] >> 16);
+      }
+    };
+    auto store_p = [&](auto nc_tag, auto edge_tag, int t0, const uint32_t* q) {
+      constexpr int NC = decltype(nc_tag)::value;
+      constexpr bool EDGE = decltype(edge_tag)::value;
+      // column t of key row rho goes to query row t - 127 + rho
+      const uint32_t dst = dP + kRowB * (uint32_t)t0;
+#pragma unroll
+      for (int k = 0; k < NC / 2; ++k) {
+        if (!EDGE || (unsigned)(t0 + 2 * k - 127 + rho) < 128u) sts16_lo(dst + kRowB * (2 * k), q[k] >> 16);
+        if (!EDGE || (unsigned)(t0 + 2 * k + 1 - 127 + rho) < 128u) sts16_lo(dst + kRowB * (2 * k + 1), q[k]);
+      }
+    };
+    // Drain NC columns t0 .. t0 + NC - 1 of A (side 0, C) or B (side 1, P).
     auto drain = [&](auto nc_tag, int side, int t0, bool edge) {
       constexpr int NC = decltype(nc_tag)::value;
       uint32_t r[NC];
@@ -338,18 +378,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld8(src, r);
       }
       tmem_ld_wait(r);
+      uint32_t q[NC / 2];
+#pragma unroll
+      for (int k = 0; k < NC / 2; ++k)
+        q[k] = f16x2_satfinite(__uint_as_float(r[2 * k]), __uint_as_float(r[2 * k + 1]));
+      using E1 = std::integral_constant<bool, true>;
+      using E0 = std::integral_constant<bool, false>;
       if (side == 0) {
-        const uint32_t dst = dC + 2u * kCwRow * t0;
-#pragma unroll
-        for (int e = 0; e < NC; ++e)
-          if (!edge || (unsigned)(t0 + e - rho) < 128u)
-            sts16(dst + 2 * kCwRow * e, f16_satfinite(__uint_as_float(r[e])));
+        if (edge) store_c(nc_tag, E1{}, t0, q); else store_c(nc_tag, E0{}, t0, q);
       } else {
-        const uint32_t dst = dP + 2u * t0;
-#pragma unroll
-        for (int e = 0; e < NC; ++e)
-          if (!edge || (unsigned)(t0 + e - 127 + rho) < 128u)
-            sts16(dst + 2 * e, f16_satfinite(__uint_as_float(r[e])));
+        if (edge) store_p(nc_tag, E1{}, t0, q); else store_p(nc_tag, E0{}, t0, q);
       }
     };
     // The five 32-column chunks a lane quarter needs from one half:
@@ -379,9 +417,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     // halves are in the tensor core; the rest, diagonal blocks included, after.
     auto gather = [&](float (&x)[32]) {
 #pragma unroll
-      for (int jj = 0; jj < 32; ++jj)
-        x[jj] = fmaf(f16_sum_f32(lds16(gC + 2 * kCwRow * (31 - jj)), lds16(gP + 2 * kPwRow * jj)), ks,
-                     x[jj]);
+      for (int k = 0; k < 4; ++k) {
+        const uint4 c4 = lds128(gC + 16u * k), p4 = lds128(gP + 16u * k);
+        const uint32_t cv[4] = {c4.x, c4.y, c4.z, c4.w}, pv[4] = {p4.x, p4.y, p4.z, p4.w};
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+          const float2 sum = f16x2_sum_f32x2(cv[w], pv[w]);
+          x[8 * k + 2 * w] = fmaf(sum.x, ks, x[8 * k + 2 * w]);
+          x[8 * k + 2 * w + 1] = fmaf(sum.y, ks, x[8 * k + 2 * w + 1]);
+        }
+      }
     };
 
     for (int it = blockIdx.x; it < n_items; it += gridDim.x) {

@@ -313,6 +313,38 @@ __device__ __forceinline__ uint16_t f16_satfinite(float x) {
 __device__ __forceinline__ float f16_sum_f32(uint16_t a, uint16_t b) {
   return __half2float(__hadd(__ushort_as_half(a), __ushort_as_half(b)));
 }
+// Two fp32 values as fp16x2 (round to nearest even, clamped to the finite
+// range): hi in bits 16-31, lo in bits 0-15.
+__device__ __forceinline__ uint32_t f16x2_satfinite(float hi, float lo) {
+  uint32_t v;
+  asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;" : "=r"(v) : "f"(hi), "f"(lo));
+  return v;
+}
+// Byte permute of the pair {b, a} (a = bytes 0-3, b = bytes 4-7).
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t v;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(v) : "r"(a), "r"(b), "r"(sel));
+  return v;
+}
+__device__ __forceinline__ void sts32(uint32_t addr, uint32_t v) {
+  asm volatile("st.shared.b32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+__device__ __forceinline__ void sts16_lo(uint32_t addr, uint32_t v) {
+  asm volatile("st.shared.b16 [%0], %1;" ::"r"(addr), "h"((uint16_t)(v & 0xFFFFu)) : "memory");
+}
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
+}
+// fp32 values of the fp16x2 sum a + b (rounded in fp16).
+__device__ __forceinline__ float2 f16x2_sum_f32x2(uint32_t a, uint32_t b) {
+  const __half2 s = __hadd2(*reinterpret_cast<const __half2*>(&a), *reinterpret_cast<const __half2*>(&b));
+  return __half22float2(s);
+}
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
