@@ -367,13 +367,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!EDGE || (unsigned)(t0 + 2 * k + 1 - 127 + rho) < 128u) sts16_lo(dst + kRowB * (2 * k + 1), q[k]);
       }
     };
-    // Drain NC columns t0 .. t0 + NC - 1 of A (side 0, C) or B (side 1, P).
+    // Drain NC columns t0 .. t0 + NC - 1 (NC = 16 or 8) of A (side 0, C) or B
+    // (side 1, P).
     auto drain = [&](auto nc_tag, int side, int t0, bool edge) {
       constexpr int NC = decltype(nc_tag)::value;
       uint32_t r[NC];
       const uint32_t src = (side ? tB : tA) + lane_off + (t0 & 127);
-      if constexpr (NC == 32) {
-        tmem_ld32(src, r);
+      if constexpr (NC == 16) {
+        tmem_ld16(src, r);
       } else {
         tmem_ld8(src, r);
       }
@@ -406,7 +407,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       int side, c;
       chunk(g, &side, &c);
-      drain(std::integral_constant<int, 32>{}, side, 128 * half + 32 * c,
+      // the whole chunk in two 16-column loads (fewer live registers)
+      drain(std::integral_constant<int, 16>{}, side, 128 * half + 32 * c,
+            c == (side == 0 ? qd : 3 - qd));
+      drain(std::integral_constant<int, 16>{}, side, 128 * half + 32 * c + 16,
             c == (side == 0 ? qd : 3 - qd));
       chunk(4, &side, &c);
       drain(std::integral_constant<int, 8>{}, side, 128 * half + 32 * c + 8 * g,
