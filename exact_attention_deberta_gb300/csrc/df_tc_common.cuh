@@ -93,13 +93,14 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity,
   if (ptx::mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   for (;;) {
-    if (ptx::mbar_try_wait(bar, parity)) return true;
     if (*abort) return false;
     if ((unsigned long long)(clock64() - t0) > budget) {
       *abort = 1;
       raise_device_error(hdr, DF_ERR_DEVICE_TIMEOUT, where);
       return false;
     }
+    // sleep until the phase completes (at most ~20 us between budget checks)
+    if (ptx::mbar_try_wait_sleep(bar, parity, 20000u)) return true;
   }
 }
 

@@ -530,6 +530,17 @@ cudaError_t launch_far_typed(const Problem& p, const TcMaps& maps, cudaStream_t 
   cudaError_t e = cudaFuncSetAttribute(tc_far_kernel<D, BF16>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
   if (e != cudaSuccess) return e;
+  // setmaxnreg.inc waits until the block's launched registers cover the split
+  // (eight softmax warps at 224, four control warps at 56): refuse to launch if
+  // the compiled register count does not
+  static int regs_ok = -1;
+  if (regs_ok < 0) {
+    cudaFuncAttributes fa;
+    e = cudaFuncGetAttributes(&fa, tc_far_kernel<D, BF16>);
+    if (e != cudaSuccess) return e;
+    regs_ok = fa.numRegs * kFarThreads >= 256 * 224 + 128 * 56 ? 1 : 0;
+  }
+  if (!regs_ok) return cudaErrorInvalidConfiguration;
   const int grid = std::min(p.max_items, far_sm_count());
   tc_far_kernel<D, BF16><<<grid, kFarThreads, bytes, s>>>(p, maps);
   return cudaGetLastError();
