@@ -44,6 +44,8 @@ def parse_args(argv=None):
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--op", choices=["attention", "pack"], default="attention",
+                    help="pack: time the padded <-> packed conversion instead of the attention step")
     return ap.parse_args(argv)
 
 
@@ -255,11 +257,99 @@ def run_reference(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
+def run_pack(args, local):
+    """Padded <-> packed conversion (HBM-bound row gathers): GB/s of df_pack_rows
+    and df_unpack_rows on right-padded batches, against the measured HBM copy
+    rate, with the mask metadata (df_pack_info) timed beside them."""
+    torch.cuda.set_device(local)
+    from exact_attention_deberta_gb300.build import build
+    build()
+    from exact_attention_deberta_gb300 import binding
+    peaks, src = load_peaks()
+    rng = np.random.default_rng(4)
+    shapes = {
+        # 16 x 8192 right-padded, lengths U{2048..8192}, hidden 768 bf16 (q of the long workload)
+        "long_padded_b16_l8192_h768_bf16": (16, 8192, 768, torch.bfloat16,
+                                            rng.integers(2048, 8193, 16)),
+        # MNLI-like padding (lognormal lengths, 93 % padding), hidden 24 x 64 fp16
+        "mnli_like_b16_l512_h1536_fp16": (16, 512, 1536, torch.float16,
+                                          np.clip(np.round(np.random.default_rng(2).lognormal(np.log(30), 0.65, 16)),
+                                                  8, 512).astype(np.int64)),
+    }
+    stream = torch.cuda.current_stream()
+    out_lines = {}
+    for name, (B, L, D, dt, lengths) in shapes.items():
+        mask = torch.from_numpy((np.arange(L)[None, :] < lengths[:, None]).astype(np.uint8)).cuda()
+        x = torch.randn(B, L, D, device="cuda").to(dt)
+        info = binding.df_pack_info(mask)
+        T, row = info.total, D * x.element_size()
+        tokens = torch.empty(max(T, 1), D, dtype=dt, device="cuda")
+        out = torch.empty_like(x)
+        lib = binding.raw_library
+        sp = binding._stream(stream)
+
+        def pack():
+            return lib.df_pack_rows(binding._ptr(x), binding._ptr(info.indices), binding._ptr(info.stats),
+                                    B * L, row, binding._ptr(tokens), sp)
+
+        def unpack():
+            return lib.df_unpack_rows(binding._ptr(tokens), binding._ptr(info.inverse), B * L, row,
+                                      binding._ptr(out), sp)
+
+        def meta():
+            return lib.df_pack_info(binding._ptr(mask), B, L, binding._ptr(info.cu_seqlens),
+                                    binding._ptr(info.indices), binding._ptr(info.inverse),
+                                    binding._ptr(info.stats), sp)
+
+        res = {}
+        for op, fn, nbytes in (("pack", pack, 2 * T * row + 4 * T),
+                               ("unpack", unpack, B * L * row + T * row + 4 * B * L),
+                               ("info", meta, B * L + 4 * (2 * B * L + B + 3))):
+            for _ in range(args.warmup):
+                assert fn() == binding.DF_OK
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize()
+            e0.record(stream)
+            for _ in range(args.steps):
+                fn()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            ms = e0.elapsed_time(e1) / args.steps
+            res[op] = {"ms": ms, "bytes": int(nbytes), "gbs": nbytes / ms / 1e6}
+        # the oracle on the host, same rows
+        t0 = time.perf_counter()
+        from oracle import pack_info as o_info, pack_rows as o_pack, unpack_rows as o_unpack
+        xm = x.view(torch.uint8).cpu().numpy().reshape(B * L, -1)
+        _, idx, inv, _, _ = o_info(mask.cpu().numpy())
+        tok = o_pack(xm, idx)
+        o_unpack(tok, inv)
+        cpu_s = time.perf_counter() - t0
+        out_lines[name] = {"tokens": T, "row_bytes": row, **res,
+                           "cpu_baseline": {"value": (res["pack"]["bytes"] + res["unpack"]["bytes"]) / cpu_s / 1e9,
+                                            "unit": "GB/s", "cores": os.cpu_count(), "kind": "oracle",
+                                            "sample": "whole workload: metadata, pack and unpack, numpy"}}
+    head = out_lines["long_padded_b16_l8192_h768_bf16"]
+    gbs = (head["pack"]["bytes"] + head["unpack"]["bytes"]) / (head["pack"]["ms"] + head["unpack"]["ms"]) / 1e6
+    line = {"metric": "padded<->packed conversion GB/s (pack + unpack bytes)", "value": gbs, "unit": "GB/s",
+            "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "higher_is_better": True,
+            "dtype": "bytes", "data": "synthetic",
+            "config": {"workload": "long_padded_b16_l8192_h768_bf16",
+                       "l2": "inputs larger than L2 (x 201 MB, out 201 MB)"},
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": gbs / peaks["hbm_gbs"], "traffic": None, "peak_source": src + " hbm_gbs"},
+            "workloads": out_lines, "gpu_launches": 2 * args.steps}
+    print(json.dumps(line), flush=True)
+
+
 def main(argv=None):
     args = parse_args(argv)
     rank, world, local = dist_env()
     if args.impl == "reference":
         run_reference(args, rank, world)
+        return
+    if args.op == "pack":
+        if rank == 0:
+            run_pack(args, local)
         return
     assert args.warmup >= 3, "at least 3 warm-up steps"
     torch.cuda.set_device(local)

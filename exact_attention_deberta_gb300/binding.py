@@ -226,4 +226,79 @@ def df_attn_last_launch_count() -> int:
     return int(_lib.df_attn_last_launch_count())
 
 
+_lib.df_pack_info.argtypes = [_vp, _i, _i, _vp, _vp, _vp, _vp, _vp]
+_lib.df_pack_info.restype = _i
+_lib.df_pack_rows.argtypes = [_vp, _vp, _vp, _i, _sz, _vp, _vp]
+_lib.df_pack_rows.restype = _i
+_lib.df_unpack_rows.argtypes = [_vp, _vp, _i, _sz, _vp, _vp]
+_lib.df_unpack_rows.restype = _i
+
+
+class PackedInfo:
+    """Metadata of a padded -> packed conversion, reusable across layers: the
+    packed -> padded row list, its inverse (-1 at padding), cu_seqlens, the
+    token count and the longest sequence."""
+
+    def __init__(self, batch, seqlen, cu_seqlens, indices, inverse, stats, total, max_seqlen):
+        self.batch, self.seqlen = batch, seqlen
+        self.cu_seqlens, self.indices, self.inverse = cu_seqlens, indices, inverse
+        self.stats = stats  # device int32 {T, max_seqlen}
+        self.total, self.max_seqlen = total, max_seqlen
+
+
+def df_pack_info(mask, stream=None) -> PackedInfo:
+    """Metadata of a uint8 mask [B, L] (nonzero = valid).  Reads T and
+    max_seqlen back to the host (one synchronisation of the stream)."""
+    if not mask.is_cuda or mask.dtype != torch.uint8 or mask.dim() != 2 or not mask.is_contiguous():
+        raise ValueError("mask must be a contiguous CUDA uint8 tensor [B, L]")
+    B, L = mask.shape
+    dev = mask.device
+    cu = torch.empty(B + 1, dtype=torch.int32, device=dev)
+    indices = torch.empty(B * L, dtype=torch.int32, device=dev)
+    inverse = torch.empty(B * L, dtype=torch.int32, device=dev)
+    stats = torch.empty(2, dtype=torch.int32, device=dev)
+    _check(_lib.df_pack_info(_ptr(mask), B, L, _ptr(cu), _ptr(indices), _ptr(inverse), _ptr(stats),
+                             _stream(stream)), "df_pack_info")
+    total, max_seqlen = (int(v) for v in stats.cpu())
+    return PackedInfo(B, L, cu, indices[:total], inverse, stats, total, max_seqlen)
+
+
+def _row_bytes(t, lead):
+    return t[0].numel() * t.element_size() if lead == 1 else t[0, 0].numel() * t.element_size()
+
+
+def pack_padded_with_info(hidden_states, attention_mask, stream=None):
+    """[B, L, ...] -> ([T, ...] rows, cu_seqlens, PackedInfo)."""
+    if not hidden_states.is_cuda or not hidden_states.is_contiguous():
+        raise ValueError("hidden_states must be a contiguous CUDA tensor [B, L, ...]")
+    mask = attention_mask.to(torch.uint8).contiguous()
+    info = df_pack_info(mask, stream)
+    B, L = info.batch, info.seqlen
+    if tuple(hidden_states.shape[:2]) != (B, L):
+        raise ValueError("hidden_states and attention_mask disagree on [B, L]")
+    tokens = torch.empty((max(info.total, 1),) + tuple(hidden_states.shape[2:]), dtype=hidden_states.dtype,
+                         device=hidden_states.device)
+    if info.total > 0:
+        _check(_lib.df_pack_rows(_ptr(hidden_states), _ptr(info.indices), _ptr(info.stats), B * L,
+                                 _row_bytes(hidden_states, 2), _ptr(tokens), _stream(stream)),
+               "df_pack_rows")
+    return tokens[:info.total], info.cu_seqlens, info
+
+
+def unpack_packed(packed, cu_seqlens, seqlen, packed_info, stream=None):
+    """[T, ...] -> ([B, L, ...] with zeros at padding, the padded-row mask)."""
+    info = packed_info
+    if seqlen != info.seqlen:
+        raise ValueError("seqlen differs from the metadata's")
+    if not packed.is_cuda or not packed.is_contiguous() or packed.shape[0] != info.total:
+        raise ValueError("packed must be a contiguous CUDA tensor with the metadata's token count")
+    B, L = info.batch, info.seqlen
+    out = torch.empty((B, L) + tuple(packed.shape[1:]), dtype=packed.dtype, device=packed.device)
+    src = packed if info.total > 0 else torch.zeros((1,) + tuple(packed.shape[1:]), dtype=packed.dtype,
+                                                    device=packed.device)
+    _check(_lib.df_unpack_rows(_ptr(src), _ptr(info.inverse), B * L, _row_bytes(out, 2), _ptr(out),
+                               _stream(stream)), "df_unpack_rows")
+    return out, (info.inverse >= 0).view(B, L)
+
+
 raw_library = _lib

@@ -236,6 +236,42 @@ df_status df_attn_fwd_noalloc(const void* q, const void* k, const void* v,
                               int buckets, int max_rel, int span, df_dtype dtype,
                               void* out, df_stream_t stream);
 
+/* ---------------------------------------------------------------------------
+ * Packing between the padded and the packed layout (DisentangledFlash 0.2.0
+ * README, "Packed unpadded inference": right-padded [B, L, hidden] input is
+ * converted to FlashAttention-style [total_tokens, hidden] rows with
+ * cu_seqlens, and the conversion's metadata is reused for every encoder layer
+ * and for unpacking the output).  The valid positions of a uint8 mask [B, L]
+ * (nonzero = valid; holes allowed) are taken in row-major order: packed row k
+ * is padded row indices[k] = b L + i, sequence b owns packed rows
+ * cu_seqlens[b] .. cu_seqlens[b + 1] - 1, and inverse[b L + i] is the packed
+ * row of a valid position or -1.  Rows are moved as bytes, so any element type
+ * works: a row is `row_bytes` bytes (a multiple of 16) and every data pointer
+ * is 16-byte aligned.
+ */
+
+/* Metadata of a mask.  Device outputs, all caller-owned:
+ *   cu_seqlens int32 [B + 1]; indices int32 [B L] (entries 0 .. T - 1 are
+ *   written); inverse int32 [B L]; stats int32 [2] = { T, max_seqlen }.
+ * T is left on the device (reading it back is the caller's synchronisation).
+ * Errors: DF_ERR_INVALID_ARG for a NULL pointer, B < 1, L < 1 or B L > 2^30;
+ * DF_ERR_CUDA if a launch fails.  Three kernel launches. */
+df_status df_pack_info(const uint8_t* mask, int B, int L, int32_t* cu_seqlens,
+                       int32_t* indices, int32_t* inverse, int32_t* stats,
+                       df_stream_t stream);
+
+/* tokens[k] = x[indices[k]] for k < stats[0]; x is [B L] rows, tokens holds at
+ * least stats[0] rows.  Reads T from stats on the device.  Errors:
+ * DF_ERR_INVALID_ARG (NULL pointer, rows < 1, row_bytes = 0 or not a multiple
+ * of 16), DF_ERR_ALIGNMENT (x or tokens not 16-byte aligned), DF_ERR_CUDA. */
+df_status df_pack_rows(const void* x, const int32_t* indices, const int32_t* stats,
+                       int rows, size_t row_bytes, void* tokens, df_stream_t stream);
+
+/* out[r] = tokens[inverse[r]] for inverse[r] >= 0, else zero bytes, for the
+ * `rows` = B L padded rows.  Errors as df_pack_rows. */
+df_status df_unpack_rows(const void* tokens, const int32_t* inverse, int rows,
+                         size_t row_bytes, void* out, df_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

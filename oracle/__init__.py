@@ -14,3 +14,4 @@ from .df_oracle import (  # noqa: F401
     attend_rows,
     metric_flops,
 )
+from .pack import pack_info, pack_rows, unpack_rows  # noqa: F401,E402

@@ -129,3 +129,19 @@ def test_host_side_rejections(binding):
     assert b.raw_library.df_attn_get_device_status(None, None) == b.DF_ERR_INVALID_ARG
     assert b.raw_library.df_rel_index_table(256, 512, 256, 0, ctypes.c_void_p(0x1000),
                                             None) == b.DF_ERR_INVALID_ARG
+
+
+def test_pack_entry_points_check_arguments_on_the_host(binding):
+    lib = binding.raw_library
+    ok_ptr, odd_ptr = ctypes.c_void_p(16 * 1024), ctypes.c_void_p(16 * 1024 + 8)
+    inv = ctypes.c_void_p(64 * 1024)
+    # rows must be 16-byte multiples, pointers 16-byte aligned, sizes positive
+    assert lib.df_pack_rows(ok_ptr, inv, inv, 4, 8, ok_ptr, None) == binding.DF_ERR_INVALID_ARG
+    assert lib.df_pack_rows(ok_ptr, inv, inv, 0, 16, ok_ptr, None) == binding.DF_ERR_INVALID_ARG
+    assert lib.df_pack_rows(odd_ptr, inv, inv, 4, 16, ok_ptr, None) == binding.DF_ERR_ALIGNMENT
+    assert lib.df_pack_rows(None, inv, inv, 4, 16, ok_ptr, None) == binding.DF_ERR_INVALID_ARG
+    assert lib.df_unpack_rows(ok_ptr, inv, 4, 24, ok_ptr, None) == binding.DF_ERR_INVALID_ARG
+    assert lib.df_unpack_rows(ok_ptr, inv, 4, 32, odd_ptr, None) == binding.DF_ERR_ALIGNMENT
+    assert lib.df_pack_info(ok_ptr, 0, 8, inv, inv, inv, inv, None) == binding.DF_ERR_INVALID_ARG
+    assert lib.df_pack_info(ok_ptr, 2, 0, inv, inv, inv, inv, None) == binding.DF_ERR_INVALID_ARG
+    assert lib.df_pack_info(None, 2, 8, inv, inv, inv, inv, None) == binding.DF_ERR_INVALID_ARG
