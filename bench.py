@@ -44,8 +44,8 @@ def parse_args(argv=None):
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--op", choices=["attention", "pack"], default="attention",
-                    help="pack: time the padded <-> packed conversion instead of the attention step")
+    ap.add_argument("--op", choices=["attention", "pack", "linear"], default="attention",
+                    help="pack: the padded <-> packed conversion; linear: the QKV and PK/PQ projections")
     return ap.parse_args(argv)
 
 
@@ -341,15 +341,67 @@ def run_pack(args, local):
     print(json.dumps(line), flush=True)
 
 
+def run_linear(args, local):
+    """The projections that feed the attention (df_linear): the fused QKV
+    projection of the 16 x 8192-token workload (hidden 768 -> 3 x 768, bf16) and
+    the PK/PQ projection of 512 relative embeddings, as TFLOP/s against the
+    measured dense bf16 rate (the kernel is timed alone: burst figure)."""
+    torch.cuda.set_device(local)
+    from exact_attention_deberta_gb300.build import build
+    build()
+    from exact_attention_deberta_gb300 import binding
+    peaks, src = load_peaks()
+    g = torch.Generator().manual_seed(4)
+    res = {}
+    for name, (M, K, N, n_out) in {"qkv_t131072_h768_bf16": (131072, 768, 768, 3),
+                                   "pkpq_r512_h768_bf16": (512, 768, 768, 2)}.items():
+        x = torch.randn(M, K, generator=g).to(torch.bfloat16).cuda()
+        ws = [(torch.randn(N, K, generator=g) / K ** 0.5).to(torch.bfloat16).cuda() for _ in range(n_out)]
+        bs = [(torch.randn(N, generator=g) * 0.1).to(torch.bfloat16).cuda() for _ in range(n_out)]
+        outs = [torch.empty(M, N, dtype=torch.bfloat16, device="cuda") for _ in range(n_out)]
+        for _ in range(args.warmup):
+            binding.df_linear(x, ws, bs, outs)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record()
+        for _ in range(args.steps):
+            binding.df_linear(x, ws, bs, outs)
+        e1.record()
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / args.steps
+        flops = 2.0 * M * K * N * n_out
+        res[name] = {"ms": ms, "flops": flops, "tflops": flops / ms / 1e9,
+                     "bytes": 2 * (M * K + n_out * (N * K + N + M * N))}
+    # the oracle (numpy float64 matmul) on a 1024-row sample of the QKV case
+    from oracle import linear as o_linear
+    xs = np.random.default_rng(0).standard_normal((1024, 768))
+    wn = [np.random.default_rng(i).standard_normal((768, 768)) for i in range(3)]
+    t0 = time.perf_counter()
+    o_linear(xs, wn)
+    cpu = 2.0 * 1024 * 768 * 768 * 3 / (time.perf_counter() - t0) / 1e12
+    head = res["qkv_t131072_h768_bf16"]
+    line = {"metric": "QKV projection TFLOP/s (2 M K N per output)", "value": head["tflops"], "unit": "TFLOP/s",
+            "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": head["ms"],
+            "higher_is_better": True, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": "qkv_t131072_h768_bf16", "l2": "x 201 MB, outputs 604 MB: larger than L2"},
+            "roofline": {"bound": "tensor", "achieved": head["tflops"], "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                         "frac": head["tflops"] / peaks["bf16_tflops"], "traffic": None,
+                         "peak_source": src + " bf16_tflops (burst)"},
+            "workloads": res, "gpu_launches": args.steps,
+            "cpu_baseline": {"value": cpu, "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
+                             "sample": "1024 x 768 rows by three 768 x 768 weights, float64 numpy"}}
+    print(json.dumps(line), flush=True)
+
+
 def main(argv=None):
     args = parse_args(argv)
     rank, world, local = dist_env()
     if args.impl == "reference":
         run_reference(args, rank, world)
         return
-    if args.op == "pack":
+    if args.op in ("pack", "linear"):
         if rank == 0:
-            run_pack(args, local)
+            (run_pack if args.op == "pack" else run_linear)(args, local)
         return
     assert args.warmup >= 3, "at least 3 warm-up steps"
     torch.cuda.set_device(local)

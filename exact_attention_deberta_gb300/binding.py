@@ -301,4 +301,57 @@ def unpack_packed(packed, cu_seqlens, seqlen, packed_info, stream=None):
     return out, (info.inverse >= 0).view(B, L)
 
 
+_PP = ctypes.POINTER(ctypes.c_void_p)
+_lib.df_linear.argtypes = [_vp, _i, _i, _i, _PP, _PP, _i, _PP, _i, _vp, _vp]
+_lib.df_linear.restype = _i
+
+
+def _ptr_array(ts):
+    arr = (ctypes.c_void_p * len(ts))()
+    for i, t in enumerate(ts):
+        arr[i] = None if t is None else t.data_ptr()
+    return arr
+
+
+def df_linear(x, weights, biases=None, outs=None, status=None, stream=None):
+    """[x . W_i^T + b_i] for 1..3 weights W_i [N, K] (nn.Linear layout) sharing x [M, K]."""
+    if x.dim() != 2 or not x.is_cuda or not x.is_contiguous() or x.dtype not in (torch.bfloat16, torch.float16):
+        raise ValueError("x must be a contiguous CUDA bf16/fp16 matrix [M, K]")
+    M, K = x.shape
+    N = weights[0].shape[0]
+    for w in weights:
+        if tuple(w.shape) != (N, K) or w.dtype != x.dtype or not w.is_contiguous() or not w.is_cuda:
+            raise ValueError("every weight must be a contiguous CUDA [N, K] matrix of x's dtype")
+    if biases is not None:
+        for b in biases:
+            if b is not None and (b.shape != (N,) or b.dtype != x.dtype or not b.is_contiguous()):
+                raise ValueError("biases must be [N] vectors of x's dtype")
+    if outs is None:
+        outs = [torch.empty(M, N, dtype=x.dtype, device=x.device) for _ in weights]
+    st = _lib.df_linear(_ptr(x), M, K, len(weights), _ptr_array(weights),
+                        _ptr_array(biases) if biases is not None else None, N, _ptr_array(outs),
+                        _DTYPE[x.dtype], _ptr(status), _stream(stream))
+    _check(st, "df_linear")
+    return outs
+
+
+def qkv_projection(hidden, w_qkv, b_qkv, heads, stream=None):
+    """Fused QKV projection: hidden [T, hidden] with the stacked weight [3 H d, hidden]
+    (and bias [3 H d]) -> q, k, v, each [T, H, d]."""
+    n3 = w_qkv.shape[0]
+    n = n3 // 3
+    ws = [w_qkv[i * n:(i + 1) * n] for i in range(3)]
+    bs = None if b_qkv is None else [b_qkv[i * n:(i + 1) * n] for i in range(3)]
+    outs = df_linear(hidden, ws, bs, stream=stream)
+    T = hidden.shape[0]
+    return [o.view(T, heads, n // heads) for o in outs]
+
+
+def rel_projection(rel_embeddings, w_key, b_key, w_query, b_query, heads, stream=None):
+    """PK = rel . W_k^T + b_k and PQ = rel . W_q^T + b_q, each [2 span, H, d]."""
+    outs = df_linear(rel_embeddings, [w_key, w_query], [b_key, b_query], stream=stream)
+    R, n = outs[0].shape
+    return [o.view(R, heads, n // heads) for o in outs]
+
+
 raw_library = _lib

@@ -272,6 +272,26 @@ df_status df_pack_rows(const void* x, const int32_t* indices, const int32_t* sta
 df_status df_unpack_rows(const void* tokens, const int32_t* inverse, int rows,
                          size_t row_bytes, void* out, df_stream_t stream);
 
+/* ---------------------------------------------------------------------------
+ * Projections that feed the attention (DisentangledFlash 0.2.0 README,
+ * "Status": the fused QKV projection; and the relative-position projections PK
+ * and PQ of the relative embeddings): for i < n_out (1..3),
+ *     out[i][m][n] = sum_k x[m][k] w[i][n][k] + bias[i][n]
+ * in fp32 on the tensor cores, rounded to `dtype` (bf16 or fp16).  x is
+ * [M, K], every w[i] is [N, K] (the nn.Linear weight layout), bias[i] is [N]
+ * (a NULL `bias` array or NULL entry means no bias) and out[i] is [M, N], all
+ * row-major device buffers of `dtype`.  `w`, `bias` and `out` are HOST arrays of
+ * n_out device pointers.  With the stacked QKV weight [3 N, K] pass its three
+ * row blocks as w[0..2]; out[0..2] are then Q, K, V in the [M, H, d] layout.
+ * Constraints: K a multiple of 64, N a multiple of 256, every pointer 16-byte
+ * aligned.  `status` (a device int32, may be NULL) receives
+ * DF_ERR_DEVICE_TIMEOUT if a bounded wait of the kernel runs out; the caller
+ * zeroes it.  Errors: DF_ERR_INVALID_ARG (NULL pointer, sizes < 1, n_out out of
+ * 1..3), DF_ERR_UNSUPPORTED (dtype, K or N), DF_ERR_ALIGNMENT, DF_ERR_CUDA. */
+df_status df_linear(const void* x, int M, int K, int n_out, const void* const* w,
+                    const void* const* bias, int N, void* const* out, df_dtype dtype,
+                    int32_t* status, df_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -15,3 +15,4 @@ from .df_oracle import (  # noqa: F401
     metric_flops,
 )
 from .pack import pack_info, pack_rows, unpack_rows  # noqa: F401,E402
+from .linear import linear  # noqa: F401,E402

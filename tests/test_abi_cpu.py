@@ -145,3 +145,17 @@ def test_pack_entry_points_check_arguments_on_the_host(binding):
     assert lib.df_pack_info(ok_ptr, 0, 8, inv, inv, inv, inv, None) == binding.DF_ERR_INVALID_ARG
     assert lib.df_pack_info(ok_ptr, 2, 0, inv, inv, inv, inv, None) == binding.DF_ERR_INVALID_ARG
     assert lib.df_pack_info(None, 2, 8, inv, inv, inv, inv, None) == binding.DF_ERR_INVALID_ARG
+
+
+def test_linear_checks_arguments_on_the_host(binding):
+    lib = binding.raw_library
+    p = ctypes.c_void_p(16 * 1024)
+    odd = ctypes.c_void_p(16 * 1024 + 4)
+    arr = (ctypes.c_void_p * 3)(16 * 1024, 16 * 1024, 16 * 1024)
+    assert lib.df_linear(p, 4, 64, 0, arr, None, 256, arr, binding.DF_BF16, None, None) == binding.DF_ERR_INVALID_ARG
+    assert lib.df_linear(p, 4, 64, 4, arr, None, 256, arr, binding.DF_BF16, None, None) == binding.DF_ERR_INVALID_ARG
+    assert lib.df_linear(p, 0, 64, 1, arr, None, 256, arr, binding.DF_BF16, None, None) == binding.DF_ERR_INVALID_ARG
+    assert lib.df_linear(p, 4, 48, 1, arr, None, 256, arr, binding.DF_BF16, None, None) == binding.DF_ERR_UNSUPPORTED
+    assert lib.df_linear(p, 4, 64, 1, arr, None, 200, arr, binding.DF_BF16, None, None) == binding.DF_ERR_UNSUPPORTED
+    assert lib.df_linear(p, 4, 64, 1, arr, None, 256, arr, binding.DF_FP32, None, None) == binding.DF_ERR_UNSUPPORTED
+    assert lib.df_linear(odd, 4, 64, 1, arr, None, 256, arr, binding.DF_BF16, None, None) == binding.DF_ERR_ALIGNMENT
