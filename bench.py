@@ -44,8 +44,9 @@ def parse_args(argv=None):
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--op", choices=["attention", "pack", "linear"], default="attention",
-                    help="pack: the padded <-> packed conversion; linear: the QKV and PK/PQ projections")
+    ap.add_argument("--op", choices=["attention", "pack", "linear", "encoder"], default="attention",
+                    help="pack: the padded <-> packed conversion; linear: the QKV and PK/PQ projections; "
+                         "encoder: a 12-layer DeBERTa-v3-base encoder on synthetic weights")
     return ap.parse_args(argv)
 
 
@@ -393,15 +394,71 @@ def run_linear(args, local):
     print(json.dumps(line), flush=True)
 
 
+def run_encoder(args, local):
+    """The pages' benchmark workload in kind: a 12-layer DeBERTa-v3-base encoder
+    (hidden 768, 12 heads, FFN 3072, buckets 256, max_rel 512) on the packed
+    layout with synthetic weights, packed lengths uniform in [0.6 L, L]
+    (L = 8192), bf16; latency of one forward (mean over `steps` fresh inputs)."""
+    torch.cuda.set_device(local)
+    from exact_attention_deberta_gb300.build import build
+    build()
+    from exact_attention_deberta_gb300.encoder import Encoder, EncoderConfig, synthetic_weights
+    cfg = EncoderConfig()
+    layers, shared = synthetic_weights(cfg, seed=0)
+    enc = Encoder(cfg, layers, shared)
+    L = 8192
+    rng = np.random.default_rng(0)
+    res = {}
+    for B in (1, 16):
+        times, toks = [], []
+        for it in range(args.warmup + args.steps):
+            lengths = rng.integers(int(0.6 * L), L + 1, B)
+            T = int(lengths.sum())
+            cu = torch.tensor(np.concatenate([[0], np.cumsum(lengths)]), dtype=torch.int32, device="cuda")
+            h = torch.randn(T, cfg.hidden, device="cuda").to(torch.bfloat16)
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            enc(h, cu, L)
+            e1.record()
+            torch.cuda.synchronize()
+            if it >= args.warmup:
+                times.append(e0.elapsed_time(e1))
+                toks.append(T)
+        ms = float(np.mean(times))
+        res[f"b{B}_l{L}"] = {"ms_mean": ms, "ms_median": float(np.median(times)), "tokens_mean": float(np.mean(toks)),
+                             "tokens_per_s": float(np.sum(toks) / (np.sum(times) / 1e3))}
+    # the oracle: one layer over one 256-token sequence on the host
+    import oracle as o
+    p64 = [{k: v.double().cpu().numpy() for k, v in layers[0].items()}]
+    x = np.random.default_rng(1).standard_normal((256, cfg.hidden))
+    rel = shared["rel_embeddings"].double().cpu().numpy()
+    t0 = time.perf_counter()
+    o.encoder(x, p64, rel, np.ones(cfg.hidden), np.zeros(cfg.hidden), np.array([0, 256]), cfg.heads,
+              buckets=cfg.buckets, max_rel=cfg.max_rel, span=cfg.span, eps=cfg.eps)
+    cpu_tps = 256 / (time.perf_counter() - t0) / cfg.layers
+    head = res["b1_l8192"]
+    line = {"metric": "DeBERTa-v3-base encoder forward latency (12 layers, packed)", "value": head["ms_mean"],
+            "unit": "ms", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "higher_is_better": False,
+            "dtype": "bf16", "data": "synthetic (random weights; no checkpoint in the container)",
+            "config": {"workload": "v3base_encoder_b1_l8192", "lengths": "uniform in [0.6 L, L]"},
+            "workloads": res, "gpu_launches": None,
+            "context": {"pages_h200_bf16_ms": {"b1_l8192": 39.35, "b16_l8192": 708.29},
+                        "note": "the pages' figures: H200, trained weights; context, not a like-for-like target"},
+            "cpu_baseline": {"value": cpu_tps, "unit": "tokens/s (12 layers)", "cores": os.cpu_count(),
+                             "kind": "oracle", "sample": "one layer over one 256-token sequence, float64 numpy"}}
+    print(json.dumps(line), flush=True)
+
+
 def main(argv=None):
     args = parse_args(argv)
     rank, world, local = dist_env()
     if args.impl == "reference":
         run_reference(args, rank, world)
         return
-    if args.op in ("pack", "linear"):
+    if args.op in ("pack", "linear", "encoder"):
         if rank == 0:
-            (run_pack if args.op == "pack" else run_linear)(args, local)
+            {"pack": run_pack, "linear": run_linear, "encoder": run_encoder}[args.op](args, local)
         return
     assert args.warmup >= 3, "at least 3 warm-up steps"
     torch.cuda.set_device(local)

@@ -302,7 +302,7 @@ def unpack_packed(packed, cu_seqlens, seqlen, packed_info, stream=None):
 
 
 _PP = ctypes.POINTER(ctypes.c_void_p)
-_lib.df_linear.argtypes = [_vp, _i, _i, _i, _PP, _PP, _i, _PP, _i, _vp, _vp]
+_lib.df_linear.argtypes = [_vp, _i, _i, _i, _PP, _PP, _i, _PP, _i, _i, _vp, _vp]
 _lib.df_linear.restype = _i
 
 
@@ -313,8 +313,11 @@ def _ptr_array(ts):
     return arr
 
 
-def df_linear(x, weights, biases=None, outs=None, status=None, stream=None):
-    """[x . W_i^T + b_i] for 1..3 weights W_i [N, K] (nn.Linear layout) sharing x [M, K]."""
+LINEAR_NONE, LINEAR_GELU = 0, 1
+
+
+def df_linear(x, weights, biases=None, outs=None, status=None, stream=None, activation=LINEAR_NONE):
+    """[act(x . W_i^T + b_i)] for 1..3 weights W_i [N, K] (nn.Linear layout) sharing x [M, K]."""
     if x.dim() != 2 or not x.is_cuda or not x.is_contiguous() or x.dtype not in (torch.bfloat16, torch.float16):
         raise ValueError("x must be a contiguous CUDA bf16/fp16 matrix [M, K]")
     M, K = x.shape
@@ -330,7 +333,7 @@ def df_linear(x, weights, biases=None, outs=None, status=None, stream=None):
         outs = [torch.empty(M, N, dtype=x.dtype, device=x.device) for _ in weights]
     st = _lib.df_linear(_ptr(x), M, K, len(weights), _ptr_array(weights),
                         _ptr_array(biases) if biases is not None else None, N, _ptr_array(outs),
-                        _DTYPE[x.dtype], _ptr(status), _stream(stream))
+                        int(activation), _DTYPE[x.dtype], _ptr(status), _stream(stream))
     _check(st, "df_linear")
     return outs
 
@@ -352,6 +355,20 @@ def rel_projection(rel_embeddings, w_key, b_key, w_query, b_query, heads, stream
     outs = df_linear(rel_embeddings, [w_key, w_query], [b_key, b_query], stream=stream)
     R, n = outs[0].shape
     return [o.view(R, heads, n // heads) for o in outs]
+
+
+_lib.df_layernorm.argtypes = [_vp, _vp, _vp, _vp, _i, _i, ctypes.c_float, _vp, _i, _vp]
+_lib.df_layernorm.restype = _i
+
+
+def df_layernorm(x, gamma, beta, residual=None, eps=1e-7, out=None, stream=None):
+    """LayerNorm(x + residual) * gamma + beta over the last dimension of [M, N]."""
+    M, N = x.shape
+    if out is None:
+        out = torch.empty_like(x)
+    _check(_lib.df_layernorm(_ptr(x), _ptr(residual), _ptr(gamma), _ptr(beta), M, N, float(eps), _ptr(out),
+                             _DTYPE[x.dtype], _stream(stream)), "df_layernorm")
+    return out
 
 
 raw_library = _lib

@@ -52,6 +52,7 @@ struct LinSmem {
 
 struct LinArgs {
   int M, K, N, n_out;
+  int act;  // 0: none, 1: GELU (erf form)
   const void* bias[3];
   void* out[3];
   int32_t* status;
@@ -205,8 +206,12 @@ __global__ void __launch_bounds__(kLinThreads, 1)
           uint32_t w[16];
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
-            const float a = __uint_as_float(r[2 * e]) + sb[32 * c + 2 * e];
-            const float b = __uint_as_float(r[2 * e + 1]) + sb[32 * c + 2 * e + 1];
+            float a = __uint_as_float(r[2 * e]) + sb[32 * c + 2 * e];
+            float b = __uint_as_float(r[2 * e + 1]) + sb[32 * c + 2 * e + 1];
+            if (args.act == 1) {  // GELU: x (1 + erf(x / sqrt 2)) / 2
+              a = 0.5f * a * (1.f + erff(a * 0.70710678118654752f));
+              b = 0.5f * b * (1.f + erff(b * 0.70710678118654752f));
+            }
             w[e] = BF16 ? pack_bf16x2(a, b) : pack_f16x2(a, b);
           }
           uint4* d4 = reinterpret_cast<uint4*>(dst + 32 * c);
@@ -287,9 +292,10 @@ cudaError_t launch_linear(const LinArgs& a, const LinMaps& maps, cudaStream_t s)
 using namespace dfa;
 
 extern "C" df_status df_linear(const void* x, int M, int K, int n_out, const void* const* w,
-                               const void* const* bias, int N, void* const* out, df_dtype dtype,
-                               int32_t* status, df_stream_t stream) {
+                               const void* const* bias, int N, void* const* out, int activation,
+                               df_dtype dtype, int32_t* status, df_stream_t stream) {
   if (!x || !w || !out || M < 1 || K < 1 || N < 1 || n_out < 1 || n_out > 3) return DF_ERR_INVALID_ARG;
+  if (activation != 0 && activation != 1) return DF_ERR_INVALID_ARG;
   if (dtype != DF_BF16 && dtype != DF_FP16) return DF_ERR_UNSUPPORTED;
   if (K % kBK != 0 || N % kBN != 0) return DF_ERR_UNSUPPORTED;
   if ((long long)M * K > (1ll << 40)) return DF_ERR_INVALID_ARG;
@@ -299,6 +305,7 @@ extern "C" df_status df_linear(const void* x, int M, int K, int n_out, const voi
   a.K = K;
   a.N = N;
   a.n_out = n_out;
+  a.act = activation;
   a.status = status;
   LinMaps maps;
   const bool bf16 = dtype == DF_BF16;

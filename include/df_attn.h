@@ -275,9 +275,11 @@ df_status df_unpack_rows(const void* tokens, const int32_t* inverse, int rows,
 /* ---------------------------------------------------------------------------
  * Projections that feed the attention (DisentangledFlash 0.2.0 README,
  * "Status": the fused QKV projection; and the relative-position projections PK
- * and PQ of the relative embeddings): for i < n_out (1..3),
- *     out[i][m][n] = sum_k x[m][k] w[i][n][k] + bias[i][n]
- * in fp32 on the tensor cores, rounded to `dtype` (bf16 or fp16).  x is
+ * and PQ of the relative embeddings), also the encoder's output and
+ * feed-forward projections: for i < n_out (1..3),
+ *     out[i][m][n] = act( sum_k x[m][k] w[i][n][k] + bias[i][n] )
+ * in fp32 on the tensor cores, rounded to `dtype` (bf16 or fp16); act is the
+ * identity (activation 0) or GELU x (1 + erf(x / sqrt 2)) / 2 (activation 1).  x is
  * [M, K], every w[i] is [N, K] (the nn.Linear weight layout), bias[i] is [N]
  * (a NULL `bias` array or NULL entry means no bias) and out[i] is [M, N], all
  * row-major device buffers of `dtype`.  `w`, `bias` and `out` are HOST arrays of
@@ -287,10 +289,24 @@ df_status df_unpack_rows(const void* tokens, const int32_t* inverse, int rows,
  * aligned.  `status` (a device int32, may be NULL) receives
  * DF_ERR_DEVICE_TIMEOUT if a bounded wait of the kernel runs out; the caller
  * zeroes it.  Errors: DF_ERR_INVALID_ARG (NULL pointer, sizes < 1, n_out out of
- * 1..3), DF_ERR_UNSUPPORTED (dtype, K or N), DF_ERR_ALIGNMENT, DF_ERR_CUDA. */
+ * 1..3, activation not 0 or 1), DF_ERR_UNSUPPORTED (dtype, K or N),
+ * DF_ERR_ALIGNMENT, DF_ERR_CUDA. */
 df_status df_linear(const void* x, int M, int K, int n_out, const void* const* w,
-                    const void* const* bias, int N, void* const* out, df_dtype dtype,
-                    int32_t* status, df_stream_t stream);
+                    const void* const* bias, int N, void* const* out, int activation,
+                    df_dtype dtype, int32_t* status, df_stream_t stream);
+
+/* Residual add + LayerNorm, the normalisation of a DeBERTa encoder layer (after
+ * the attention output and after the feed-forward block) and of its relative
+ * embeddings: for every row m of [M, N],
+ *     y = x[m] + residual[m]   (residual may be NULL)
+ *     out[m] = (y - mean(y)) / sqrt(var(y) + eps) * gamma + beta
+ * with fp32 statistics (population variance), rounded to `dtype` (bf16 or
+ * fp16).  gamma, beta are [N] in `dtype`; every buffer is a row-major device
+ * buffer, 16-byte aligned.  N must be 256 v with v in {1, 2, 3, 4, 6, 8}.
+ * Errors: DF_ERR_INVALID_ARG (NULL pointer, M < 1, eps <= 0),
+ * DF_ERR_UNSUPPORTED (dtype or N), DF_ERR_ALIGNMENT, DF_ERR_CUDA. */
+df_status df_layernorm(const void* x, const void* residual, const void* gamma, const void* beta,
+                       int M, int N, float eps, void* out, df_dtype dtype, df_stream_t stream);
 
 #ifdef __cplusplus
 }

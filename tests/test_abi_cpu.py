@@ -152,10 +152,23 @@ def test_linear_checks_arguments_on_the_host(binding):
     p = ctypes.c_void_p(16 * 1024)
     odd = ctypes.c_void_p(16 * 1024 + 4)
     arr = (ctypes.c_void_p * 3)(16 * 1024, 16 * 1024, 16 * 1024)
-    assert lib.df_linear(p, 4, 64, 0, arr, None, 256, arr, binding.DF_BF16, None, None) == binding.DF_ERR_INVALID_ARG
-    assert lib.df_linear(p, 4, 64, 4, arr, None, 256, arr, binding.DF_BF16, None, None) == binding.DF_ERR_INVALID_ARG
-    assert lib.df_linear(p, 0, 64, 1, arr, None, 256, arr, binding.DF_BF16, None, None) == binding.DF_ERR_INVALID_ARG
-    assert lib.df_linear(p, 4, 48, 1, arr, None, 256, arr, binding.DF_BF16, None, None) == binding.DF_ERR_UNSUPPORTED
-    assert lib.df_linear(p, 4, 64, 1, arr, None, 200, arr, binding.DF_BF16, None, None) == binding.DF_ERR_UNSUPPORTED
-    assert lib.df_linear(p, 4, 64, 1, arr, None, 256, arr, binding.DF_FP32, None, None) == binding.DF_ERR_UNSUPPORTED
-    assert lib.df_linear(odd, 4, 64, 1, arr, None, 256, arr, binding.DF_BF16, None, None) == binding.DF_ERR_ALIGNMENT
+    assert lib.df_linear(p, 4, 64, 0, arr, None, 256, arr, 0, binding.DF_BF16, None, None) == binding.DF_ERR_INVALID_ARG
+    assert lib.df_linear(p, 4, 64, 4, arr, None, 256, arr, 0, binding.DF_BF16, None, None) == binding.DF_ERR_INVALID_ARG
+    assert lib.df_linear(p, 0, 64, 1, arr, None, 256, arr, 0, binding.DF_BF16, None, None) == binding.DF_ERR_INVALID_ARG
+    assert lib.df_linear(p, 4, 48, 1, arr, None, 256, arr, 0, binding.DF_BF16, None, None) == binding.DF_ERR_UNSUPPORTED
+    assert lib.df_linear(p, 4, 64, 1, arr, None, 200, arr, 0, binding.DF_BF16, None, None) == binding.DF_ERR_UNSUPPORTED
+    assert lib.df_linear(p, 4, 64, 1, arr, None, 256, arr, 0, binding.DF_FP32, None, None) == binding.DF_ERR_UNSUPPORTED
+    assert lib.df_linear(odd, 4, 64, 1, arr, None, 256, arr, 0, binding.DF_BF16, None, None) == binding.DF_ERR_ALIGNMENT
+    assert lib.df_linear(p, 4, 64, 1, arr, None, 256, arr, 2, binding.DF_BF16, None, None) == binding.DF_ERR_INVALID_ARG
+
+
+def test_layernorm_checks_arguments_on_the_host(binding):
+    lib = binding.raw_library
+    p, odd = ctypes.c_void_p(16 * 1024), ctypes.c_void_p(16 * 1024 + 2)
+    f = ctypes.c_float
+    assert lib.df_layernorm(p, None, p, p, 0, 768, f(1e-7), p, binding.DF_BF16, None) == binding.DF_ERR_INVALID_ARG
+    assert lib.df_layernorm(p, None, p, p, 4, 768, f(0.0), p, binding.DF_BF16, None) == binding.DF_ERR_INVALID_ARG
+    assert lib.df_layernorm(p, None, p, p, 4, 700, f(1e-7), p, binding.DF_BF16, None) == binding.DF_ERR_UNSUPPORTED
+    assert lib.df_layernorm(p, None, p, p, 4, 1280, f(1e-7), p, binding.DF_BF16, None) == binding.DF_ERR_UNSUPPORTED
+    assert lib.df_layernorm(p, None, p, p, 4, 768, f(1e-7), p, binding.DF_FP32, None) == binding.DF_ERR_UNSUPPORTED
+    assert lib.df_layernorm(p, odd, p, p, 4, 768, f(1e-7), p, binding.DF_BF16, None) == binding.DF_ERR_ALIGNMENT

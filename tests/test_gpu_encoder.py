@@ -1,0 +1,64 @@
+"""GPU parity of the encoder's kernels against the float64 oracle on the same
+rounded inputs: the residual LayerNorm, the GELU epilogue of the projection,
+and two whole DeBERTa-v3 encoder layers on a packed batch of three sequences."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+
+pytestmark = pytest.mark.gpu
+
+
+def _np(t):
+    return t.double().cpu().numpy()
+
+
+@pytest.mark.parametrize("M,N,dtype,res", [(1, 768, torch.bfloat16, True), (1000, 768, torch.bfloat16, False),
+                                           (37, 1024, torch.float16, True), (513, 256, torch.float16, True),
+                                           (64, 2048, torch.bfloat16, True)])
+def test_layernorm_matches_oracle(lib, M, N, dtype, res):
+    g = torch.Generator().manual_seed(M + N)
+    x = (torch.randn(M, N, generator=g) * 2 + 0.5).to(dtype).cuda()
+    r = torch.randn(M, N, generator=g).to(dtype).cuda() if res else None
+    gam = (1 + 0.1 * torch.randn(N, generator=g)).to(dtype).cuda()
+    bet = (0.1 * torch.randn(N, generator=g)).to(dtype).cuda()
+    out = lib.df_layernorm(x, gam, bet, residual=r, eps=1e-7)
+    y = _np(x) + (_np(r) if res else 0)
+    want = oracle.layer_norm(y, _np(gam), _np(bet), 1e-7)
+    tol = 2e-2 if dtype == torch.bfloat16 else 4e-3
+    assert np.abs(_np(out) - want).max() <= tol * (1 + np.abs(want).max())
+
+
+def test_gelu_epilogue(lib):
+    g = torch.Generator().manual_seed(3)
+    x = torch.randn(300, 768, generator=g).to(torch.bfloat16).cuda()
+    w = (torch.randn(3072, 768, generator=g) / 768 ** 0.5).to(torch.bfloat16).cuda()
+    b = (0.1 * torch.randn(3072, generator=g)).to(torch.bfloat16).cuda()
+    (y,) = lib.df_linear(x, [w], [b], activation=lib.LINEAR_GELU)
+    (lin,) = oracle.linear(_np(x), [_np(w)], [_np(b)])
+    want = oracle.gelu(lin)
+    err = np.abs(_np(y) - want)
+    assert (err <= 2e-2 + 1e-2 * np.abs(want)).all(), float(err.max())
+
+
+def test_two_encoder_layers_match_oracle(lib):
+    from exact_attention_deberta_gb300.encoder import Encoder, EncoderConfig, synthetic_weights
+    cfg = EncoderConfig(hidden=768, heads=12, layers=2, ffn=3072)
+    layers, shared = synthetic_weights(cfg, seed=5)
+    lengths = [300, 150, 77]
+    T = sum(lengths)
+    cu = torch.tensor(np.concatenate([[0], np.cumsum(lengths)]), dtype=torch.int32)
+    g = torch.Generator().manual_seed(9)
+    h = torch.randn(T, cfg.hidden, generator=g).to(torch.bfloat16).cuda()
+    out = Encoder(cfg, layers, shared)(h, cu.cuda(), max(lengths))
+    torch.cuda.synchronize()
+    want = oracle.encoder(_np(h), [{k: _np(v) for k, v in p.items()} for p in layers],
+                          _np(shared["rel_embeddings"]), _np(shared["rel_g"]), _np(shared["rel_b"]), cu.numpy(),
+                          cfg.heads, buckets=cfg.buckets, max_rel=cfg.max_rel, span=cfg.span, eps=cfg.eps)
+    got = _np(out)
+    assert np.isfinite(got).all()
+    err = np.abs(got - want)
+    # bf16 rounding after every step of two layers: a few bf16 ulps of O(1) values
+    assert err.mean() < 1e-2 and err.max() < 1.5e-1, (float(err.mean()), float(err.max()))
