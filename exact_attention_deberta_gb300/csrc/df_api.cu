@@ -115,7 +115,7 @@ df_status check_params(int H, int L, int d, df_dtype dtype, int buckets, int max
   if (H < 1 || L < 1 || span < 1) return DF_ERR_INVALID_ARG;
   if (dtype != DF_BF16 && dtype != DF_FP16 && dtype != DF_FP32) return DF_ERR_INVALID_ARG;
   if (buckets > 0 && (buckets / 2 < 1 || buckets / 2 >= max_rel - 1)) return DF_ERR_INVALID_ARG;
-  if (d != 64 && d != 128) return DF_ERR_UNSUPPORTED;
+  if (d != 32 && d != 64 && d != 128) return DF_ERR_UNSUPPORTED;
   if (L > 65536 || span > 65536 || H > 1024) return DF_ERR_UNSUPPORTED;
   return DF_OK;
 }
@@ -253,7 +253,7 @@ df_status df_attn_fwd(const void* q, const void* k, const void* v, const void* p
   if (launch_plan(p, s) != cudaSuccess) return DF_ERR_CUDA;
   int launches = 0;
   cudaError_t e;
-  if (dtype != DF_FP32 && tc_enabled()) {
+  if (dtype != DF_FP32 && d != 32 && tc_enabled()) {
     e = launch_tc(p, s, g_prof_start, g_prof_mid, g_prof_stop, &launches);
   } else {
     if (g_prof_start) cudaEventRecord(g_prof_start, s);

@@ -276,11 +276,16 @@ cudaError_t launch_typed(const Problem& p, cudaStream_t s) {
 
 cudaError_t launch_simt(const Problem& p, cudaStream_t s, int* launches) {
   *launches = p.max_items > 0 ? 1 : 0;
-  const bool d64 = p.d == 64;
   switch (p.dtype) {
-    case DF_BF16: return d64 ? launch_typed<__nv_bfloat16, 64>(p, s) : launch_typed<__nv_bfloat16, 128>(p, s);
-    case DF_FP16: return d64 ? launch_typed<__half, 64>(p, s) : launch_typed<__half, 128>(p, s);
-    default: return d64 ? launch_typed<float, 64>(p, s) : launch_typed<float, 128>(p, s);
+    case DF_BF16:
+      return p.d == 32 ? launch_typed<__nv_bfloat16, 32>(p, s)
+             : p.d == 64 ? launch_typed<__nv_bfloat16, 64>(p, s) : launch_typed<__nv_bfloat16, 128>(p, s);
+    case DF_FP16:
+      return p.d == 32 ? launch_typed<__half, 32>(p, s)
+             : p.d == 64 ? launch_typed<__half, 64>(p, s) : launch_typed<__half, 128>(p, s);
+    default:
+      return p.d == 32 ? launch_typed<float, 32>(p, s)
+             : p.d == 64 ? launch_typed<float, 64>(p, s) : launch_typed<float, 128>(p, s);
   }
 }
 

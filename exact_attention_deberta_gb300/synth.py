@@ -68,6 +68,9 @@ WORKLOADS = {
     "long_packed_h8d128": Workload("long_packed_h8d128", 4, "packed", "bf16", 8, 128, 8192, 16,
                                    "full"),
     "long_packed_fp32": Workload("long_packed_fp32", 4, "packed", "fp32", 12, 64, 2048, 4, "full"),
+    # head size 32 (hidden 768 as 24 x 32), packed varlen, bf16
+    "packed_varlen_h24d32": Workload("packed_varlen_h24d32", 3, "packed", "bf16", 24, 32, 2048, 64,
+                                     "uniform64"),
 }
 
 

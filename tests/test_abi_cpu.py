@@ -53,7 +53,8 @@ def test_supported_matrix(binding):
     assert binding.df_attn_supported(8, 8192, 128, torch.float16) == ok
     assert binding.df_attn_supported(12, 2048, 64, torch.float32) == ok
     assert binding.df_attn_supported(12, 512, 48, torch.bfloat16) == binding.DF_ERR_UNSUPPORTED
-    assert binding.df_attn_supported(12, 512, 32, torch.bfloat16) == binding.DF_ERR_UNSUPPORTED
+    assert binding.df_attn_supported(12, 512, 32, torch.bfloat16) == ok
+    assert binding.df_attn_supported(12, 512, 96, torch.bfloat16) == binding.DF_ERR_UNSUPPORTED
     assert binding.df_attn_supported(0, 512, 64, torch.bfloat16) == binding.DF_ERR_INVALID_ARG
     assert binding.df_attn_supported(12, 0, 64, torch.bfloat16) == binding.DF_ERR_INVALID_ARG
     # buckets/2 must stay below max_rel - 1 for the logarithm to grow

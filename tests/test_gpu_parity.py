@@ -284,3 +284,15 @@ def test_deterministic(lib):
     a = run_gpu(lib, x).clone()
     b = run_gpu(lib, x)
     assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("layout,dtype,lengths", [("packed", "bf16", [700, 1, 129, 0, 300]),
+                                                  ("padded", "fp16", [512, 77, 0, 200]),
+                                                  ("packed", "fp32", [333, 64, 1000])])
+def test_head_size_32(lib, layout, dtype, lengths):
+    """d = 32 (the CUDA-core kernel for every dtype): every row against the oracle,
+    with ragged, empty and single-token sequences and far tiles (L up to 1000)."""
+    L = max(lengths)
+    x = synth.custom_inputs(layout=layout, dtype=dtype, H=4, d=32, lengths=lengths, L=L, seed=len(lengths) + L)
+    out = run_gpu(lib, x)
+    assert_close(out.double().cpu().numpy(), oracle_full(x), dtype, f"d32-{layout}-{dtype}")
