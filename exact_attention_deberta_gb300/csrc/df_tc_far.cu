@@ -13,16 +13,18 @@
 //
 // Warp roles of one CTA (one CTA per SM, persistent over the work list):
 //   warp 0      TMA producer of Q (two buffers, so the next item's Q lands
-//               while the current one finishes) and of K for every far tile;
-//   warp 2      TMA producer of V; K and V have separate stage barriers, a K
+//               while the current one finishes), of K for every far tile and,
+//               at d = 64, of V; K and V have separate stage barriers (a K
 //               stage is free once its QK has completed, a V stage once its
-//               P.V has, so K loads run further ahead;
+//               P.V has);
 //   warp 1      tcgen05.mma issuer of S = Q.K^T into a TMEM score buffer
 //               (three at d = 64, P overwriting its S, so QK(G) waits only
 //               for P(G - 3).V; at d = 128 this warp also issues the P.V);
-//   warp 3      at d = 64 the issuer of O_b += P.V with P read back from TMEM,
-//               so that QK never queues behind a blocking P.V issue; idle at
-//               d = 128;
+//   warps 3, 2  at d = 64 the issuers of O_0 += P.V and O_1 += P.V for the
+//               tiles of softmax warpgroup 0 and 1, with P read back from
+//               TMEM: a P.V goes out as soon as its P is stored, never behind
+//               the other warpgroup's blocking issue; at d = 128 warp 2 loads
+//               V and warp 3 idles;
 //   warps 4-7   softmax warpgroup 0: even far tiles, accumulator O_0;
 //   warps 8-11  softmax warpgroup 1: odd far tiles, accumulator O_1.
 // The control warpgroup gives registers back (setmaxnreg) so that each softmax
@@ -56,8 +58,8 @@ struct FarSmem {
   static constexpr uint32_t ml = sel + 2 * kAugBytes;                // float4 [2 wg][128]
   static constexpr uint32_t bars = ml + 2 * 128 * 16;
   // q_full[2], q_empty[2], k_full[S], k_empty[S], v_full[S], v_empty[S], s_full[3],
-  // p_full[2][2], o_final, drain[2], buf_free[3], sel_full
-  static constexpr int kBars = 4 + 4 * kStages + 3 + 4 + 3 + 3 + 1;
+  // p_full[2][2], o_final, drain[3], buf_free[3], sel_full
+  static constexpr int kBars = 4 + 4 * kStages + 3 + 4 + 4 + 3 + 1;
   static constexpr uint32_t misc = bars + kBars * 8;                 // abort flag, tmem slot
   static constexpr uint32_t bytes = misc + 16;
   static constexpr uint32_t alloc = bytes + 1024;
@@ -112,8 +114,8 @@ __global__ void __launch_bounds__(kFarThreads, 1)
   // next S waits for a P.V issued after this phase.
   uint64_t* p_full = s_full + 3;
   uint64_t* o_final = p_full + 4;
-  uint64_t* drain = o_final + 1;         // [2]: one per MMA-issuing thread
-  uint64_t* buf_free = drain + 2;  // [3] d = 64: the P.V that read the buffer is done
+  uint64_t* drain = o_final + 1;         // [3]: one per MMA-issuing thread
+  uint64_t* buf_free = drain + 3;  // [3] d = 64: the P.V that read the buffer is done
   uint64_t* sel_full = buf_free + 3;  // selector blocks landed
   volatile int* s_abort = reinterpret_cast<volatile int*>(sm + SL::misc);
   uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + SL::misc + 4);
@@ -130,9 +132,8 @@ __global__ void __launch_bounds__(kFarThreads, 1)
       mbar_init(buf_free + b, 1);
     }
     for (int b = 0; b < 4; ++b) mbar_init(p_full + b, 4);
-    mbar_init(o_final, 1);
-    mbar_init(drain, 1);
-    mbar_init(drain + 1, 1);
+    mbar_init(o_final, 1);  // d = 128: every P.V of the item done (d = 64 waits per tile)
+    for (int b = 0; b < 3; ++b) mbar_init(drain + b, 1);
     mbar_init(sel_full, 1);
     *s_abort = 0;
     mbar_fence_init();
@@ -164,18 +165,16 @@ __global__ void __launch_bounds__(kFarThreads, 1)
   const unsigned long long budget = p.wait_budget;
   df_ws_header* hdr = p.hdr;
 
-  if (warp == 0 || warp == 2) {
+  if (warp == 0 || (!kTriS && warp == 2)) {
     // ------------------------------------------------------------ TMA producers
-    // warp 0: Q of every item and K of every far tile; warp 2: V.  K stages are
-    // released when QK has read them, V stages when P.V has, so K runs ahead.
+    // warp 0: Q of every item and K of every far tile, and at d = 64 also V;
+    // d = 128: warp 2 loads V.  K stages are released when QK has read them, V
+    // stages when P.V has.
     setmaxnreg_dec<56>();
     if (lane == 0) {
       const bool is_k = warp == 0;
-      uint64_t* full = is_k ? k_full : v_full;
-      uint64_t* empty = is_k ? k_empty : v_empty;
-      const uint32_t off = is_k ? 0u : SL::kTileBytes;
-      const CUtensorMap* map = is_k ? &maps.k : &maps.v;
-      uint32_t g = 0, qc = 0, g_issued = 0, q_issued = 0;  // loads are issued in order
+      const bool with_v = !is_k || kTriS;
+      uint32_t g = 0, qc = 0, gk_issued = 0, gv_issued = 0, q_issued = 0;  // loads are issued in order
       if (is_k) {  // the two selector blocks, once
         mbar_expect_tx(sel_full, 2 * kAugBytes);
         tma_load_2d(sSel, &maps.kaug_sel, 0, 0, sel_full);
@@ -198,36 +197,45 @@ __global__ void __launch_bounds__(kFarThreads, 1)
         for (int t = 0; t < ig.nt; ++t, ++g) {
           const int s = g % S;
           const int row = ig.start + ig.block_of(t) * 128;
-          if (wait_or_abort(empty + s, ((g / S) & 1) ^ 1, budget, s_abort, hdr, is_k ? 302 : 303)) {
-            uint8_t* st = sKV + s * SL::kStageBytes + off;
-            mbar_expect_tx(full + s, SL::kTileBytes + (is_k ? kAugBytes : 0u));
+          uint8_t* st = sKV + s * SL::kStageBytes;
+          if (is_k && wait_or_abort(k_empty + s, ((g / S) & 1) ^ 1, budget, s_abort, hdr, 302)) {
+            mbar_expect_tx(k_full + s, SL::kTileBytes + kAugBytes);
             for (int c = 0; c < kChunks; ++c)
-              tma_load_2d(st + c * kBoxBytes, map, ig.h * D + c * 64, row, full + s);
-            if (is_k)  // the keys' p2c terms, 16 values per key
-              tma_load_2d(sKV + s * SL::kStageBytes + 2 * SL::kTileBytes, &maps.kaug, ig.h * 16, row,
-                          full + s);
-            g_issued = g + 1;
+              tma_load_2d(st + c * kBoxBytes, &maps.k, ig.h * D + c * 64, row, k_full + s);
+            // the keys' p2c terms, 16 values per key
+            tma_load_2d(st + 2 * SL::kTileBytes, &maps.kaug, ig.h * 16, row, k_full + s);
+            gk_issued = g + 1;
+          }
+          if (with_v && wait_or_abort(v_empty + s, ((g / S) & 1) ^ 1, budget, s_abort, hdr, 303)) {
+            mbar_expect_tx(v_full + s, SL::kTileBytes);
+            for (int c = 0; c < kChunks; ++c)
+              tma_load_2d(st + SL::kTileBytes + c * kBoxBytes, &maps.v, ig.h * D + c * 64, row, v_full + s);
+            gv_issued = g + 1;
           }
         }
       }
       // no copy may still be landing when the CTA leaves: wait for the last load
       // issued into every stage and into both Q buffers
-      for (uint32_t k = g_issued > (uint32_t)S ? g_issued - S : 0; k < g_issued; ++k)
-        mbar_wait(full + k % S, (k / S) & 1, kDrainBudget);
+      for (uint32_t k = gk_issued > (uint32_t)S ? gk_issued - S : 0; k < gk_issued; ++k)
+        mbar_wait(k_full + k % S, (k / S) & 1, kDrainBudget);
+      for (uint32_t k = gv_issued > (uint32_t)S ? gv_issued - S : 0; k < gv_issued; ++k)
+        mbar_wait(v_full + k % S, (k / S) & 1, kDrainBudget);
       for (uint32_t k = q_issued > 2 ? q_issued - 2 : 0; k < q_issued; ++k)
         mbar_wait(q_full + (k & 1), (k >> 1) & 1, kDrainBudget);
       if (is_k) mbar_wait(sel_full, 0, kDrainBudget);
     }
-  } else if (warp == 1 || (kTriS && warp == 3)) {
+  } else if (warp == 1 || (kTriS && (warp == 2 || warp == 3))) {
     // ------------------------------------------------------------ MMA issuers
-    // d = 64: warp 1 issues S = Q.K^T, warp 3 issues O += P.V, so that neither
-    // chain waits behind the other's blocking issue; every commit is made by the
-    // thread whose MMAs it covers.  d = 128 (P overwrites S): warp 1 issues both
-    // in order.
+    // d = 64: warp 1 issues S = Q.K^T, warps 3 and 2 issue O_b += P.V for the
+    // tiles of warpgroup 0 and 1, so that no chain waits behind another's
+    // blocking issue (a P.V goes out as soon as its P is stored, not after the
+    // other warpgroup's); every commit is made by the thread whose MMAs it
+    // covers.  d = 128 (P overwrites S): warp 1 issues both in order.
     setmaxnreg_dec<56>();
     if (lane == 0) {
       const bool qk_role = warp == 1;
-      const bool pv_role = warp == 3 || !kTriS;
+      const bool pv_role = warp != 1 || !kTriS;
+      const int pv_wg = warp == 3 ? 0 : 1;  // d = 64: the warpgroup whose tiles this thread multiplies
       uint32_t g = 0, qc = 0;
       uint32_t pn[2] = {0, 0};  // tiles of warpgroup b whose P has been consumed
       const bool sel_ok = !qk_role || wait_or_abort(sel_full, 0, budget, s_abort, hdr, 316);
@@ -286,7 +294,7 @@ __global__ void __launch_bounds__(kFarThreads, 1)
           if (qk_role) {
             for (int t = 0; t < ig.nt; ++t) issue_qk(t);
           } else {
-            for (int t = 0; t < ig.nt; ++t) issue_pv(t);
+            for (int t = pv_wg; t < ig.nt; t += 2) issue_pv(t);
           }
         } else {
           // P overwrites S: QK(t) can only follow PV(t - 2)
@@ -297,13 +305,13 @@ __global__ void __launch_bounds__(kFarThreads, 1)
         }
         g += ig.nt;
         if (qk_role) mma_commit(q_empty + qb);
-        if (pv_role) mma_commit(o_final);
+        if (pv_role && !kTriS) mma_commit(o_final);
       }
-      uint64_t* my_drain = drain + (warp == 3 ? 1 : 0);
+      uint64_t* my_drain = drain + (warp == 1 ? 0 : warp == 3 ? 1 : 2);
       mma_commit(my_drain);
       mbar_wait(my_drain, 0, kDrainBudget);
     }
-  } else if (warp == 3) {  // d = 128: idle
+  } else if (warp == 3) {  // d = 128: idle (warp 2 loads V)
     setmaxnreg_dec<56>();
   } else {
     // ------------------------------------------------------------ softmax warpgroups
@@ -458,8 +466,18 @@ __global__ void __launch_bounds__(kFarThreads, 1)
         o_has = true;
       }
       // ---- merge the two warpgroups' partial results and write O
-      wait_or_abort(o_final, ic & 1, budget, s_abort, hdr, 322);
-      ++ic;
+      if (kTriS) {
+        // the last P.V into this warpgroup's O (its own issuer's, through the
+        // tile's buffer); the other warpgroup waits for its own before the
+        // barrier below, so both O are complete after it
+        if (wg < ig.nt) {
+          const uint32_t G = gbase + wg + 2 * ((ig.nt - 1 - wg) / 2);
+          wait_or_abort(buf_free + G % 3, (G / 3) & 1, budget, s_abort, hdr, 322);
+        }
+      } else {
+        wait_or_abort(o_final, ic & 1, budget, s_abort, hdr, 322);
+        ++ic;
+      }
       tc_fence_after();
       sML[wg * 128 + row] = make_float4(m_run, l_run, o_has ? 1.f : 0.f, 0.f);
       named_sync(3, 256);
