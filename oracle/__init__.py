@@ -17,3 +17,10 @@ from .df_oracle import (  # noqa: F401
 from .pack import pack_info, pack_rows, unpack_rows  # noqa: F401,E402
 from .linear import linear  # noqa: F401,E402
 from .encoder import layer_norm, gelu, encoder_layer, encoder  # noqa: F401,E402
+from .backward import (  # noqa: F401,E402
+    backward_head,
+    backward_sequence,
+    backward_padded,
+    backward_packed,
+    backward_metric_flops,
+)

@@ -1,0 +1,149 @@
+"""Pins of the float64 backward oracle against facts that do not come from it.
+
+* Central differences of the forward oracle (itself pinned in
+  test_oracle_pins.py): every entry of every gradient on a small head whose
+  distances reach the identity zone, the log zone and saturation, and
+  directional derivatives on padded (masked) and packed batches.
+* Shift invariances of the score: adding one vector to every PK row adds
+  Q_i.u to the whole row i of scores, so the softmax (and the loss) does not
+  move and sum_r dPK[r] = 0; with PQ = 0 the same holds for K.  Also
+  sum_j dV_j = sum_i dO_i over valid rows, since each softmax row sums to 1.
+* With PK = PQ = 0 the method is plain attention with scale 1/sqrt(3 d):
+  dQ, dK, dV equal torch's scaled-dot-product attention gradients (float64
+  autograd, a library routine).
+* Masked query rows and masked keys get zero gradients.
+"""
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import attend_packed, attend_padded, attend_sequence
+from oracle.backward import backward_head, backward_packed, backward_padded, backward_sequence
+
+CFG = dict(buckets=4, max_rel=8, span=4)   # mid 2: identity |r| <= 2, log zone, saturation at 7
+
+
+def _rand(rng, *shape):
+    return rng.standard_normal(shape)
+
+
+def _loss_seq(q, k, v, pk, pq, w, valid=None):
+    return float(np.sum(attend_sequence(q, k, v, pk, pq, valid=valid, **CFG) * w))
+
+
+def test_every_entry_matches_central_differences():
+    rng = np.random.default_rng(11)
+    n, H, d = 10, 1, 3
+    q, k, v, w = (_rand(rng, n, H, d) for _ in range(4))
+    pk, pq = (_rand(rng, 2 * CFG["span"], H, d) for _ in range(2))
+    valid = np.ones(n, dtype=bool)
+    valid[[3, 8]] = False   # one masked row/key inside, one near the end
+    grads = backward_sequence(q, k, v, pk, pq, w, valid=valid, **CFG)
+    args = [q, k, v, pk, pq]
+    eps = 1e-6
+    for which, (x, g) in enumerate(zip(args, grads)):
+        num = np.zeros_like(x)
+        for e in np.ndindex(x.shape):
+            old = x[e]
+            x[e] = old + eps
+            up = _loss_seq(*args, w, valid)
+            x[e] = old - eps
+            dn = _loss_seq(*args, w, valid)
+            x[e] = old
+            num[e] = (up - dn) / (2 * eps)
+        np.testing.assert_allclose(g, num, rtol=1e-6, atol=1e-8, err_msg=f"input {which}")
+
+
+def _directional(loss, args, grads, rng, eps=1e-6):
+    for which, (x, g) in enumerate(zip(args, grads)):
+        u = rng.standard_normal(x.shape)
+        x0 = x.copy()
+        x[...] = x0 + eps * u
+        up = loss()
+        x[...] = x0 - eps * u
+        dn = loss()
+        x[...] = x0
+        fd = (up - dn) / (2 * eps)
+        an = float(np.sum(g * u))
+        assert abs(fd - an) <= 1e-6 * max(1.0, abs(an)), (which, fd, an)
+
+
+def test_padded_directional_derivatives():
+    rng = np.random.default_rng(12)
+    B, L, H, d = 2, 12, 2, 4
+    q, k, v, w = (_rand(rng, B, L, H, d) for _ in range(4))
+    pk, pq = (_rand(rng, 2 * CFG["span"], H, d) for _ in range(2))
+    mask = np.ones((B, L), dtype=np.uint8)
+    mask[0, 9:] = 0          # right padding
+    mask[1, [0, 5]] = 0      # holes
+    grads = backward_padded(q, k, v, pk, pq, w, mask, **CFG)
+    args = [q, k, v, pk, pq]
+
+    def loss():
+        return float(np.sum(attend_padded(*args, mask, **CFG) * w))
+
+    _directional(loss, args, grads, rng)
+    # masked tokens: no gradient into their q, k, v
+    for g in grads[:3]:
+        assert np.all(g[mask == 0] == 0.0)
+
+
+def test_packed_directional_derivatives():
+    rng = np.random.default_rng(13)
+    cu = np.array([0, 5, 6, 17])   # lengths 5, 1, 11
+    T, H, d = 17, 2, 4
+    q, k, v, w = (_rand(rng, T, H, d) for _ in range(4))
+    pk, pq = (_rand(rng, 2 * CFG["span"], H, d) for _ in range(2))
+    grads = backward_packed(q, k, v, pk, pq, w, cu, **CFG)
+    args = [q, k, v, pk, pq]
+
+    def loss():
+        return float(np.sum(attend_packed(*args, cu, **CFG) * w))
+
+    _directional(loss, args, grads, rng)
+
+
+def test_position_shift_invariance():
+    rng = np.random.default_rng(14)
+    n, d = 40, 8
+    cfg = dict(buckets=16, max_rel=32, span=16)
+    q, k, v, w = (_rand(rng, n, d) for _ in range(4))
+    pk, pq = (_rand(rng, 32, d) for _ in range(2))
+    valid = rng.random(n) > 0.2
+    dq, dk, dv, dpk, dpq = backward_head(q, k, v, pk, pq, w, valid=valid, **cfg)
+    np.testing.assert_allclose(dpk.sum(axis=0), 0.0, atol=1e-10)
+    np.testing.assert_allclose(dv.sum(axis=0), w[valid].sum(axis=0), rtol=1e-10, atol=1e-10)
+    # with PQ = 0 the key side has the same invariance
+    dq, dk, dv, dpk, dpq = backward_head(q, k, v, pk, np.zeros_like(pq), w, valid=valid, **cfg)
+    np.testing.assert_allclose(dk.sum(axis=0), 0.0, atol=1e-10)
+    assert np.abs(dpq).max() > 0   # PQ = 0 still has a gradient
+
+
+def test_reduces_to_library_attention_without_positions():
+    rng = np.random.default_rng(15)
+    n, d = 33, 16
+    q, k, v, w = (_rand(rng, n, d) for _ in range(4))
+    zeros = np.zeros((2 * 64, d))
+    dq, dk, dv, _, _ = backward_head(q, k, v, zeros, zeros, w, buckets=64, max_rel=128, span=64)
+    tq, tk, tv = (torch.tensor(a, dtype=torch.float64, requires_grad=True) for a in (q, k, v))
+    out = torch.nn.functional.scaled_dot_product_attention(
+        tq[None, None], tk[None, None], tv[None, None], scale=1.0 / math.sqrt(3 * d))[0, 0]
+    out.backward(torch.tensor(w, dtype=torch.float64))
+    np.testing.assert_allclose(dq, tq.grad.numpy(), rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(dk, tk.grad.numpy(), rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(dv, tv.grad.numpy(), rtol=1e-10, atol=1e-12)
+
+
+@pytest.mark.parametrize("n", [0, 1])
+def test_degenerate_lengths(n):
+    rng = np.random.default_rng(16)
+    d = 4
+    q, k, v, w = (_rand(rng, n, d) for _ in range(4))
+    pk, pq = (_rand(rng, 8, d) for _ in range(2))
+    dq, dk, dv, dpk, dpq = backward_head(q, k, v, pk, pq, w, **CFG)
+    # one token attends only to itself with weight 1: O = V, every score gradient is 0
+    assert np.all(dq == 0) and np.all(dk == 0) and np.all(dpk == 0) and np.all(dpq == 0)
+    np.testing.assert_array_equal(dv, w)
