@@ -165,6 +165,46 @@ def df_attn_fwd(q, k, v, pos_key, pos_query, key_mask=None, cu_seqlens=None, *, 
     return out
 
 
+_lib.df_attn_bwd.argtypes = [_vp] * 8 + [_i] * 9 + [_vp] * 5 + [_vp, _sz, _vp]
+_lib.df_attn_bwd.restype = _i
+_lib.df_attn_bwd_workspace_size.argtypes = [_i] * 7
+_lib.df_attn_bwd_workspace_size.restype = _sz
+
+
+def df_attn_bwd_workspace_size(B, H, L, d, buckets=256, max_rel=512, span=None) -> int:
+    span = default_span(buckets, max_rel) if span is None else span
+    return int(_lib.df_attn_bwd_workspace_size(B, H, L, d, buckets, max_rel, span))
+
+
+def df_attn_bwd(q, k, v, pos_key, pos_query, dout, key_mask=None, cu_seqlens=None, *,
+                max_seqlen=None, buckets=256, max_rel=512, span=None, grads=None,
+                workspace=None, stream=None):
+    """Backward pass; returns float32 (dq, dk, dv, dpos_key, dpos_query).
+
+    ``grads`` may pass those five tensors preallocated (float32, contiguous)."""
+    placeholder = workspace if workspace is not None else q  # checked, not used
+    B, H, L, T, d, span, _, _ = _prepare(q, k, v, pos_key, pos_query, key_mask, cu_seqlens,
+                                         max_seqlen, buckets, max_rel, span, q, placeholder)
+    if workspace is None:
+        size = df_attn_bwd_workspace_size(B, H, L, d, buckets, max_rel, span)
+        if size == 0:
+            _check(DF_ERR_UNSUPPORTED, "df_attn_bwd_workspace_size")
+        workspace = torch.empty(size, dtype=torch.uint8, device=q.device)
+    if dout.shape != q.shape or dout.dtype != q.dtype or not dout.is_contiguous():
+        raise ValueError("dout must match q in shape and dtype and be contiguous")
+    if grads is None:
+        f32 = dict(dtype=torch.float32, device=q.device)
+        grads = (torch.empty(q.shape, **f32), torch.empty(q.shape, **f32), torch.empty(q.shape, **f32),
+                 torch.empty(pos_key.shape, **f32), torch.empty(pos_key.shape, **f32))
+    dq, dk, dv, dpk, dpq = grads
+    st = _lib.df_attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(pos_key), _ptr(pos_query), _ptr(dout),
+                          _ptr(key_mask), _ptr(cu_seqlens), B, H, L, T, d, buckets, max_rel, span,
+                          _DTYPE[q.dtype], _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dpk), _ptr(dpq),
+                          _ptr(workspace), workspace.numel(), _stream(stream))
+    _check(st, "df_attn_bwd")
+    return dq, dk, dv, dpk, dpq
+
+
 def df_attn_plan(q, k, pos_key, pos_query, key_mask=None, cu_seqlens=None, *, max_seqlen=None,
                  buckets=256, max_rel=512, span=None, out=None, workspace=None, stream=None):
     """Planning step alone; returns (out, workspace)."""

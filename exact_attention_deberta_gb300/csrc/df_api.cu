@@ -111,6 +111,42 @@ Layout make_layout(int B, int H, int L, int d, int buckets, int max_rel, int spa
   return l;
 }
 
+// Backward sections, after the forward's: row statistics, the two
+// bucket-sum tables and the partial position gradients.
+struct BwdLayout {
+  size_t lse, drow, gc, gp, part, total;
+  int splits;
+};
+
+constexpr int kBwdMaxR = 512;  // bucket-sum rows of a block live in shared memory
+
+int bwd_splits(long long T, int H) {
+  long long s = (T + 1023) / 1024;
+  s = s < 1 ? 1 : (s > 64 ? 64 : s);
+  const long long cap = 65535 / (H > 0 ? H : 1);
+  return (int)(s < cap ? s : (cap < 1 ? 1 : cap));
+}
+
+BwdLayout make_bwd_layout(int B, int H, int L, int d, int buckets, int max_rel, int span) {
+  const Layout f = make_layout(B, H, L, d, buckets, max_rel, span);
+  BwdLayout l{};
+  const size_t T = (size_t)B * L, R = 2 * (size_t)span;
+  size_t off = f.total;
+  l.lse = off;
+  off = align256(off + T * H * sizeof(float));
+  l.drow = off;
+  off = align256(off + T * H * sizeof(float));
+  l.gc = off;
+  off = align256(off + T * H * R * sizeof(float));
+  l.gp = off;
+  off = align256(off + T * H * R * sizeof(float));
+  l.splits = bwd_splits((long long)T, H);
+  l.part = off;
+  off = align256(off + 2 * (size_t)l.splits * H * R * d * sizeof(float));
+  l.total = off;
+  return l;
+}
+
 df_status check_params(int H, int L, int d, df_dtype dtype, int buckets, int max_rel, int span) {
   if (H < 1 || L < 1 || span < 1) return DF_ERR_INVALID_ARG;
   if (dtype != DF_BF16 && dtype != DF_FP16 && dtype != DF_FP32) return DF_ERR_INVALID_ARG;
@@ -171,6 +207,7 @@ df_status build_problem(const void* q, const void* k, const void* v, const void*
   P.diag_m0 = lay.diag_m0;
   const unsigned long long wb = g_wait_budget.load();
   P.wait_budget = wb ? wb : kDefaultWaitBudget;
+  P.zero_out = 1;
   return DF_OK;
 }
 
@@ -262,6 +299,72 @@ df_status df_attn_fwd(const void* q, const void* k, const void* v, const void* p
     if (g_prof_stop) cudaEventRecord(g_prof_stop, s);
   }
   if (e != cudaSuccess) return DF_ERR_CUDA;
+  g_last_launches.store(1 + launches);
+  return DF_OK;
+}
+
+size_t df_attn_bwd_workspace_size(int B, int H, int L, int d, int buckets, int max_rel, int span) {
+  if (B < 0 || check_params(H, L, d, DF_BF16, buckets, max_rel, span) != DF_OK) return 0;
+  if (2 * span > kBwdMaxR) return 0;
+  return make_bwd_layout(B, H, L, d, buckets, max_rel, span).total;
+}
+
+df_status df_attn_bwd(const void* q, const void* k, const void* v, const void* pos_key,
+                      const void* pos_query, const void* dout, const uint8_t* key_mask,
+                      const int32_t* cu_seqlens, int B, int H, int L, int total_tokens, int d,
+                      int buckets, int max_rel, int span, df_dtype dtype, float* dq, float* dk,
+                      float* dv, float* dpos_key, float* dpos_query, void* workspace,
+                      size_t workspace_bytes, df_stream_t stream) {
+  BwdProblem b;
+  memset(&b, 0, sizeof(b));
+  df_status st = build_problem(q, k, v, pos_key, pos_query, key_mask, cu_seqlens, B, H, L,
+                               total_tokens, d, buckets, max_rel, span, dtype, dq, workspace,
+                               workspace_bytes, true, &b.f);
+  if (st != DF_OK) return st;
+  if (2 * span > kBwdMaxR) return DF_ERR_UNSUPPORTED;
+  const int T = total_tokens;
+  if (!dpos_key || !dpos_query || (T > 0 && (!dout || !dk || !dv))) return DF_ERR_INVALID_ARG;
+  if (!aligned16(dpos_key) || !aligned16(dpos_query) ||
+      (T > 0 && (!aligned16(dout) || !aligned16(dk) || !aligned16(dv))))
+    return DF_ERR_ALIGNMENT;
+  const BwdLayout bl = make_bwd_layout(B, H, L, d, buckets, max_rel, span);
+  if (workspace_bytes < bl.total) return DF_ERR_WORKSPACE;
+  char* base = static_cast<char*>(workspace);
+  b.f.zero_out = 0;  // `out` is dq here: the planner must leave it alone
+  b.dout = dout;
+  b.dq = dq;
+  b.dk = dk;
+  b.dv = dv;
+  b.dpk = dpos_key;
+  b.dpq = dpos_query;
+  b.lse = reinterpret_cast<float*>(base + bl.lse);
+  b.drow = reinterpret_cast<float*>(base + bl.drow);
+  b.gc = reinterpret_cast<float*>(base + bl.gc);
+  b.gp = reinterpret_cast<float*>(base + bl.gp);
+  b.part = reinterpret_cast<float*>(base + bl.part);
+  b.R = 2 * span;
+  b.splits = bwd_splits(T, H);
+  b.kchunk = T > 0 ? (T + b.splits - 1) / b.splits : 1;
+  b.sscale = (float)(1.0 / sqrt(3.0 * d));
+  cudaStream_t s = (cudaStream_t)stream;
+  const size_t R = (size_t)b.R;
+  // rows outside every sequence (and masked ones) must read as zero
+  if (T > 0) {
+    const size_t grad = (size_t)T * H * d * sizeof(float), gsum = (size_t)T * H * R * sizeof(float);
+    if (cudaMemsetAsync(dq, 0, grad, s) != cudaSuccess || cudaMemsetAsync(dk, 0, grad, s) != cudaSuccess ||
+        cudaMemsetAsync(dv, 0, grad, s) != cudaSuccess || cudaMemsetAsync(b.gc, 0, gsum, s) != cudaSuccess ||
+        cudaMemsetAsync(b.gp, 0, gsum, s) != cudaSuccess)
+      return DF_ERR_CUDA;
+  } else {
+    const size_t pos = R * H * d * sizeof(float);
+    if (cudaMemsetAsync(dpos_key, 0, pos, s) != cudaSuccess ||
+        cudaMemsetAsync(dpos_query, 0, pos, s) != cudaSuccess)
+      return DF_ERR_CUDA;
+  }
+  if (launch_plan(b.f, s) != cudaSuccess) return DF_ERR_CUDA;
+  int launches = 0;
+  if (launch_bwd(b, s, g_prof_start, g_prof_mid, g_prof_stop, &launches) != cudaSuccess)
+    return DF_ERR_CUDA;
   g_last_launches.store(1 + launches);
   return DF_OK;
 }

@@ -61,6 +61,27 @@ struct Problem {
   int n_diag;
   int diag_m0;
   unsigned long long wait_budget;
+  int zero_out;               // the planner zeroes the output rows of masked tokens
+};
+
+// Views of the backward pass (gradients in fp32).
+struct BwdProblem {
+  Problem f;                  // the forward's inputs and planning views
+  const void* dout;           // [tokens][H][d], the I/O type
+  float* dq;                  // [tokens][H][d]
+  float* dk;
+  float* dv;
+  float* dpk;                 // [2 span][H][d]
+  float* dpq;
+  float* lse;                 // [T][H] row log-sum-exp of the logits (log2 units); +inf: no output
+  float* drow;                // [T][H] dO_i . O_i
+  float* gc;                  // [T][H][R] sums of dS along each query row, by relative index
+  float* gp;                  // [T][H][R] the same along each key column
+  float* part;                // [2][splits][H][R][d] partial position gradients
+  int R;                      // 2 span
+  int splits;                 // token ranges of the position-gradient reduction
+  int kchunk;                 // tokens per range
+  float sscale;               // 1 / sqrt(3 d)
 };
 
 // DeBERTa log-bucketed relative position.  The identity inside |r| <= mid;
@@ -112,4 +133,6 @@ cudaError_t launch_plan(const Problem& p, cudaStream_t s);
 cudaError_t launch_index_table(int buckets, int max_rel, int span, int max_len, int32_t* idx,
                                cudaStream_t s);
 cudaError_t launch_simt(const Problem& p, cudaStream_t s, int* launches);
+cudaError_t launch_bwd(const BwdProblem& b, cudaStream_t s, cudaEvent_t ev0, cudaEvent_t ev_mid,
+                       cudaEvent_t ev1, int* launches);
 }  // namespace dfa

@@ -79,7 +79,7 @@ __device__ void scalar_block(const Problem& p, int blk) {
         b1 = fmaf(kf, rows[3][c], b1);
       }
     }
-  } else if (in_range) {
+  } else if (in_range && p.zero_out) {
     uint4* o4 = reinterpret_cast<uint4*>(static_cast<T*>(p.out) + row);
     for (int v = 0; v < d * (int)sizeof(T) / 16; ++v) o4[v] = make_uint4(0u, 0u, 0u, 0u);
   }

@@ -149,6 +149,13 @@ def make_inputs(w: Workload | str, *, lengths: Optional[np.ndarray] = None) -> I
     return Inputs(w, n, q, k, v, pk, pq, mask, cu)
 
 
+def grad_output(x: Inputs, salt: int = 1) -> torch.Tensor:
+    """Upstream gradient dL/dO of the backward pass: standard normal values of
+    q's shape and dtype, drawn from a generator of its own."""
+    rng = np.random.default_rng([x.w.seed, 7919, salt])
+    return _normal(rng, tuple(x.q.shape), x.w.dtype)
+
+
 def custom_inputs(*, layout: str, dtype: str, H: int, d: int, lengths, L: Optional[int] = None,
                   seed: int = 0, buckets: int = 256, max_rel: int = 512,
                   span: Optional[int] = None) -> Inputs:

@@ -107,6 +107,51 @@ df_status df_attn_fwd(const void* q, const void* k, const void* v,
  * arguments df_attn_supported() rejects. */
 size_t df_attn_workspace_size(int B, int H, int L, int d, int buckets, int max_rel, int span);
 
+/*
+ * Backward pass: gradients of sum(out * dout) with respect to q, k, v, pos_key
+ * and pos_query, for the forward defined above.  The pages have no backward
+ * (DisentangledFlash 0.2.0 README, "Status": training keeps the stock path);
+ * this one differentiates the same score exactly.  With p the softmax row,
+ * dP_ij = dout_i.V_j, D_i = dout_i.O_i and dS_ij = p_ij (dP_ij - D_i)/sqrt(3 d):
+ *   dv_j      = sum_i p_ij dout_i
+ *   dq_i      = sum_j dS_ij (K_j + PK[idx(i-j)])
+ *   dk_j      = sum_i dS_ij (Q_i + PQ[idx(i-j)])
+ *   dpos_key[r]   = sum over (i, j) with idx(i-j) = r of dS_ij Q_i
+ *   dpos_query[r] = sum over (i, j) with idx(i-j) = r of dS_ij K_j
+ * A masked query row (its output is the constant 0) and a masked key pass no
+ * gradient: their rows of dq, dk, dv are 0, as are rows outside every sequence.
+ *
+ *   q, k, v, pos_key, pos_query, key_mask, cu_seqlens, B, H, L, total_tokens,
+ *   d, buckets, max_rel, span, dtype: as for df_attn_fwd (every dtype and
+ *                      d in {32, 64, 128}); 2 * span <= 512, else
+ *                      DF_ERR_UNSUPPORTED
+ *   dout               gradient of the output, layout and dtype of q
+ *   dq, dk, dv         float32, layout of q: written in full (overwritten)
+ *   dpos_key, dpos_query  float32 [2 span, H, d]: written in full, summed over
+ *                      every sequence of the call
+ *   workspace          at least df_attn_bwd_workspace_size() bytes, 256-byte
+ *                      aligned, contents need not be initialised
+ *
+ * Everything is computed in fp32 on CUDA cores: the forward is recomputed per
+ * query block (row log-sum-exp and O, so `out` is not an input), the score
+ * tiles are recomputed on the key side, and the position gradients are
+ * reduced over fixed token ranges with no global atomics (the per-block
+ * bucket sums use shared-memory atomics, so the last bits may differ from
+ * run to run).  Returns once the work is enqueued.
+ */
+df_status df_attn_bwd(const void* q, const void* k, const void* v,
+                      const void* pos_key, const void* pos_query, const void* dout,
+                      const uint8_t* key_mask, const int32_t* cu_seqlens,
+                      int B, int H, int L, int total_tokens, int d,
+                      int buckets, int max_rel, int span, df_dtype dtype,
+                      float* dq, float* dk, float* dv, float* dpos_key, float* dpos_query,
+                      void* workspace, size_t workspace_bytes, df_stream_t stream);
+
+/* Bytes of workspace df_attn_bwd needs for these sizes (T bounded by B*L);
+ * about 8 * B*L*H*span bytes for the bucket sums.  0 for arguments that
+ * df_attn_bwd rejects. */
+size_t df_attn_bwd_workspace_size(int B, int H, int L, int d, int buckets, int max_rel, int span);
+
 /* DF_OK if (H, L, d, dtype, buckets, max_rel, span) is implemented; otherwise
  * DF_ERR_INVALID_ARG or DF_ERR_UNSUPPORTED.  Host only, no CUDA call. */
 df_status df_attn_supported(int H, int L, int d, df_dtype dtype, int buckets, int max_rel,

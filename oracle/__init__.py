@@ -19,6 +19,8 @@ from .linear import linear  # noqa: F401,E402
 from .encoder import layer_norm, gelu, encoder_layer, encoder  # noqa: F401,E402
 from .backward import (  # noqa: F401,E402
     backward_head,
+    backward_rows,
+    backward_keys,
     backward_sequence,
     backward_padded,
     backward_packed,

@@ -99,6 +99,79 @@ def backward_head(q, k, v, pk, pq, dout, *, buckets, max_rel, span, valid=None):
     return dq, dk, dv, dpk, dpq
 
 
+def _row_softmax(q, k, v, pk, pq, rr, keys, valid, scale, buckets, max_rel, span):
+    """Scores, softmax and output of query rows rr (all keys of the head)."""
+    idx = rel_index(rr[:, None] - keys[None, :], buckets, max_rel, span)
+    z = q[rr] @ k.T + np.einsum("md,mnd->mn", q[rr], pk[idx]) + np.einsum("nd,mnd->mn", k, pq[idx])
+    z *= scale
+    z[:, ~valid] = -np.inf
+    z -= z.max(axis=1, keepdims=True)
+    p = np.exp(z)
+    p /= p.sum(axis=1, keepdims=True)
+    return idx, p, p @ v
+
+
+def backward_rows(q, k, v, pk, pq, dout, rows, *, buckets, max_rel, span, valid=None):
+    """dQ of the given query rows of one head: [n, d] inputs -> [len(rows), d].
+
+    A row's dQ needs only its own softmax row: dS_ij = scale p_ij (dO_i.V_j -
+    dO_i.O_i) and dQ_i = sum_j dS_ij (K_j + PK[idx_ij]).
+    """
+    q, k, v, pk, pq, dout = (_as_f64(a) for a in (q, k, v, pk, pq, dout))
+    n, d = q.shape
+    valid = np.ones(n, dtype=bool) if valid is None else np.asarray(valid, dtype=bool)
+    rows = np.asarray(rows, dtype=np.int64)
+    out = np.zeros((rows.size, d))
+    live = valid[rows]
+    if not np.any(live):
+        return out
+    rr = rows[live]
+    scale = 1.0 / math.sqrt(3.0 * d)
+    keys = np.arange(n)
+    idx, p, o = _row_softmax(q, k, v, pk, pq, rr, keys, valid, scale, buckets, max_rel, span)
+    dS = scale * p * (dout[rr] @ v.T - np.sum(dout[rr] * o, axis=1, keepdims=True))
+    out[live] = dS @ k + np.einsum("mn,mnd->md", dS, pk[idx])
+    return out
+
+
+def backward_keys(q, k, v, pk, pq, dout, keys_sel, *, buckets, max_rel, span, valid=None):
+    """(dK, dV) of the given keys of one head: [n, d] inputs -> two [m, d].
+
+    Every valid query row's softmax is needed (its normaliser and D_i), one
+    row chunk at a time; only the selected key columns are kept.
+    """
+    q, k, v, pk, pq, dout = (_as_f64(a) for a in (q, k, v, pk, pq, dout))
+    n, d = q.shape
+    valid = np.ones(n, dtype=bool) if valid is None else np.asarray(valid, dtype=bool)
+    sel = np.asarray(keys_sel, dtype=np.int64)
+    dk = np.zeros((sel.size, d))
+    dv = np.zeros((sel.size, d))
+    scale = 1.0 / math.sqrt(3.0 * d)
+    keys = np.arange(n)
+    rows_all = np.nonzero(valid)[0]
+    c2p = q @ pk.T
+    p2c = k @ pq.T
+    chunk = max(1, _BLOCK_BYTES // (8 * max(n, 1)))
+    for c0 in range(0, rows_all.size, chunk):
+        rr = rows_all[c0:c0 + chunk]
+        idx = rel_index(rr[:, None] - keys[None, :], buckets, max_rel, span)
+        z = q[rr] @ k.T + np.take_along_axis(c2p[rr], idx, axis=1) + p2c[keys[None, :], idx]
+        z *= scale
+        z[:, ~valid] = -np.inf
+        z -= z.max(axis=1, keepdims=True)
+        p = np.exp(z)
+        p /= p.sum(axis=1, keepdims=True)
+        o = p @ v
+        dmean = np.sum(dout[rr] * o, axis=1, keepdims=True)
+        ps = p[:, sel]
+        dS = scale * ps * (dout[rr] @ v[sel].T - dmean)
+        dv += ps.T @ dout[rr]
+        dk += dS.T @ q[rr] + np.einsum("ms,msd->sd", dS, pq[idx[:, sel]])
+    dk[~valid[sel]] = 0.0
+    dv[~valid[sel]] = 0.0
+    return dk, dv
+
+
 def backward_sequence(q, k, v, pk, pq, dout, *, buckets, max_rel, span, valid=None):
     """All heads of one sequence: [n, H, d] inputs, [2 span, H, d] positions."""
     q, k, v, pk, pq, dout = (_as_f64(a) for a in (q, k, v, pk, pq, dout))

@@ -173,3 +173,37 @@ def test_layernorm_checks_arguments_on_the_host(binding):
     assert lib.df_layernorm(p, None, p, p, 4, 1280, f(1e-7), p, binding.DF_BF16, None) == binding.DF_ERR_UNSUPPORTED
     assert lib.df_layernorm(p, None, p, p, 4, 768, f(1e-7), p, binding.DF_FP32, None) == binding.DF_ERR_UNSUPPORTED
     assert lib.df_layernorm(p, odd, p, p, 4, 768, f(1e-7), p, binding.DF_BF16, None) == binding.DF_ERR_ALIGNMENT
+
+
+def _bwd_raw(binding, **over):
+    """Call df_attn_bwd with fake (never dereferenced) aligned pointers."""
+    a = dict(q=0x10000, k=0x20000, v=0x30000, pk=0x40000, pq=0x50000, do=0x58000, mask=0x60000,
+             cu=None, B=2, H=2, L=64, T=128, d=64, buckets=256, max_rel=512, span=256, dtype=0,
+             dq=0x70000, dk=0x78000, dv=0x80000, dpk=0x88000, dpq=0x90000, ws=0x100000,
+             ws_bytes=1 << 40)
+    a.update(over)
+    vp = lambda x: None if x is None else ctypes.c_void_p(x)  # noqa: E731
+    return binding.raw_library.df_attn_bwd(
+        vp(a["q"]), vp(a["k"]), vp(a["v"]), vp(a["pk"]), vp(a["pq"]), vp(a["do"]), vp(a["mask"]),
+        vp(a["cu"]), a["B"], a["H"], a["L"], a["T"], a["d"], a["buckets"], a["max_rel"], a["span"],
+        a["dtype"], vp(a["dq"]), vp(a["dk"]), vp(a["dv"]), vp(a["dpk"]), vp(a["dpq"]), vp(a["ws"]),
+        a["ws_bytes"], None)
+
+
+def test_backward_checks_arguments_on_the_host(binding):
+    b = binding
+    fwd = b.df_attn_workspace_size(2, 2, 64, 64)
+    bwd = b.df_attn_bwd_workspace_size(2, 2, 64, 64)
+    # the bucket sums alone take 2 tables x T x H x 2 span floats
+    assert bwd >= fwd + 2 * 128 * 2 * 512 * 4
+    assert b.df_attn_bwd_workspace_size(2, 2, 64, 64, buckets=0, max_rel=512) == 0  # 2 span > 512
+    assert b.df_attn_bwd_workspace_size(2, 2, 64, 48) == 0
+    assert _bwd_raw(b, buckets=0, span=512) == b.DF_ERR_UNSUPPORTED
+    assert _bwd_raw(b, d=96) == b.DF_ERR_UNSUPPORTED
+    assert _bwd_raw(b, ws_bytes=bwd - 1) == b.DF_ERR_WORKSPACE
+    assert _bwd_raw(b, dpk=None) == b.DF_ERR_INVALID_ARG
+    assert _bwd_raw(b, do=None) == b.DF_ERR_INVALID_ARG
+    assert _bwd_raw(b, dq=None) == b.DF_ERR_INVALID_ARG
+    assert _bwd_raw(b, do=0x58004) == b.DF_ERR_ALIGNMENT
+    assert _bwd_raw(b, dv=0x80008) == b.DF_ERR_ALIGNMENT
+    assert _bwd_raw(b, mask=None) == b.DF_ERR_INVALID_ARG

@@ -21,7 +21,8 @@ import pytest
 import torch
 
 from oracle import attend_packed, attend_padded, attend_sequence
-from oracle.backward import backward_head, backward_packed, backward_padded, backward_sequence
+from oracle.backward import (backward_head, backward_keys, backward_packed, backward_padded,
+                             backward_rows, backward_sequence)
 
 CFG = dict(buckets=4, max_rel=8, span=4)   # mid 2: identity |r| <= 2, log zone, saturation at 7
 
@@ -147,3 +148,32 @@ def test_degenerate_lengths(n):
     # one token attends only to itself with weight 1: O = V, every score gradient is 0
     assert np.all(dq == 0) and np.all(dk == 0) and np.all(dpk == 0) and np.all(dpq == 0)
     np.testing.assert_array_equal(dv, w)
+
+
+def test_row_and_key_helpers_match_the_full_backward():
+    rng = np.random.default_rng(17)
+    n, d = 70, 8
+    cfg = dict(buckets=16, max_rel=32, span=16)
+    q, k, v, w = (_rand(rng, n, d) for _ in range(4))
+    pk, pq = (_rand(rng, 32, d) for _ in range(2))
+    valid = rng.random(n) > 0.15
+    dq, dk, dv, _, _ = backward_head(q, k, v, pk, pq, w, valid=valid, **cfg)
+    rows = np.array([0, 5, 33, 69, int(np.nonzero(~valid)[0][0])])
+    np.testing.assert_allclose(backward_rows(q, k, v, pk, pq, w, rows, valid=valid, **cfg), dq[rows],
+                               rtol=1e-10, atol=1e-12)
+    bk, bv = backward_keys(q, k, v, pk, pq, w, rows, valid=valid, **cfg)
+    np.testing.assert_allclose(bk, dk[rows], rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(bv, dv[rows], rtol=1e-10, atol=1e-12)
+
+
+def test_gradient_product_identity():
+    """sum dK.K - sum dPQ.PQ = sum dQ.Q - sum dPK.PK (both are sum_ij dS_ij Q_i.K_j)."""
+    rng = np.random.default_rng(18)
+    n, d = 50, 6
+    cfg = dict(buckets=16, max_rel=32, span=16)
+    q, k, v, w = (_rand(rng, n, d) for _ in range(4))
+    pk, pq = (_rand(rng, 32, d) for _ in range(2))
+    dq, dk, dv, dpk, dpq = backward_head(q, k, v, pk, pq, w, **cfg)
+    lhs = np.sum(dk * k) - np.sum(dpq * pq)
+    rhs = np.sum(dq * q) - np.sum(dpk * pk)
+    assert abs(lhs - rhs) < 1e-10 * (1 + abs(lhs))
