@@ -44,9 +44,10 @@ def parse_args(argv=None):
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--op", choices=["attention", "pack", "linear", "encoder"], default="attention",
+    ap.add_argument("--op", choices=["attention", "pack", "linear", "encoder", "bwd"], default="attention",
                     help="pack: the padded <-> packed conversion; linear: the QKV and PK/PQ projections; "
-                         "encoder: a 12-layer DeBERTa-v3-base encoder on synthetic weights")
+                         "encoder: a 12-layer DeBERTa-v3-base encoder on synthetic weights; "
+                         "bwd: the backward pass (dQ, dK, dV, dPK, dPQ) of the attention")
     return ap.parse_args(argv)
 
 
@@ -394,6 +395,136 @@ def run_linear(args, local):
     print(json.dumps(line), flush=True)
 
 
+def bwd_kernel_flops(lengths, H, d, span):
+    """Algorithmic flops of the two backward tile kernels.  Query kernel: the
+    forward recomputed (Q.K^T and P.V) and a second Q.K^T with dP = dO.V^T and
+    dQ = dS.K, 10 n^2 d; key kernel: Q.K^T, dP, dK = dS^T.Q and dV = P^T.dO,
+    8 n^2 d.  Each recomputation of the scores also costs the two position
+    projections, 8 n span d (two in the query kernel, one in the key kernel)."""
+    q = sum(H * (10.0 * n * n * d + 16.0 * n * span * d) for n in lengths)
+    k = sum(H * (8.0 * n * n * d + 8.0 * n * span * d) for n in lengths)
+    return float(q), float(k)
+
+
+def run_bwd(args, local):
+    """Backward pass of the attention (df_attn_bwd, strict fp32 on CUDA cores)
+    over the same workload as the forward bench; the metric counts 22 n^2 d per
+    head (the eleven n x n x d products of the direct formulation)."""
+    torch.cuda.set_device(local)
+    from exact_attention_deberta_gb300.build import build
+    build()
+    from exact_attention_deberta_gb300 import binding, synth
+    from oracle import backward_head, backward_metric_flops
+    x = synth.make_inputs(args.workload)
+    H, d, span = x.w.H, x.w.d, x.w.span
+    kw = dict(buckets=x.w.buckets, max_rel=x.w.max_rel, span=span)
+    host = {n: getattr(x, n) for n in ("q", "k", "v", "pk", "pq", "key_mask", "cu_seqlens")
+            if getattr(x, n) is not None}
+    host["dout"] = synth.grad_output(x)
+    dev = {n: t.cuda() for n, t in host.items()}
+    B = len(x.lengths)
+    ws = torch.empty(binding.df_attn_bwd_workspace_size(B, H, x.w.L, d, **kw), dtype=torch.uint8,
+                     device="cuda")
+    f32 = dict(dtype=torch.float32, device="cuda")
+    grads = tuple(torch.empty(dev["q"].shape, **f32) for _ in range(3)) + tuple(
+        torch.empty(dev["pk"].shape, **f32) for _ in range(2))
+    stream = torch.cuda.current_stream()
+
+    def step(inp):
+        mode = (dict(cu_seqlens=inp["cu_seqlens"], max_seqlen=x.w.L) if x.w.layout == "packed"
+                else dict(key_mask=inp["key_mask"]))
+        binding.df_attn_bwd(inp["q"], inp["k"], inp["v"], inp["pk"], inp["pq"], inp["dout"], grads=grads,
+                            workspace=ws, **mode, **kw)
+
+    for _ in range(args.warmup):
+        step(dev)
+    torch.cuda.synchronize()
+    assert binding.df_attn_get_device_status(ws) == binding.DF_OK
+    launches = binding.df_attn_last_launch_count()
+    kev = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(3)) for _ in range(args.steps)]
+    for evs in kev:
+        for e in evs:
+            e.record(stream)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        t0.record(stream)
+        for i in range(args.steps):
+            binding.df_attn_set_profile_events(kev[i][0], kev[i][2])
+            binding.df_attn_set_profile_split(kev[i][1])
+            step(dev)
+        t1.record(stream)
+        torch.cuda.synchronize()
+    binding.df_attn_set_profile_events(None, None)
+    binding.df_attn_set_profile_split(None)
+    ms = t0.elapsed_time(t1) / args.steps
+    q_ms = sum(a.elapsed_time(m) for a, m, _ in kev) / args.steps
+    k_ms = sum(m.elapsed_time(b) for _, m, b in kev) / args.steps
+    e2e = None
+    if not args.no_e2e:
+        pinned = {n: t.pin_memory() for n, t in host.items()}
+        dev2 = {n: torch.empty_like(t) for n, t in dev.items()}
+        outs = [torch.empty(g.shape, dtype=g.dtype, pin_memory=True) for g in grads]
+        h2d = sum(t.numel() * t.element_size() for t in pinned.values())
+        d2h = sum(t.numel() * t.element_size() for t in outs)
+        steps_e2e = max(1, min(args.steps, 3))
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps_e2e):
+            for n in pinned:
+                dev2[n].copy_(pinned[n], non_blocking=True)
+            step(dev2)
+            for o, g in zip(outs, grads):
+                o.copy_(g, non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e2e = (e0.elapsed_time(e1) / steps_e2e, h2d, d2h)
+    flops = backward_metric_flops(x.lengths, H, d)
+    value = flops / ms / 1e9
+    q_flops, k_flops = bwd_kernel_flops(x.lengths, H, d, span)
+    peak = 152 * 128 * 2 * 2.07e9 / 1e12
+    kern = [("bwd_q_kernel", q_flops, q_ms), ("bwd_k_kernel", k_flops, k_ms)]
+    kern.sort(key=lambda t: -t[2])
+    (kname, kfl, kms), (oname, ofl, oms) = kern
+    line = {"metric": "disentangled-attn bwd TFLOP/s (22*L^2*d/head)", "value": value, "unit": "TFLOP/s",
+            "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic",
+            "config": {"workload": x.w.name, "sequences": len(x.lengths), "seq_len": int(x.w.L), "H": H,
+                       "d": d, "io_dtype": x.w.dtype, "grad_dtype": "fp32", "layout": x.w.layout,
+                       "buckets": x.w.buckets, "max_rel": x.w.max_rel, "span": span,
+                       "l2": "inputs and gradients larger than L2"},
+            "gpu_launches": launches * args.steps,
+            "roofline": {"bound": "alu", "achieved": kfl / (kms * 1e-3) / 1e12, "peak": peak, "unit": "TFLOP/s",
+                         "frac": kfl / (kms * 1e-3) / 1e12 / peak, "traffic": None, "kernel": kname,
+                         "kernel_ms": kms, "algorithmic_flops": kfl,
+                         "peak_source": "derived: 152 SM x 128 FP32 lanes x 2 x 2.07 GHz",
+                         "other_kernel": {"kernel": oname, "kernel_ms": oms, "algorithmic_flops": ofl,
+                                          "achieved": ofl / (oms * 1e-3) / 1e12,
+                                          "frac": ofl / (oms * 1e-3) / 1e12 / peak},
+                         "rest_ms": ms - q_ms - k_ms},
+            "clocks": clk.summary()}
+    if e2e:
+        line["e2e"] = {"value": flops / e2e[0] / 1e9, "unit": "TFLOP/s", "h2d_bytes_per_step": e2e[1],
+                       "d2h_bytes_per_step": e2e[2]}
+    if not args.no_cpu_baseline:
+        # the first sequence, heads 0..2 (about 10 s of float64 work on 16 cores)
+        n = int(x.lengths[0])
+        st = int(x.cu_seqlens[0]) if x.w.layout == "packed" else 0
+        sl = slice(st, st + n)
+        heads = min(3, H)
+        t_0 = time.perf_counter()
+        for h in range(heads):
+            a = [t[sl, h] for t in (x.q, x.k, x.v)] + [x.pk[:, h], x.pq[:, h], host["dout"][sl, h]]
+            backward_head(*a, **kw)
+        secs = time.perf_counter() - t_0
+        line["cpu_baseline"] = {"value": heads * 22.0 * n * n * d / secs / 1e12, "unit": "TFLOP/s",
+                                "cores": torch.get_num_threads(), "kind": "oracle",
+                                "sample": f"backward of heads 0..{heads - 1} of one {n}-token sequence, "
+                                          f"float64 numpy, {secs:.1f} s"}
+    print(json.dumps(line), flush=True)
+
+
 def run_encoder(args, local):
     """The pages' benchmark workload in kind: a 12-layer DeBERTa-v3-base encoder
     (hidden 768, 12 heads, FFN 3072, buckets 256, max_rel 512) on the packed
@@ -456,9 +587,9 @@ def main(argv=None):
     if args.impl == "reference":
         run_reference(args, rank, world)
         return
-    if args.op in ("pack", "linear", "encoder"):
+    if args.op in ("pack", "linear", "encoder", "bwd"):
         if rank == 0:
-            {"pack": run_pack, "linear": run_linear, "encoder": run_encoder}[args.op](args, local)
+            {"pack": run_pack, "linear": run_linear, "encoder": run_encoder, "bwd": run_bwd}[args.op](args, local)
         return
     assert args.warmup >= 3, "at least 3 warm-up steps"
     torch.cuda.set_device(local)
