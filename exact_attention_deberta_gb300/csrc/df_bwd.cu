@@ -15,11 +15,14 @@
 // Launches (one stream, in order):
 //   query kernel  per 64 query rows: pass 1 is the forward in fp32 (row
 //                 log-sum-exp and O, hence D_i); pass 2 recomputes the tiles,
-//                 forms dS, accumulates dQ = dS.K and the row's bucket sums
-//                 G_c2p[i][r] = sum_{j: idx_ij = r} dS_ij in shared memory.
+//                 forms dS, accumulates dQ = dS.K and the bucket sums
+//                 G_c2p[i][r] = sum_{j: idx_ij = r} dS_ij.
 //   key kernel    per 64 keys: recomputes the tiles with the stored row
 //                 statistics, accumulates dV = P^T.dO, dK = dS^T.Q and the
-//                 column's bucket sums G_p2c[j][r].
+//                 bucket sums G_p2c[j][r].
+// The bucket sums go to the zero-initialised global tables with atomic adds
+// from near tiles; a far tile has a single relative index, so its row (column)
+// sums stay in registers for the whole block and are added once at the end.
 //   GEMMs         dQ += G_c2p.PK, dK += G_p2c.PQ, and dPK = G_c2p^T.Q,
 //                 dPQ = G_p2c^T.K reduced over fixed token ranges (partial
 //                 sums, then one summing kernel; no global atomics).
@@ -54,8 +57,13 @@ struct BwdSmem {
   static constexpr int pq = pk + DC * (WB + 1);    // [DC][WB + 1] PQ band; later tile B [BM][BN]
   static constexpr int rowA = pq + DC * (WB + 1);  // [2][BM] query scalars (neg, pos side)
   static constexpr int colB = rowA + 2 * BM;       // [3][BN] key scalars (neg, pos), key bias
-  static constexpr int big = colB + 3 * BN;        // bucket sums [64][R] (pass 1: V and P)
+  static constexpr int floats = colB + 3 * BN;
   static_assert(BM * BN <= DC * (WB + 1), "tiles A and B reuse the band buffers");
+  // pass 1 of the query kernel keeps V [BN][D] and P [BM][BN + 1] in the dO,
+  // V and band buffers, which it does not otherwise use after the scores
+  static constexpr int pass1 = g;
+  static constexpr int pass1_floats = pk + 2 * DC * (WB + 1) - g;
+  static_assert(BN * 128 + BM * (BN + 1) <= pass1_floats, "pass-1 V and P fit at d = 128");
 };
 
 struct TileGeom {
@@ -82,14 +90,15 @@ __device__ __forceinline__ void tile_geom(const Problem& p, int rsp, int rsn, in
   }
 }
 
-// Raw score terms of tile (i0, j0): s = Q.K^T, and for a near tile the
-// position products cp = Q_i.PK[idx], pc = K_j.PQ[idx]; with DP also
-// dp = dO.V^T.  Also stages the query / key scalars of the tile.
+// Raw score of tile (i0, j0): s = Q.K^T, plus for a near tile the position
+// products Q_i.PK[idx] + K_j.PQ[idx] in the same accumulator; with DP also
+// dp = dO.V^T.  Also stages the query / key scalars of the tile.  Every kernel
+// forms the scores through this function, so they agree to the last bit.
 template <typename T, int D, bool DP>
 __device__ __forceinline__ void score_tile(const Problem& p, const T* __restrict__ gdo,
                                            const float* scal_h, int start, int n, int h, int i0,
                                            int j0, const TileGeom& g, float* sm, float (&s)[4][4],
-                                           float (&cp)[4][4], float (&pc)[4][4], float (&dp)[4][4]) {
+                                           float (&dp)[4][4]) {
   const T* __restrict__ gq = static_cast<const T*>(p.q);
   const T* __restrict__ gk = static_cast<const T*>(p.k);
   const T* __restrict__ gv = static_cast<const T*>(p.v);
@@ -121,7 +130,7 @@ __device__ __forceinline__ void score_tile(const Problem& p, const T* __restrict
 #pragma unroll
   for (int a = 0; a < 4; ++a)
 #pragma unroll
-    for (int b = 0; b < 4; ++b) s[a][b] = cp[a][b] = pc[a][b] = dp[a][b] = 0.f;
+    for (int b = 0; b < 4; ++b) s[a][b] = dp[a][b] = 0.f;
   for (int kc = 0; kc < D; kc += DC) {
     if (kc) __syncthreads();
     for (int e = tid; e < BM * DC; e += kThreads) {
@@ -166,8 +175,8 @@ __device__ __forceinline__ void score_tile(const Problem& p, const T* __restrict
         for (int a = 0; a < 4; ++a)
 #pragma unroll
           for (int b = 0; b < 4; ++b) {
-            cp[a][b] = fmaf(qa[a], pkd[a - b + 3], cp[a][b]);
-            pc[a][b] = fmaf(kb[b], pqd[a - b + 3], pc[a][b]);
+            s[a][b] = fmaf(qa[a], pkd[a - b + 3], s[a][b]);
+            s[a][b] = fmaf(kb[b], pqd[a - b + 3], s[a][b]);
           }
       }
       if (DP) {
@@ -188,8 +197,7 @@ __device__ __forceinline__ void score_tile(const Problem& p, const T* __restrict
 // Logits of the tile in log2 units (the forward's), -inf at masked and
 // out-of-range keys.
 __device__ __forceinline__ void tile_logits(const float* sm, const TileGeom& g, int n, int j0, float ks,
-                                            const float (&s)[4][4], const float (&cp)[4][4],
-                                            const float (&pc)[4][4], float (&x)[4][4]) {
+                                            const float (&s)[4][4], float (&x)[4][4]) {
   const float* rowA = sm + BwdSmem::rowA;
   const float* colB = sm + BwdSmem::colB;
   const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
@@ -204,27 +212,32 @@ __device__ __forceinline__ void tile_logits(const float* sm, const TileGeom& g, 
         const float be = g.far_pos ? colB[BN + jj] : colB[jj];
         v = fmaf(s[a][b], ks, al + be);
       } else {
-        v = fmaf(s[a][b] + cp[a][b] + pc[a][b], ks, colB[2 * BN + jj]);
+        v = fmaf(s[a][b], ks, colB[2 * BN + jj]);
       }
       x[a][b] = j0 + jj < n ? v : -INFINITY;
     }
 }
 
-// Adds the tile's dS to the bucket sums: rows of G are the tile's query rows
-// (BY_ROW) or its keys.  A far tile has one relative index, so each thread
-// first sums its four entries of a row (column).
+// Adds the tile's dS to the bucket sums.  G points at the table row of the
+// block's first query row (BY_ROW) or key, rows H * R floats apart; `lim` is
+// the number of rows inside the sequence.  Near tiles add each nonzero entry
+// to the global table; a far tile has one relative index (bucket 0 or
+// 2 span - 1), so its entries go to the per-thread sums `far` ([row or
+// column u][side]), flushed by the caller.
 template <bool BY_ROW>
-__device__ __forceinline__ void bucket_sums(float* G, int R, const TileGeom& g, const float (&ds)[4][4]) {
+__device__ __forceinline__ void bucket_sums(float* G, size_t row_stride, int lim, const TileGeom& g,
+                                            const float (&ds)[4][4], float (&far)[4][2]) {
   const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
   if (g.far) {
-    const int r = g.far_pos ? R - 1 : 0;
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
       float sum = 0.f;
 #pragma unroll
       for (int e = 0; e < 4; ++e) sum += BY_ROW ? ds[u][e] : ds[e][u];
-      const int row = BY_ROW ? ty + 16 * u : tx + 16 * u;
-      atomicAdd(G + (size_t)row * R + r, sum);
+      if (g.far_pos)
+        far[u][1] += sum;
+      else
+        far[u][0] += sum;
     }
   } else {
 #pragma unroll
@@ -232,14 +245,15 @@ __device__ __forceinline__ void bucket_sums(float* G, int R, const TileGeom& g, 
 #pragma unroll
       for (int b = 0; b < 4; ++b) {
         const int row = BY_ROW ? ty + 16 * a : tx + 16 * b;
-        atomicAdd(G + (size_t)row * R + g.lo + g.col[a - b + 3], ds[a][b]);
+        if (row < lim && ds[a][b] != 0.f)
+          atomicAdd(G + (size_t)row * row_stride + g.lo + g.col[a - b + 3], ds[a][b]);
       }
   }
 }
 
 // ---------------------------------------------------------------- query side
 template <typename T, int D>
-__global__ void __launch_bounds__(kThreads) bwd_q_kernel(const BwdProblem b) {
+__global__ void __launch_bounds__(kThreads, D <= 64 ? 2 : 1) bwd_q_kernel(const BwdProblem b) {
   extern __shared__ float sm[];
   const Problem& p = b.f;
   constexpr int NC = D / 16;  // output columns per thread
@@ -252,10 +266,9 @@ __global__ void __launch_bounds__(kThreads) bwd_q_kernel(const BwdProblem b) {
   const int n_items = p.hdr->n_items;
   const int rsp = p.hdr->r_sat_pos, rsn = p.hdr->r_sat_neg;
   const float ks = p.kscale;
-  float* G = sm + BwdSmem::big;   // pass 2: [BM][R]
-  float* Vs = G;                  // pass 1: [BN][D]
-  float* Ps = G + BN * D;         // pass 1: [BM][BN + 1]
-  float* tA = sm + BwdSmem::pk;   // pass 2: dS tile [BM][BN]
+  float* Vs = sm + BwdSmem::pass1;  // pass 1: [BN][D]
+  float* Ps = Vs + BN * D;          // pass 1: [BM][BN + 1]
+  float* tA = sm + BwdSmem::pk;     // pass 2: dS tile [BM][BN]
   float* Ks = sm + BwdSmem::k;
 
   for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
@@ -279,9 +292,10 @@ __global__ void __launch_bounds__(kThreads) bwd_q_kernel(const BwdProblem b) {
         const int j0 = jb * BN;
         TileGeom g;
         tile_geom(p, rsp, rsn, i0, j0, ty, tx, g);
-        float s[4][4], cp[4][4], pc[4][4], dp[4][4], x[4][4];
-        score_tile<T, D, false>(p, gdo, scal_h, start, n, h, i0, j0, g, sm, s, cp, pc, dp);
-        tile_logits(sm, g, n, j0, ks, s, cp, pc, x);
+        float s[4][4], dp[4][4], x[4][4];
+        score_tile<T, D, false>(p, gdo, scal_h, start, n, h, i0, j0, g, sm, s, dp);
+        tile_logits(sm, g, n, j0, ks, s, x);
+        __syncthreads();  // V and P overwrite the band buffers
 #pragma unroll
         for (int a = 0; a < 4; ++a) {
           float mt = fmaxf(fmaxf(x[a][0], x[a][1]), fmaxf(x[a][2], x[a][3]));
@@ -346,20 +360,21 @@ __global__ void __launch_bounds__(kThreads) bwd_q_kernel(const BwdProblem b) {
         }
       }
       // ---- pass 2: dS, dQ = dS.K and the rows' bucket sums
-      __syncthreads();  // pass-1 readers of V and P are done
-      for (int e = tid; e < BM * R; e += kThreads) G[e] = 0.f;
-      float dq[4][NC];
+      float* G = b.gc + ((size_t)(start + i0) * H + h) * R;
+      float dq[4][NC], far[4][2];
 #pragma unroll
-      for (int a = 0; a < 4; ++a)
+      for (int a = 0; a < 4; ++a) {
+        far[a][0] = far[a][1] = 0.f;
 #pragma unroll
         for (int c = 0; c < NC; ++c) dq[a][c] = 0.f;
+      }
       for (int jb = 0; jb < nkb; ++jb) {
         const int j0 = jb * BN;
         TileGeom g;
         tile_geom(p, rsp, rsn, i0, j0, ty, tx, g);
-        float s[4][4], cp[4][4], pc[4][4], dp[4][4], x[4][4], ds[4][4];
-        score_tile<T, D, true>(p, gdo, scal_h, start, n, h, i0, j0, g, sm, s, cp, pc, dp);
-        tile_logits(sm, g, n, j0, ks, s, cp, pc, x);
+        float s[4][4], dp[4][4], x[4][4], ds[4][4];
+        score_tile<T, D, true>(p, gdo, scal_h, start, n, h, i0, j0, g, sm, s, dp);
+        tile_logits(sm, g, n, j0, ks, s, x);
 #pragma unroll
         for (int a = 0; a < 4; ++a)
 #pragma unroll
@@ -370,7 +385,7 @@ __global__ void __launch_bounds__(kThreads) bwd_q_kernel(const BwdProblem b) {
         for (int a = 0; a < 4; ++a)
 #pragma unroll
           for (int bb = 0; bb < 4; ++bb) tA[(ty + 16 * a) * BN + tx + 16 * bb] = ds[a][bb];
-        bucket_sums<true>(G, R, g, ds);
+        bucket_sums<true>(G, (size_t)H * R, n - i0, g, ds, far);
 #pragma unroll
         for (int kc = 0; kc < D; kc += DC) {
           __syncthreads();
@@ -395,16 +410,21 @@ __global__ void __launch_bounds__(kThreads) bwd_q_kernel(const BwdProblem b) {
 #pragma unroll
       for (int a = 0; a < 4; ++a) {
         const int i = i0 + ty + 16 * a;
+        // far-tile sums of the row: reduce over the 16 lanes that share it
+#pragma unroll
+        for (int sd = 0; sd < 2; ++sd)
+#pragma unroll
+          for (int off = 8; off > 0; off >>= 1) far[a][sd] += __shfl_xor_sync(0xffffffffu, far[a][sd], off);
         if (i < n) {
           float* dst = b.dq + ((size_t)(start + i) * H + h) * D;
 #pragma unroll
           for (int c = 0; c < NC; ++c) dst[tx + 16 * c] = dq[a][c];
+          if (tx == 0) {
+            float* grow = G + (size_t)(ty + 16 * a) * H * R;
+            if (far[a][0] != 0.f) atomicAdd(grow, far[a][0]);
+            if (far[a][1] != 0.f) atomicAdd(grow + R - 1, far[a][1]);
+          }
         }
-      }
-      __syncthreads();  // every bucket-sum atomic has landed
-      for (int e = tid; e < BM * R; e += kThreads) {
-        const int r = e / R, c = e % R;
-        if (i0 + r < n) b.gc[((size_t)(start + i0 + r) * H + h) * R + c] = G[e];
       }
     }
   }
@@ -412,7 +432,7 @@ __global__ void __launch_bounds__(kThreads) bwd_q_kernel(const BwdProblem b) {
 
 // ------------------------------------------------------------------ key side
 template <typename T, int D>
-__global__ void __launch_bounds__(kThreads) bwd_k_kernel(const BwdProblem b) {
+__global__ void __launch_bounds__(kThreads, D <= 64 ? 2 : 1) bwd_k_kernel(const BwdProblem b) {
   extern __shared__ float sm[];
   const Problem& p = b.f;
   constexpr int NC = D / 16;
@@ -424,7 +444,6 @@ __global__ void __launch_bounds__(kThreads) bwd_k_kernel(const BwdProblem b) {
   const int n_items = p.hdr->n_items;
   const int rsp = p.hdr->r_sat_pos, rsn = p.hdr->r_sat_neg;
   const float ks = p.kscale;
-  float* G = sm + BwdSmem::big;  // [BN][R]
   float* tA = sm + BwdSmem::pk;  // P tile [BM][BN]
   float* tB = sm + BwdSmem::pq;  // dS tile [BM][BN]
   float* Qs = sm + BwdSmem::q;
@@ -438,20 +457,21 @@ __global__ void __launch_bounds__(kThreads) bwd_k_kernel(const BwdProblem b) {
     for (int sub = 0; sub < kQBlock / BN; ++sub) {
       const int j0 = kb * kQBlock + sub * BN;
       if (j0 >= n) break;
-      __syncthreads();  // the previous block's bucket sums are written out
-      for (int e = tid; e < BN * R; e += kThreads) G[e] = 0.f;
-      float dk[4][NC], dv[4][NC];
+      float* G = b.gp + ((size_t)(start + j0) * H + h) * R;
+      float dk[4][NC], dv[4][NC], far[4][2];
 #pragma unroll
-      for (int a = 0; a < 4; ++a)
+      for (int a = 0; a < 4; ++a) {
+        far[a][0] = far[a][1] = 0.f;
 #pragma unroll
         for (int c = 0; c < NC; ++c) dk[a][c] = dv[a][c] = 0.f;
+      }
       for (int ib = 0; ib < nqb; ++ib) {
         const int i0 = ib * BM;
         TileGeom g;
         tile_geom(p, rsp, rsn, i0, j0, ty, tx, g);
-        float s[4][4], cp[4][4], pc[4][4], dp[4][4], x[4][4], pe[4][4], ds[4][4];
-        score_tile<T, D, true>(p, gdo, scal_h, start, n, h, i0, j0, g, sm, s, cp, pc, dp);
-        tile_logits(sm, g, n, j0, ks, s, cp, pc, x);
+        float s[4][4], dp[4][4], x[4][4], pe[4][4], ds[4][4];
+        score_tile<T, D, true>(p, gdo, scal_h, start, n, h, i0, j0, g, sm, s, dp);
+        tile_logits(sm, g, n, j0, ks, s, x);
 #pragma unroll
         for (int a = 0; a < 4; ++a) {
           const int i = i0 + ty + 16 * a;
@@ -472,7 +492,7 @@ __global__ void __launch_bounds__(kThreads) bwd_k_kernel(const BwdProblem b) {
             tA[(ty + 16 * a) * BN + tx + 16 * bb] = pe[a][bb];
             tB[(ty + 16 * a) * BN + tx + 16 * bb] = ds[a][bb];
           }
-        bucket_sums<false>(G, R, g, ds);
+        bucket_sums<false>(G, (size_t)H * R, n - j0, g, ds, far);
         // dK += dS^T.Q and dV += P^T.dO over this query block, chunk by chunk;
         // thread rows are keys ty + 16 a
 #pragma unroll
@@ -513,11 +533,17 @@ __global__ void __launch_bounds__(kThreads) bwd_k_kernel(const BwdProblem b) {
           }
         }
       }
-      __syncthreads();  // every bucket-sum atomic has landed
-      for (int e = tid; e < BN * R; e += kThreads) {
-        const int r = e / R, c = e % R;
-        if (j0 + r < n) b.gp[((size_t)(start + j0 + r) * H + h) * R + c] = G[e];
-      }
+      // far-tile sums of key column tx + 16 u: the two half-warps hold
+      // neighbouring query rows of the same keys
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+#pragma unroll
+        for (int sd = 0; sd < 2; ++sd) {
+          const float v = far[u][sd] + __shfl_xor_sync(0xffffffffu, far[u][sd], 16);
+          const int jj = tx + 16 * u;
+          if ((threadIdx.x & 16) == 0 && jj < n - j0 && v != 0.f)
+            atomicAdd(G + (size_t)jj * H * R + (sd ? R - 1 : 0), v);
+        }
     }
   }
 }
@@ -625,9 +651,8 @@ cudaError_t launch_typed(const BwdProblem& b, cudaStream_t s, cudaEvent_t ev0, c
                          cudaEvent_t ev1, int* launches) {
   const Problem& p = b.f;
   const int H = p.H, R = b.R, T_ = p.T;
-  const size_t big_q = std::max((size_t)BM * R, (size_t)BN * D + (size_t)BM * (BN + 1));
-  const size_t bytes_q = (BwdSmem::big + big_q) * sizeof(float);
-  const size_t bytes_k = (BwdSmem::big + (size_t)BN * R) * sizeof(float);
+  const size_t bytes_q = BwdSmem::floats * sizeof(float);
+  const size_t bytes_k = bytes_q;
   cudaError_t e = cudaFuncSetAttribute(bwd_q_kernel<T, D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)bytes_q);
   if (e != cudaSuccess) return e;
