@@ -90,6 +90,33 @@ __device__ __forceinline__ void tile_geom(const Problem& p, int rsp, int rsn, in
   }
 }
 
+// dst[c * STRIDE + r] = fp32 of row r, column c (c < DC) of a [rows][ts]
+// array starting at `base`, for r < rows; rows at or past `lim` read as 0.
+// Each thread moves 16-byte vectors; within a warp the transposed stores hit
+// 32 different banks (STRIDE = 1 modulo 32).
+template <typename T, int STRIDE>
+__device__ __forceinline__ void stage_t(const T* __restrict__ base, size_t ts, int rows, int lim,
+                                        float* dst) {
+  constexpr int V = 16 / sizeof(T);  // elements per vector
+  constexpr int VPR = DC / V;        // vectors per row
+  static_assert(STRIDE % 32 == 1, "conflict-free transposed stores");
+  for (int e = threadIdx.x; e < rows * VPR; e += kThreads) {
+    const int r = e / VPR, v = e % VPR;
+    float f[V];
+    if (r < lim) {
+      const uint4 raw = *reinterpret_cast<const uint4*>(base + (size_t)r * ts + v * V);
+      const T* el = reinterpret_cast<const T*>(&raw);
+#pragma unroll
+      for (int k = 0; k < V; ++k) f[k] = IO<T>::to_f(el[k]);
+    } else {
+#pragma unroll
+      for (int k = 0; k < V; ++k) f[k] = 0.f;
+    }
+#pragma unroll
+    for (int k = 0; k < V; ++k) dst[(v * V + k) * STRIDE + r] = f[k];
+  }
+}
+
 // Raw score of tile (i0, j0): s = Q.K^T, plus for a near tile the position
 // products Q_i.PK[idx] + K_j.PQ[idx] in the same accumulator; with DP also
 // dp = dO.V^T.  Also stages the query / key scalars of the tile.  Every kernel
@@ -133,24 +160,18 @@ __device__ __forceinline__ void score_tile(const Problem& p, const T* __restrict
     for (int b = 0; b < 4; ++b) s[a][b] = dp[a][b] = 0.f;
   for (int kc = 0; kc < D; kc += DC) {
     if (kc) __syncthreads();
-    for (int e = tid; e < BM * DC; e += kThreads) {
-      const int r = e / DC, c = e % DC;
-      const size_t off = (size_t)h * D + kc + c;
-      const bool qi = i0 + r < n, kj = j0 + r < n;
-      Qs[c * (BM + 1) + r] = qi ? IO<T>::load(gq + (start + i0 + r) * ts + off) : 0.f;
-      Ks[c * (BN + 1) + r] = kj ? IO<T>::load(gk + (start + j0 + r) * ts + off) : 0.f;
-      if (DP) {
-        Gs[c * (BM + 1) + r] = qi ? IO<T>::load(gdo + (start + i0 + r) * ts + off) : 0.f;
-        Vc[c * (BN + 1) + r] = kj ? IO<T>::load(gv + (start + j0 + r) * ts + off) : 0.f;
-      }
+    const size_t qrow = (size_t)(start + i0) * ts + (size_t)h * D + kc;
+    const size_t krow = (size_t)(start + j0) * ts + (size_t)h * D + kc;
+    stage_t<T, BM + 1>(gq + qrow, ts, BM, n - i0, Qs);
+    stage_t<T, BN + 1>(gk + krow, ts, BN, n - j0, Ks);
+    if (DP) {
+      stage_t<T, BM + 1>(gdo + qrow, ts, BM, n - i0, Gs);
+      stage_t<T, BN + 1>(gv + krow, ts, BN, n - j0, Vc);
     }
     if (!g.far) {
-      for (int e = tid; e < g.w * DC; e += kThreads) {
-        const int u = e / DC, c = e % DC;
-        const size_t off = (size_t)(g.lo + u) * ts + (size_t)h * D + kc + c;
-        PKs[c * (WB + 1) + u] = IO<T>::load(gpk + off);
-        PQs[c * (WB + 1) + u] = IO<T>::load(gpq + off);
-      }
+      const size_t prow = (size_t)g.lo * ts + (size_t)h * D + kc;
+      stage_t<T, WB + 1>(gpk + prow, ts, g.w, g.w, PKs);
+      stage_t<T, WB + 1>(gpq + prow, ts, g.w, g.w, PQs);
     }
     __syncthreads();
 #pragma unroll 2
@@ -315,9 +336,26 @@ __global__ void __launch_bounds__(kThreads, D <= 64 ? 2 : 1) bwd_q_kernel(const 
             Ps[(ty + 16 * a) * (BN + 1) + tx + 16 * bb] = pv;
           }
         }
-        for (int e = tid; e < BN * D; e += kThreads) {
-          const int j = e / D, c = e % D;
-          Vs[e] = j0 + j < n ? IO<T>::load(gv + (start + j0 + j) * ts + (size_t)h * D + c) : 0.f;
+        {
+          constexpr int V = 16 / sizeof(T), VPR = D / V;
+          for (int e = tid; e < BN * VPR; e += kThreads) {
+            const int j = e / VPR, v = e % VPR;
+            float4 f[V / 4];
+            if (j0 + j < n) {
+              const uint4 raw = *reinterpret_cast<const uint4*>(gv + (size_t)(start + j0 + j) * ts +
+                                                                (size_t)h * D + v * V);
+              const T* el = reinterpret_cast<const T*>(&raw);
+#pragma unroll
+              for (int k = 0; k < V / 4; ++k)
+                f[k] = make_float4(IO<T>::to_f(el[4 * k]), IO<T>::to_f(el[4 * k + 1]),
+                                   IO<T>::to_f(el[4 * k + 2]), IO<T>::to_f(el[4 * k + 3]));
+            } else {
+#pragma unroll
+              for (int k = 0; k < V / 4; ++k) f[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll
+            for (int k = 0; k < V / 4; ++k) reinterpret_cast<float4*>(Vs + j * D + v * V)[k] = f[k];
+          }
         }
         __syncthreads();
 #pragma unroll 4
@@ -389,11 +427,7 @@ __global__ void __launch_bounds__(kThreads, D <= 64 ? 2 : 1) bwd_q_kernel(const 
 #pragma unroll
         for (int kc = 0; kc < D; kc += DC) {
           __syncthreads();
-          for (int e = tid; e < BN * DC; e += kThreads) {
-            const int r = e / DC, c = e % DC;
-            Ks[c * (BN + 1) + r] =
-                j0 + r < n ? IO<T>::load(gk + (start + j0 + r) * ts + (size_t)h * D + kc + c) : 0.f;
-          }
+          stage_t<T, BN + 1>(gk + (size_t)(start + j0) * ts + (size_t)h * D + kc, ts, BN, n - j0, Ks);
           __syncthreads();
 #pragma unroll 4
           for (int j = 0; j < BN; ++j) {
@@ -498,13 +532,9 @@ __global__ void __launch_bounds__(kThreads, D <= 64 ? 2 : 1) bwd_k_kernel(const 
 #pragma unroll
         for (int kc = 0; kc < D; kc += DC) {
           __syncthreads();
-          for (int e = tid; e < BM * DC; e += kThreads) {
-            const int r = e / DC, c = e % DC;
-            const bool qi = i0 + r < n;
-            const size_t off = (size_t)(start + i0 + r) * ts + (size_t)h * D + kc + c;
-            Qs[c * (BM + 1) + r] = qi ? IO<T>::load(gq + off) : 0.f;
-            Gs[c * (BM + 1) + r] = qi ? IO<T>::load(gdo + off) : 0.f;
-          }
+          const size_t qrow = (size_t)(start + i0) * ts + (size_t)h * D + kc;
+          stage_t<T, BM + 1>(gq + qrow, ts, BM, n - i0, Qs);
+          stage_t<T, BM + 1>(gdo + qrow, ts, BM, n - i0, Gs);
           __syncthreads();
 #pragma unroll 4
           for (int i = 0; i < BM; ++i) {
