@@ -43,6 +43,8 @@ def parse_args(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--group-tokens", type=int, default=0,
+                    help="host-buffer forward: tokens per group of sequences (0: B*L/8)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--op", choices=["attention", "pack", "linear", "encoder", "bwd"], default="attention",
                     help="pack: the padded <-> packed conversion; linear: the QKV and PK/PQ projections; "
@@ -662,27 +664,33 @@ def main(argv=None):
 
     e2e = None
     if not args.no_e2e:
+        # the host-buffer entry point: page-locked inputs and output, the copies
+        # of each group of sequences overlapped with the kernels of another
         pinned = {n: t.pin_memory() for n, t in host.items()}
-        dev2 = {n: torch.empty_like(t) for n, t in dev.items()}
         out_h = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
         h2d = sum(t.numel() * t.element_size() for t in pinned.values())
         d2h = out_h.numel() * out_h.element_size()
+        scratch = torch.empty(binding.df_attn_fwd_host_scratch_size(
+            B, H, x.w.L, d, dev["q"].dtype, group_tokens=args.group_tokens, **kw), dtype=torch.uint8,
+            device="cuda")
+
+        def host_step():
+            mode = (dict(cu_seqlens=pinned["cu_seqlens"], max_seqlen=x.w.L) if x.w.layout == "packed"
+                    else dict(key_mask=pinned["key_mask"]))
+            binding.df_attn_fwd_host(pinned["q"], pinned["k"], pinned["v"], pinned["pk"], pinned["pq"],
+                                     out=out_h, group_tokens=args.group_tokens, scratch=scratch, **mode, **kw)
+
         for _ in range(2):
-            for n in pinned:
-                dev2[n].copy_(pinned[n], non_blocking=True)
-            step(dev2, out)
-            out_h.copy_(out, non_blocking=True)
+            host_step()
         torch.cuda.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
         for _ in range(args.steps):
-            for n in pinned:
-                dev2[n].copy_(pinned[n], non_blocking=True)
-            step(dev2, out)
-            out_h.copy_(out, non_blocking=True)
+            host_step()
         e1.record(stream)
         torch.cuda.synchronize()
         e2e_ms = e0.elapsed_time(e1) / args.steps
+        assert binding.df_attn_get_device_status(scratch) == binding.DF_OK
         e2e = (e2e_ms, h2d, d2h)
 
     # max over ranks

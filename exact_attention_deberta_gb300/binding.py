@@ -205,6 +205,47 @@ def df_attn_bwd(q, k, v, pos_key, pos_query, dout, key_mask=None, cu_seqlens=Non
     return dq, dk, dv, dpk, dpq
 
 
+_ll = ctypes.c_longlong
+_lib.df_attn_fwd_host.argtypes = [_vp] * 7 + [_i] * 9 + [_vp, _ll, _vp, _sz, _vp]
+_lib.df_attn_fwd_host.restype = _i
+_lib.df_attn_fwd_host_scratch_size.argtypes = [_i] * 8 + [_ll]
+_lib.df_attn_fwd_host_scratch_size.restype = _sz
+
+
+def df_attn_fwd_host_scratch_size(B, H, L, d, dtype, buckets=256, max_rel=512, span=None,
+                                  group_tokens=0) -> int:
+    span = default_span(buckets, max_rel) if span is None else span
+    dt = _DTYPE[dtype] if isinstance(dtype, torch.dtype) else int(dtype)
+    return int(_lib.df_attn_fwd_host_scratch_size(B, H, L, d, buckets, max_rel, span, dt, group_tokens))
+
+
+def df_attn_fwd_host(q, k, v, pos_key, pos_query, key_mask=None, cu_seqlens=None, *, max_seqlen=None,
+                     buckets=256, max_rel=512, span=None, out=None, group_tokens=0, scratch=None,
+                     stream=None):
+    """Forward from host (CPU, ideally pinned) tensors with the copies overlapped
+    with the kernels; returns ``out`` (a host tensor), complete once ``stream``
+    is synchronised."""
+    B, H, L, T, d = _shape_args(q, key_mask, cu_seqlens, max_seqlen)
+    span = default_span(buckets, max_rel) if span is None else span
+    for name, t in (("q", q), ("k", k), ("v", v), ("pos_key", pos_key), ("pos_query", pos_query),
+                    ("key_mask", key_mask), ("cu_seqlens", cu_seqlens), ("out", out)):
+        if t is not None and (t.is_cuda or not t.is_contiguous()):
+            raise ValueError(f"{name} must be a contiguous host tensor")
+    if out is None:
+        out = torch.empty(q.shape, dtype=q.dtype, pin_memory=True)
+    if scratch is None:
+        size = df_attn_fwd_host_scratch_size(B, H, L, d, q.dtype, buckets, max_rel, span, group_tokens)
+        if size == 0:
+            _check(DF_ERR_UNSUPPORTED, "df_attn_fwd_host_scratch_size")
+        scratch = torch.empty(size, dtype=torch.uint8, device="cuda")
+    st = _lib.df_attn_fwd_host(_ptr(q), _ptr(k), _ptr(v), _ptr(pos_key), _ptr(pos_query), _ptr(key_mask),
+                               _ptr(cu_seqlens), B, H, L, T, d, buckets, max_rel, span, _DTYPE[q.dtype],
+                               _ptr(out), int(group_tokens), _ptr(scratch), scratch.numel(),
+                               _stream(stream))
+    _check(st, "df_attn_fwd_host")
+    return out
+
+
 def df_attn_plan(q, k, pos_key, pos_query, key_mask=None, cu_seqlens=None, *, max_seqlen=None,
                  buckets=256, max_rel=512, span=None, out=None, workspace=None, stream=None):
     """Planning step alone; returns (out, workspace)."""

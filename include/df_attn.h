@@ -152,6 +152,42 @@ df_status df_attn_bwd(const void* q, const void* k, const void* v,
  * df_attn_bwd rejects. */
 size_t df_attn_bwd_workspace_size(int B, int H, int L, int d, int buckets, int max_rel, int span);
 
+/*
+ * Forward from HOST buffers with the copies overlapped: q, k, v, pos_key,
+ * pos_query, out, and key_mask / cu_seqlens are HOST pointers (page-locked
+ * memory lets the copies run asynchronously; pageable memory works but
+ * serialises them).  Sequences are independent (padded: batch rows), so the
+ * batch is cut into groups of whole sequences of at most
+ * max(group_tokens, L) tokens (group_tokens = 0: max(B*L/8, L)) and each group
+ * runs as one df_attn_fwd call, with results identical to a single call on
+ * the whole batch.  Two library-owned copy streams (created once per device)
+ * pipeline the copy-in of group g + 1 and the copy-out of group g - 1 around
+ * the forward of group g on `stream`; `stream` waits for the last copy-out, so
+ * `out` is complete once `stream` is.  In packed mode cu_seqlens is validated
+ * on the host (cu_seqlens[0] = 0, cu_seqlens[B] = total_tokens, every length
+ * in [0, L]).
+ *
+ *   scratch   device memory of df_attn_fwd_host_scratch_size() bytes, 256-byte
+ *             aligned: two slots of q, k, v, out for one group, the relative
+ *             embeddings and the forward's workspace, which sits at offset 0
+ *             (df_attn_get_device_status(scratch, stream) reads its status)
+ *
+ * Calls are serialised by a mutex while they enqueue; calls that share a
+ * scratch buffer must be ordered by their streams.  Returns DF_ERR_CUDA if a
+ * copy or event call fails (work may then be partly enqueued).
+ */
+df_status df_attn_fwd_host(const void* q, const void* k, const void* v,
+                           const void* pos_key, const void* pos_query,
+                           const uint8_t* key_mask, const int32_t* cu_seqlens,
+                           int B, int H, int L, int total_tokens, int d,
+                           int buckets, int max_rel, int span, df_dtype dtype,
+                           void* out, long long group_tokens,
+                           void* scratch, size_t scratch_bytes, df_stream_t stream);
+
+/* Bytes of device scratch df_attn_fwd_host needs (0 for rejected arguments). */
+size_t df_attn_fwd_host_scratch_size(int B, int H, int L, int d, int buckets, int max_rel, int span,
+                                     df_dtype dtype, long long group_tokens);
+
 /* DF_OK if (H, L, d, dtype, buckets, max_rel, span) is implemented; otherwise
  * DF_ERR_INVALID_ARG or DF_ERR_UNSUPPORTED.  Host only, no CUDA call. */
 df_status df_attn_supported(int H, int L, int d, df_dtype dtype, int buckets, int max_rel,

@@ -207,3 +207,30 @@ def test_backward_checks_arguments_on_the_host(binding):
     assert _bwd_raw(b, do=0x58004) == b.DF_ERR_ALIGNMENT
     assert _bwd_raw(b, dv=0x80008) == b.DF_ERR_ALIGNMENT
     assert _bwd_raw(b, mask=None) == b.DF_ERR_INVALID_ARG
+
+
+def test_host_forward_checks_arguments_on_the_host(binding):
+    """df_attn_fwd_host reads cu_seqlens on the host and rejects a bad call
+    before any CUDA call (fake device pointers are never touched)."""
+    b = binding
+    lib = b.raw_library
+    cu = np.array([0, 5, 12, 12], dtype=np.int32)
+    vp = lambda x: None if x is None else ctypes.c_void_p(x)  # noqa: E731
+    cu_p = cu.ctypes.data_as(ctypes.c_void_p)
+    size = b.df_attn_fwd_host_scratch_size(3, 2, 16, 64, b.DF_BF16)
+    assert size > b.df_attn_workspace_size(3, 2, 16, 64)
+    assert b.df_attn_fwd_host_scratch_size(3, 2, 16, 48, b.DF_BF16) == 0
+
+    def call(cu_ptr=cu_p, mask=None, T=12, L=16, scratch=0x100000, nbytes=size, group=0):
+        return lib.df_attn_fwd_host(vp(0x1000), vp(0x2000), vp(0x3000), vp(0x4000), vp(0x5000),
+                                    vp(mask), cu_ptr, 3, 2, L, T, 64, 256, 512, 256, 0, vp(0x6000),
+                                    group, vp(scratch), nbytes, None)
+
+    assert call(T=13) == b.DF_ERR_INVALID_ARG          # cu_seqlens[B] != total_tokens
+    assert call(L=6) == b.DF_ERR_INVALID_ARG           # a length above L
+    assert call(mask=0x7000) == b.DF_ERR_INVALID_ARG   # both mask and cu_seqlens
+    assert call(nbytes=size - 1) == b.DF_ERR_WORKSPACE
+    assert call(scratch=0x100010) == b.DF_ERR_ALIGNMENT
+    assert call(group=-1) == b.DF_ERR_INVALID_ARG
+    bad = np.array([0, 7, 5, 12], dtype=np.int32)       # decreasing
+    assert call(cu_ptr=bad.ctypes.data_as(ctypes.c_void_p)) == b.DF_ERR_INVALID_ARG
