@@ -44,7 +44,7 @@ def parse_args(argv=None):
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--group-tokens", type=int, default=0,
-                    help="host-buffer forward: tokens per group of sequences (0: B*L/8)")
+                    help="host-buffer forward: tokens per group of sequences (0: B*L/4)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--op", choices=["attention", "pack", "linear", "encoder", "bwd"], default="attention",
                     help="pack: the padded <-> packed conversion; linear: the QKV and PK/PQ projections; "

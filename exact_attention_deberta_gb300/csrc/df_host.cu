@@ -63,7 +63,7 @@ struct HostLayout {
 };
 
 long long group_capacity(int B, int L, long long group_tokens) {
-  const long long auto_cap = ((long long)B * L + 7) / 8;
+  const long long auto_cap = ((long long)B * L + 3) / 4;
   const long long want = group_tokens > 0 ? group_tokens : auto_cap;
   return std::max<long long>(want, L);
 }
@@ -141,22 +141,30 @@ extern "C" df_status df_attn_fwd_host(const void* q, const void* k, const void* 
     long long t0, t1;    // tokens [t0, t1)
     int cu_off;          // rebased cu_seqlens of the group inside the cu section
   };
+  // The first groups ramp up from L tokens (one full sequence), doubling, to
+  // the slot capacity: the pipeline starts computing after a short copy-in.
   std::vector<Group> groups;
   std::vector<int32_t> cu_all;
+  auto ramp = [&](size_t gi) {
+    return gi >= 40 ? lay.cap_tokens : std::min<long long>(lay.cap_tokens, (long long)L << gi);
+  };
   if (packed) {
     int s = 0;
     while (s < B) {
+      const long long cap = ramp(groups.size());
       Group g{s, s, cu_seqlens[s], cu_seqlens[s], (int)cu_all.size()};
-      while (g.s1 < B && (g.s1 == g.s0 || cu_seqlens[g.s1 + 1] - g.t0 <= lay.cap_tokens)) ++g.s1;
+      while (g.s1 < B && (g.s1 == g.s0 || cu_seqlens[g.s1 + 1] - g.t0 <= cap)) ++g.s1;
       g.t1 = cu_seqlens[g.s1];
       for (int e = g.s0; e <= g.s1; ++e) cu_all.push_back(cu_seqlens[e] - (int32_t)g.t0);
       groups.push_back(g);
       s = g.s1;
     }
   } else {
-    for (int r = 0; r < B; r += lay.cap_rows) {
-      const int r1 = std::min(B, r + lay.cap_rows);
+    for (int r = 0; r < B;) {
+      const int rows = (int)std::max<long long>(1, ramp(groups.size()) / L);
+      const int r1 = std::min(B, r + rows);
       groups.push_back(Group{r, r1, (long long)r * L, (long long)r1 * L, 0});
+      r = r1;
     }
   }
 

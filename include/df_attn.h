@@ -158,9 +158,10 @@ size_t df_attn_bwd_workspace_size(int B, int H, int L, int d, int buckets, int m
  * memory lets the copies run asynchronously; pageable memory works but
  * serialises them).  Sequences are independent (padded: batch rows), so the
  * batch is cut into groups of whole sequences of at most
- * max(group_tokens, L) tokens (group_tokens = 0: max(B*L/8, L)) and each group
- * runs as one df_attn_fwd call, with results identical to a single call on
- * the whole batch.  Two library-owned copy streams (created once per device)
+ * max(group_tokens, L) tokens (group_tokens = 0: max(B*L/4, L)), the first
+ * groups ramping up from L tokens by doubling, and each group runs as one
+ * df_attn_fwd call, with results identical to a single call on the whole
+ * batch.  Two library-owned copy streams (created once per device)
  * pipeline the copy-in of group g + 1 and the copy-out of group g - 1 around
  * the forward of group g on `stream`; `stream` waits for the last copy-out, so
  * `out` is complete once `stream` is.  In packed mode cu_seqlens is validated
