@@ -147,6 +147,34 @@ BwdLayout make_bwd_layout(int B, int H, int L, int d, int buckets, int max_rel, 
   return l;
 }
 
+// Head size 32 with 16-bit I/O runs the d = 64 tensor-core kernels on
+// zero-widened copies: the d = 64 layout first (its header at offset 0), then
+// q, k, v, out [T][H][64] and PK, PQ [2 span][H][64].
+struct Pad32Layout {
+  size_t fwd, q, k, v, o, pk, pq, total;
+};
+
+Pad32Layout make_pad32_layout(int B, int H, int L, int buckets, int max_rel, int span) {
+  Pad32Layout l{};
+  l.fwd = make_layout(B, H, L, 64, buckets, max_rel, span).total;
+  const size_t tok = align256((size_t)B * L * H * 64 * 2), pos = align256(2 * (size_t)span * H * 64 * 2);
+  l.q = l.fwd;
+  l.k = l.q + tok;
+  l.v = l.k + tok;
+  l.o = l.v + tok;
+  l.pk = l.o + tok;
+  l.pq = l.pk + pos;
+  l.total = l.pq + pos;
+  return l;
+}
+
+size_t workspace_bytes_for(int B, int H, int L, int d, int buckets, int max_rel, int span) {
+  const size_t own = make_layout(B, H, L, d, buckets, max_rel, span).total;
+  if (d != 32) return own;
+  const size_t wide = make_pad32_layout(B, H, L, buckets, max_rel, span).total;
+  return own > wide ? own : wide;
+}
+
 df_status check_params(int H, int L, int d, df_dtype dtype, int buckets, int max_rel, int span) {
   if (H < 1 || L < 1 || span < 1) return DF_ERR_INVALID_ARG;
   if (dtype != DF_BF16 && dtype != DF_FP16 && dtype != DF_FP32) return DF_ERR_INVALID_ARG;
@@ -235,7 +263,7 @@ df_status df_attn_supported(int H, int L, int d, df_dtype dtype, int buckets, in
 
 size_t df_attn_workspace_size(int B, int H, int L, int d, int buckets, int max_rel, int span) {
   if (B < 0 || check_params(H, L, d, DF_BF16, buckets, max_rel, span) != DF_OK) return 0;
-  return make_layout(B, H, L, d, buckets, max_rel, span).total;
+  return workspace_bytes_for(B, H, L, d, buckets, max_rel, span);
 }
 
 df_status df_attn_workspace_layout(int B, int H, int L, int d, int buckets, int max_rel, int span,
@@ -287,6 +315,30 @@ df_status df_attn_fwd(const void* q, const void* k, const void* v, const void* p
                                workspace_bytes, true, &p);
   if (st != DF_OK) return st;
   cudaStream_t s = (cudaStream_t)stream;
+  if (dtype != DF_FP32 && d == 32 && tc_enabled()) {
+    // d = 32 on the tensor cores: widen to 64 with zeros, run the d = 64
+    // kernels with the d = 32 scale, narrow the output
+    const Pad32Layout pl = make_pad32_layout(B, H, L, buckets, max_rel, span);
+    if (workspace_bytes < pl.total) return DF_ERR_WORKSPACE;
+    char* base = static_cast<char*>(workspace);
+    Problem w;
+    st = build_problem(base + pl.q, base + pl.k, base + pl.v, base + pl.pk, base + pl.pq, key_mask,
+                       cu_seqlens, B, H, L, total_tokens, 64, buckets, max_rel, span, dtype,
+                       base + pl.o, workspace, pl.fwd, true, &w);
+    if (st != DF_OK) return st;
+    w.kscale = p.kscale;  // the scale of the true head size
+    const void* src[5] = {q, k, v, pos_key, pos_query};
+    void* dst[5] = {base + pl.q, base + pl.k, base + pl.v, base + pl.pk, base + pl.pq};
+    const long long tok_rows = (long long)total_tokens * H, pos_rows = 2ll * span * H;
+    const long long rows[5] = {tok_rows, tok_rows, tok_rows, pos_rows, pos_rows};
+    if (launch_pad32(src, dst, rows, s) != cudaSuccess || launch_plan(w, s) != cudaSuccess)
+      return DF_ERR_CUDA;
+    int launches = 0;
+    if (launch_tc(w, s, g_prof_start, g_prof_mid, g_prof_stop, &launches) != cudaSuccess) return DF_ERR_CUDA;
+    if (launch_unpad32(base + pl.o, out, tok_rows, s) != cudaSuccess) return DF_ERR_CUDA;
+    g_last_launches.store(3 + launches);
+    return DF_OK;
+  }
   if (launch_plan(p, s) != cudaSuccess) return DF_ERR_CUDA;
   int launches = 0;
   cudaError_t e;

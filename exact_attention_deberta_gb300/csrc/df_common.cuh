@@ -133,6 +133,9 @@ cudaError_t launch_plan(const Problem& p, cudaStream_t s);
 cudaError_t launch_index_table(int buckets, int max_rel, int span, int max_len, int32_t* idx,
                                cudaStream_t s);
 cudaError_t launch_simt(const Problem& p, cudaStream_t s, int* launches);
+cudaError_t launch_pad32(const void* const src[5], void* const dst[5], const long long rows[5],
+                         cudaStream_t s);
+cudaError_t launch_unpad32(const void* src, void* dst, long long rows, cudaStream_t s);
 cudaError_t launch_bwd(const BwdProblem& b, cudaStream_t s, cudaEvent_t ev0, cudaEvent_t ev_mid,
                        cudaEvent_t ev1, int* launches);
 }  // namespace dfa

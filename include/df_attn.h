@@ -71,9 +71,9 @@ typedef enum { DF_BF16 = 0, DF_FP16 = 1, DF_FP32 = 2 } df_dtype;
  *   key_mask           uint8 [B, L] in padded mode, NULL in packed mode
  *   cu_seqlens         int32 [B + 1] in packed mode, NULL in padded mode
  *   B                  batch rows (padded) or number of sequences (packed), >= 0
- *   H, d               heads and head size; d in {32, 64, 128} (bf16 / fp16 with
- *                      d = 64 or 128 run on the tensor cores; d = 32 and every
- *                      fp32 call on the CUDA-core kernel)
+ *   H, d               heads and head size; d in {32, 64, 128} (bf16 / fp16 run on
+ *                      the tensor cores, d = 32 as d = 64 on zero-widened copies
+ *                      in the workspace; every fp32 call on the CUDA-core kernel)
  *   L                  padded length, or an upper bound of every packed length
  *                      (max_seqlen); 1 <= L <= 65536
  *   total_tokens       rows of q/k/v/out: B*L in padded mode, cu_seqlens[B] in

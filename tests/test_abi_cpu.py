@@ -234,3 +234,12 @@ def test_host_forward_checks_arguments_on_the_host(binding):
     assert call(group=-1) == b.DF_ERR_INVALID_ARG
     bad = np.array([0, 7, 5, 12], dtype=np.int32)       # decreasing
     assert call(cu_ptr=bad.ctypes.data_as(ctypes.c_void_p)) == b.DF_ERR_INVALID_ARG
+
+
+def test_head_size_32_workspace_holds_the_widened_copies(binding):
+    """bf16 / fp16 at d = 32 run the d = 64 kernels on zero-widened copies: the
+    workspace holds the d = 64 layout plus q, k, v, out and PK, PQ at 64 columns."""
+    B, H, L = 4, 24, 2048
+    d64 = binding.df_attn_workspace_layout(B, H, L, 64)["total"]
+    widened = 4 * B * L * H * 64 * 2 + 2 * 512 * H * 64 * 2
+    assert binding.df_attn_workspace_size(B, H, L, 32) >= d64 + widened

@@ -290,8 +290,9 @@ def test_deterministic(lib):
                                                   ("padded", "fp16", [512, 77, 0, 200]),
                                                   ("packed", "fp32", [333, 64, 1000])])
 def test_head_size_32(lib, layout, dtype, lengths):
-    """d = 32 (the CUDA-core kernel for every dtype): every row against the oracle,
-    with ragged, empty and single-token sequences and far tiles (L up to 1000)."""
+    """d = 32 (bf16 / fp16: the d = 64 tensor-core kernels on zero-widened heads;
+    fp32: the CUDA-core kernel): every row against the oracle, with ragged, empty
+    and single-token sequences and far tiles (L up to 1000)."""
     L = max(lengths)
     x = synth.custom_inputs(layout=layout, dtype=dtype, H=4, d=32, lengths=lengths, L=L, seed=len(lengths) + L)
     out = run_gpu(lib, x)
