@@ -46,10 +46,11 @@ def parse_args(argv=None):
     ap.add_argument("--group-tokens", type=int, default=0,
                     help="host-buffer forward: tokens per group of sequences (0: B*L/4)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--op", choices=["attention", "pack", "linear", "encoder", "bwd"], default="attention",
+    ap.add_argument("--op", choices=["attention", "pack", "linear", "encoder", "bwd", "small"], default="attention",
                     help="pack: the padded <-> packed conversion; linear: the QKV and PK/PQ projections; "
                          "encoder: a 12-layer DeBERTa-v3-base encoder on synthetic weights; "
-                         "bwd: the backward pass (dQ, dK, dV, dPK, dPQ) of the attention")
+                         "bwd: the backward pass (dQ, dK, dV, dPK, dPQ) of the attention; "
+                         "small: per-call latency of the small padded workloads (launch / HBM bound)")
     return ap.parse_args(argv)
 
 
@@ -397,6 +398,92 @@ def run_linear(args, local):
     print(json.dumps(line), flush=True)
 
 
+def run_small(args, local):
+    """The small workloads, where launch latency and HBM set the time: per call,
+    >= 200 back-to-back calls timed one by one with CUDA events (median and
+    mean), both as eager calls and as the replay of a CUDA graph that holds one
+    call; TFLOP/s on the metric's count and GB/s of algorithmic bytes (Q, K, V,
+    O of the valid tokens, PK and PQ, the mask) against the measured HBM rate.
+    The float64 oracle is timed on each workload in full."""
+    torch.cuda.set_device(local)
+    from exact_attention_deberta_gb300.build import build
+    build()
+    from exact_attention_deberta_gb300 import binding, synth
+    from oracle import attend_padded
+    peaks, src = load_peaks()
+    calls = max(200, args.steps)
+    stream = torch.cuda.current_stream()
+    res = {}
+    for name in ("tiny_fp32", "tiny_fp32_pad97", "v3base_padded_bf16", "v2xl_heavypad_fp16"):
+        x = synth.make_inputs(name)
+        H, d, span, L = x.w.H, x.w.d, x.w.span, x.w.L
+        kw = dict(buckets=x.w.buckets, max_rel=x.w.max_rel, span=span)
+        dev = {n: getattr(x, n).cuda() for n in ("q", "k", "v", "pk", "pq", "key_mask")}
+        out = torch.empty_like(dev["q"])
+        B = dev["q"].shape[0]
+        ws = torch.empty(binding.df_attn_workspace_size(B, H, L, d, **kw), dtype=torch.uint8, device="cuda")
+
+        def call():
+            binding.df_attn_fwd(dev["q"], dev["k"], dev["v"], dev["pk"], dev["pq"], key_mask=dev["key_mask"],
+                                out=out, workspace=ws, **kw)
+
+        for _ in range(max(3, args.warmup)):
+            call()
+        torch.cuda.synchronize()
+        launches = binding.df_attn_last_launch_count()
+
+        def timed(fn):
+            ev = [torch.cuda.Event(enable_timing=True) for _ in range(calls + 1)]
+            ev[0].record(stream)
+            for i in range(calls):
+                fn()
+                ev[i + 1].record(stream)
+            torch.cuda.synchronize()
+            t = [ev[i].elapsed_time(ev[i + 1]) * 1e3 for i in range(calls)]
+            return float(np.median(t)), float(np.mean(t))
+
+        eager = timed(call)
+        try:
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph):
+                call()
+            graph.replay()
+            torch.cuda.synchronize()
+            replay = timed(graph.replay)
+        except RuntimeError as e:  # a capture the runtime refuses: report the eager calls only
+            print(f"graph capture of {name} failed: {e}", file=sys.stderr)
+            replay = eager
+        assert binding.df_attn_get_device_status(ws) == binding.DF_OK
+        lengths = [int(n) for n in x.lengths]
+        flops = metric_flops(lengths, H, d)
+        es = out.element_size()
+        T = sum(lengths)
+        nbytes = 4 * T * H * d * es + 2 * 2 * span * H * d * es + B * L
+        t0 = time.perf_counter()
+        attend_padded(x.q, x.k, x.v, x.pk, x.pq, x.key_mask, **kw)
+        oracle_s = time.perf_counter() - t0
+        res[name] = {"tokens": T, "launches_per_call": launches, "flops": flops, "bytes": nbytes,
+                     "eager_us_median": eager[0], "eager_us_mean": eager[1],
+                     "graph_us_median": replay[0], "graph_us_mean": replay[1],
+                     "tflops_graph": flops / (replay[0] * 1e-6) / 1e12,
+                     "gbs_graph": nbytes / (replay[0] * 1e-6) / 1e9,
+                     "hbm_frac_graph": nbytes / (replay[0] * 1e-6) / 1e9 / peaks["hbm_gbs"],
+                     "oracle_s_full": oracle_s}
+    head = res["v3base_padded_bf16"]
+    line = {"metric": "small padded batch latency (us per call, CUDA-graph replay, median)",
+            "value": head["graph_us_median"], "unit": "us", "n_gpus": 1, "steps": calls, "warmup": max(3, args.warmup),
+            "ms_per_step": head["graph_us_median"] / 1e3, "higher_is_better": False, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": "v3base_padded_bf16", "B": 16, "L": 512, "H": 12, "d": 64,
+                       "l2": "inputs smaller than L2: back-to-back calls, as the workload's own use"},
+            "roofline": {"bound": "hbm", "achieved": head["gbs_graph"], "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": head["hbm_frac_graph"], "traffic": None, "peak_source": src + " hbm_gbs"},
+            "workloads": res, "gpu_launches": head["launches_per_call"] * calls * 2,
+            "cpu_baseline": {"value": head["oracle_s_full"] * 1e6, "unit": "us", "cores": torch.get_num_threads(),
+                             "kind": "oracle", "sample": "each workload in full, float64 numpy"}}
+    print(json.dumps(line), flush=True)
+
+
 def bwd_kernel_flops(lengths, H, d, span):
     """Algorithmic flops of the two backward tile kernels.  Query kernel: the
     forward recomputed (Q.K^T and P.V) and a second Q.K^T with dP = dO.V^T and
@@ -589,9 +676,10 @@ def main(argv=None):
     if args.impl == "reference":
         run_reference(args, rank, world)
         return
-    if args.op in ("pack", "linear", "encoder", "bwd"):
+    if args.op in ("pack", "linear", "encoder", "bwd", "small"):
         if rank == 0:
-            {"pack": run_pack, "linear": run_linear, "encoder": run_encoder, "bwd": run_bwd}[args.op](args, local)
+            {"pack": run_pack, "linear": run_linear, "encoder": run_encoder, "bwd": run_bwd,
+             "small": run_small}[args.op](args, local)
         return
     assert args.warmup >= 3, "at least 3 warm-up steps"
     torch.cuda.set_device(local)

@@ -76,6 +76,21 @@ void near_offsets(int L, int buckets, int max_rel, int span, int lt, int* m0, in
   *n = hi >= lo ? hi - lo + 1 : 0;
 }
 
+// Whether a far tile (every distance of a 128 x 128 tile saturated) can occur
+// for sequences of at most L tokens.  The largest offset is 128 (nkb - 1); a
+// margin of 2 in r covers a last-ulp difference between host and device logs,
+// so "no" here is "no" on the device too.
+bool far_tiles_possible(int L, int buckets, int max_rel, int span, int lt) {
+  const int top = 2 * span - 1;
+  int rsp = lt + kQBlock, rsn = -(lt + kQBlock);
+  for (int r = 0; r < lt; ++r)
+    if (host_rel_index(r, buckets, max_rel, span) == top) { rsp = r; break; }
+  for (int r = 0; r > -lt; --r)
+    if (host_rel_index(r, buckets, max_rel, span) == 0) { rsn = r; break; }
+  const int reach = 128 * ((L + kKBlock - 1) / kKBlock - 1) - 127;
+  return reach >= rsp - 2 || -reach <= rsn + 2;
+}
+
 Layout make_layout(int B, int H, int L, int d, int buckets, int max_rel, int span) {
   Layout l{};
   l.lt = ((L + 127) / 128) * 128 + 128;
@@ -236,6 +251,7 @@ df_status build_problem(const void* q, const void* k, const void* v, const void*
   const unsigned long long wb = g_wait_budget.load();
   P.wait_budget = wb ? wb : kDefaultWaitBudget;
   P.zero_out = 1;
+  P.far_possible = far_tiles_possible(L, buckets, max_rel, span, lay.lt) ? 1 : 0;
   return DF_OK;
 }
 

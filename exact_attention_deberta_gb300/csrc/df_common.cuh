@@ -62,6 +62,7 @@ struct Problem {
   int diag_m0;
   unsigned long long wait_budget;
   int zero_out;               // the planner zeroes the output rows of masked tokens
+  int far_possible;           // 0: no tile of any sequence (length <= L) is a far tile
 };
 
 // Views of the backward pass (gradients in fp32).

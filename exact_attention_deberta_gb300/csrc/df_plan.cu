@@ -123,45 +123,72 @@ __device__ void write_kaug_selectors(const Problem& p) {
   }
 }
 
+constexpr int kSmemSeqs = 512;  // batches up to this size rank in shared memory
+
 __device__ void build_worklist(const Problem& p) {
+  __shared__ int4 s_seq[kSmemSeqs];  // {start, n, nblk, first item}
   const int B = p.B, L = p.L;
+  const bool in_smem = B <= kSmemSeqs;
   // The status word reports the latest call: this block is the only one of the
   // planning kernel that can raise, so it clears the word before anything else.
   if (threadIdx.x == 0) { p.hdr->status = 0; p.hdr->status_where = 0; }
   __syncthreads();
-  for (int s = threadIdx.x; s < B; s += blockDim.x) {
-    int start, n;
-    if (p.packed) {
-      start = p.cu_seqlens[s];
-      n = p.cu_seqlens[s + 1] - start;
+  if (p.packed) {
+    for (int s = threadIdx.x; s < B; s += blockDim.x) {
+      const int start = p.cu_seqlens[s];
+      int n = p.cu_seqlens[s + 1] - start;
       if (n < 0 || n > L || start < 0 || start + (n > 0 ? n : 0) > p.T) {
         raise_device_error(p.hdr, DF_ERR_INVALID_ARG, 100);
         n = 0;
       }
-    } else {
-      start = s * L;
-      const uint8_t* row = p.key_mask + (size_t)s * L;
-      n = 0;
-      for (int j = L - 1; j >= 0; --j)
-        if (row[j]) { n = j + 1; break; }
+      p.seqs[s] = make_int4(start, n, (n + kQBlock - 1) / kQBlock, 0);
+      if (in_smem) s_seq[s] = p.seqs[s];
     }
-    p.seqs[s] = make_int4(start, n, (n + kQBlock - 1) / kQBlock, 0);
+  } else {
+    // padded: n = last valid position + 1; one warp per batch row, each lane
+    // takes every 32nd position and the warp keeps the largest valid one
+    const int lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+    for (int s = threadIdx.x >> 5; s < B; s += nw) {
+      const uint8_t* row = p.key_mask + (size_t)s * L;
+      int last = -1;
+      for (int j = lane; j < L; j += 32)
+        if (row[j]) last = j;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) last = max(last, __shfl_xor_sync(0xffffffffu, last, o));
+      const int n = last + 1;
+      if (lane == 0) {
+        p.seqs[s] = make_int4(s * L, n, (n + kQBlock - 1) / kQBlock, 0);
+        if (in_smem) s_seq[s] = p.seqs[s];
+      }
+    }
   }
   __syncthreads();
   for (int s = threadIdx.x; s < B; s += blockDim.x) {
-    const int4 me = p.seqs[s];
+    const int4 me = in_smem ? s_seq[s] : p.seqs[s];
     int rank = 0, base = 0;
     for (int o = 0; o < B; ++o) {
-      const int nb = p.seqs[o].z;
+      const int nb = in_smem ? s_seq[o].z : p.seqs[o].z;
       const bool before = nb > me.z || (nb == me.z && o < s);
       rank += before;
       base += before ? nb * p.H : 0;
     }
-    for (int h = 0; h < p.H; ++h)
-      for (int b = 0; b < me.z; ++b)
-        p.items[base + h * me.z + b] = make_int4(me.x, me.y, h, b);
+    if (!in_smem)
+      for (int h = 0; h < p.H; ++h)
+        for (int b = 0; b < me.z; ++b)
+          p.items[base + h * me.z + b] = make_int4(me.x, me.y, h, b);
     if (rank == B - 1) p.hdr->n_items = base + me.z * p.H;
     p.seqs[s].w = rank;
+    if (in_smem) s_seq[s].w = base;  // read back only after the barrier below
+  }
+  if (in_smem) {
+    // the whole block writes every sequence's items
+    __syncthreads();
+    for (int s = 0; s < B; ++s) {
+      const int4 me = s_seq[s];
+      const int count = me.z * p.H;
+      for (int e = threadIdx.x; e < count; e += blockDim.x)
+        p.items[me.w + e] = make_int4(me.x, me.y, e / me.z, e % me.z);
+    }
   }
   if (threadIdx.x == 0) {
     if (B == 0) p.hdr->n_items = 0;

@@ -512,9 +512,10 @@ cudaError_t launch_tc(const Problem& p, cudaStream_t s, cudaEvent_t ev0, cudaEve
   else
     e = bf16 ? launch_near_typed<128, true>(p, maps, s) : launch_near_typed<128, false>(p, maps, s);
   if (ev_mid) cudaEventRecord(ev_mid, s);
-  if (e == cudaSuccess) e = launch_far(p, maps, s);
+  // with no far tile possible the near-tile kernel writes every output row
+  if (e == cudaSuccess && p.far_possible) e = launch_far(p, maps, s);
   if (ev1) cudaEventRecord(ev1, s);
-  *launches = 2;
+  *launches = p.far_possible ? 2 : 1;
   return e;
 }
 
