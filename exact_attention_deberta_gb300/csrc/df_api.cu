@@ -133,7 +133,6 @@ struct BwdLayout {
   int splits;
 };
 
-constexpr int kBwdMaxR = 512;  // bucket-sum rows of a block live in shared memory
 
 int bwd_splits(long long T, int H) {
   long long s = (T + 1023) / 1024;
@@ -373,7 +372,6 @@ df_status df_attn_fwd(const void* q, const void* k, const void* v, const void* p
 
 size_t df_attn_bwd_workspace_size(int B, int H, int L, int d, int buckets, int max_rel, int span) {
   if (B < 0 || check_params(H, L, d, DF_BF16, buckets, max_rel, span) != DF_OK) return 0;
-  if (2 * span > kBwdMaxR) return 0;
   return make_bwd_layout(B, H, L, d, buckets, max_rel, span).total;
 }
 
@@ -389,7 +387,6 @@ df_status df_attn_bwd(const void* q, const void* k, const void* v, const void* p
                                total_tokens, d, buckets, max_rel, span, dtype, dq, workspace,
                                workspace_bytes, true, &b.f);
   if (st != DF_OK) return st;
-  if (2 * span > kBwdMaxR) return DF_ERR_UNSUPPORTED;
   const int T = total_tokens;
   if (!dpos_key || !dpos_query || (T > 0 && (!dout || !dk || !dv))) return DF_ERR_INVALID_ARG;
   if (!aligned16(dpos_key) || !aligned16(dpos_query) ||

@@ -123,8 +123,7 @@ size_t df_attn_workspace_size(int B, int H, int L, int d, int buckets, int max_r
  *
  *   q, k, v, pos_key, pos_query, key_mask, cu_seqlens, B, H, L, total_tokens,
  *   d, buckets, max_rel, span, dtype: as for df_attn_fwd (every dtype and
- *                      d in {32, 64, 128}); 2 * span <= 512, else
- *                      DF_ERR_UNSUPPORTED
+ *                      d in {32, 64, 128})
  *   dout               gradient of the output, layout and dtype of q
  *   dq, dk, dv         float32, layout of q: written in full (overwritten)
  *   dpos_key, dpos_query  float32 [2 span, H, d]: written in full, summed over
@@ -148,8 +147,8 @@ df_status df_attn_bwd(const void* q, const void* k, const void* v,
                       void* workspace, size_t workspace_bytes, df_stream_t stream);
 
 /* Bytes of workspace df_attn_bwd needs for these sizes (T bounded by B*L);
- * about 8 * B*L*H*span bytes for the bucket sums.  0 for arguments that
- * df_attn_bwd rejects. */
+ * about 16 * B*L*H*span bytes for the two bucket-sum tables.  0 for arguments
+ * that df_attn_bwd rejects. */
 size_t df_attn_bwd_workspace_size(int B, int H, int L, int d, int buckets, int max_rel, int span);
 
 /*

@@ -196,9 +196,9 @@ def test_backward_checks_arguments_on_the_host(binding):
     bwd = b.df_attn_bwd_workspace_size(2, 2, 64, 64)
     # the bucket sums alone take 2 tables x T x H x 2 span floats
     assert bwd >= fwd + 2 * 128 * 2 * 512 * 4
-    assert b.df_attn_bwd_workspace_size(2, 2, 64, 64, buckets=0, max_rel=512) == 0  # 2 span > 512
+    # no bucketing: span = max_rel = 512, twice the bucket-sum tables
+    assert b.df_attn_bwd_workspace_size(2, 2, 64, 64, buckets=0, max_rel=512) >= fwd + 2 * 128 * 2 * 1024 * 4
     assert b.df_attn_bwd_workspace_size(2, 2, 64, 48) == 0
-    assert _bwd_raw(b, buckets=0, span=512) == b.DF_ERR_UNSUPPORTED
     assert _bwd_raw(b, d=96) == b.DF_ERR_UNSUPPORTED
     assert _bwd_raw(b, ws_bytes=bwd - 1) == b.DF_ERR_WORKSPACE
     assert _bwd_raw(b, dpk=None) == b.DF_ERR_INVALID_ARG

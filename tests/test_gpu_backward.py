@@ -90,12 +90,15 @@ def test_backward_matches_oracle(lib, name):
             assert np.all(g[dead] == 0.0), f"{nm}: masked tokens must get exact zeros"
 
 
-def test_backward_unsupported_span(lib):
-    x = synth.custom_inputs(layout="packed", dtype="bf16", H=1, d=64, lengths=[16], buckets=0,
-                            max_rel=512)   # span 512: 2 span > 512
-    with pytest.raises(lib.DFError) as e:
-        _run(lib, x, synth.grad_output(x))
-    assert e.value.status == lib.DF_ERR_UNSUPPORTED
+def test_backward_without_buckets_span_512(lib):
+    """DeBERTa without position buckets: span = max_rel = 512 (1024 PK / PQ rows)."""
+    x = synth.custom_inputs(layout="packed", dtype="bf16", H=2, d=64, lengths=[700, 90], buckets=0,
+                            max_rel=512, seed=8)
+    dout = synth.grad_output(x)
+    got = _run(lib, x, dout)
+    ref = _oracle(x, dout)
+    for nm, g, r in zip(("dq", "dk", "dv", "dpk", "dpq"), got, ref):
+        _close(f"nobuckets512/{nm}", g, r)
 
 
 def _identities(x, dout, got, tol=TOL):
