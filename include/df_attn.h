@@ -1,6 +1,8 @@
 /*
- * df_attn.h -- C ABI of the exact DeBERTa-v2/v3 disentangled-attention forward
- * pass for NVIDIA GB300 (sm_103a).
+ * df_attn.h -- C ABI of the exact DeBERTa-v2/v3 disentangled attention for
+ * NVIDIA GB300 (sm_103a): the fused forward pass, its backward pass, the
+ * forward from host buffers, and the steps on either side of the attention
+ * (padded <-> packed conversion, projections, LayerNorm).
  *
  * The operation (DisentangledFlash 0.2.0 README, section "Status":
  * "DeBERTa-v2/v3-style C2P/P2C disentangled attention", "factorized 2-D padding
