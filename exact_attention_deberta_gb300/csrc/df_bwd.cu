@@ -26,10 +26,11 @@
 //   GEMMs         dQ += G_c2p.PK, dK += G_p2c.PQ, and dPK = G_c2p^T.Q,
 //                 dPQ = G_p2c^T.K reduced over fixed token ranges (partial
 //                 sums, then one summing kernel; no global atomics).
-// Score tiles are 64 x 64 with 4 x 4 register micro-tiles (rows ty + 16 a,
-// columns tx + 16 b) as in the strict-fp32 forward; the position terms of a
-// near tile come from the PK / PQ rows of the tile's index band, and a far
-// tile (every distance saturated) uses the per-token scalars of the planner.
+// Score tiles are 64 x 64 with 4 x 4 register micro-tiles (rows 4 ty + a,
+// columns 4 tx + b, read as 16-byte vectors from swizzled shared buffers); the
+// position terms of a near tile come from the PK / PQ rows of the tile's index
+// band, and a far tile (every distance saturated) uses the per-token scalars of
+// the planner.
 #include "df_common.cuh"
 
 #include <math.h>
@@ -44,32 +45,49 @@ constexpr int BM = 64;   // query rows per tile
 constexpr int BN = 64;   // keys per tile
 constexpr int DC = 32;   // head-dim chunk staged at once
 constexpr int WB = 128;  // index-band capacity (BM + BN - 1 rows)
+constexpr int CS = 68;   // row stride of the chunk and tile buffers (16-byte rows of 4)
 constexpr int kThreads = 256;
 static_assert(BM == BN, "query and key chunks are staged by one loop");
 
-// Shared-memory map of the two tile kernels, in floats.
+// Shared-memory map of the two tile kernels, in floats.  Thread (tx, ty) owns
+// rows 4 ty + a and columns 4 tx + b of a tile, so its four operands of one
+// step are one 16-byte load.
 struct BwdSmem {
-  static constexpr int q = 0;                      // [DC][BM + 1] query chunk
-  static constexpr int k = q + DC * (BM + 1);      // [DC][BN + 1] key chunk
-  static constexpr int g = k + DC * (BN + 1);      // [DC][BM + 1] dO chunk
-  static constexpr int v = g + DC * (BM + 1);      // [DC][BN + 1] V chunk
-  static constexpr int pk = v + DC * (BN + 1);     // [DC][WB + 1] PK band; later tile A [BM][BN]
-  static constexpr int pq = pk + DC * (WB + 1);    // [DC][WB + 1] PQ band; later tile B [BM][BN]
-  static constexpr int rowA = pq + DC * (WB + 1);  // [2][BM] query scalars (neg, pos side)
+  static constexpr int q = 0;                      // [DC][CS] query chunk (swizzled rows)
+  static constexpr int k = q + DC * CS;            // [DC][CS] key chunk
+  static constexpr int g = k + DC * CS;            // [DC][CS] dO chunk
+  static constexpr int v = g + DC * CS;            // [DC][CS] V chunk
+  static constexpr int pk = v + DC * CS;           // [DC][WB + 1] PK band
+  static constexpr int pq = pk + DC * (WB + 1);    // [DC][WB + 1] PQ band
+  static constexpr int ta = pq + DC * (WB + 1);    // [BM][CS] dS tile (query side) / P tile (key side)
+  static constexpr int tb = ta + BM * CS;          // [BM][CS] dS tile (key side)
+  static constexpr int rowA = tb + BM * CS;        // [2][BM] query scalars (neg, pos side)
   static constexpr int colB = rowA + 2 * BM;       // [3][BN] key scalars (neg, pos), key bias
   static constexpr int floats = colB + 3 * BN;
-  static_assert(BM * BN <= DC * (WB + 1), "tiles A and B reuse the band buffers");
-  // pass 1 of the query kernel keeps V [BN][D] and P [BM][BN + 1] in the dO,
-  // V and band buffers, which it does not otherwise use after the scores
+  // pass 1 of the query kernel keeps V^T [D][CS] (swizzled like a chunk) in
+  // the dO, V and band buffers, which it does not use after the scores, and P
+  // [BM][CS] in tile A
   static constexpr int pass1 = g;
-  static constexpr int pass1_floats = pk + 2 * DC * (WB + 1) - g;
-  static_assert(BN * 128 + BM * (BN + 1) <= pass1_floats, "pass-1 V and P fit at d = 128");
+  static_assert(g + 128 * CS <= ta, "pass-1 V^T fits at d = 128");
+  static_assert(q % 4 == 0 && k % 4 == 0 && g % 4 == 0 && v % 4 == 0 && ta % 4 == 0 && tb % 4 == 0,
+                "16-byte aligned buffers");
 };
+
+// Row swizzle of the chunk buffers: row r of column c sits at r ^ swz(c).  The
+// mask is a multiple of 4 below 32, so each group of four rows stays together
+// and in order (16-byte reads), and the transposed 16-byte staging stores of a
+// warp land in 32 different banks.
+template <typename T>
+__device__ __forceinline__ int swz(int c) {
+  return (16 / (int)sizeof(T)) * ((c >> 3) & 3);
+}
+
+__device__ __forceinline__ float4 lds4(const float* p) { return *reinterpret_cast<const float4*>(p); }
 
 struct TileGeom {
   bool far_pos, far_neg, far;
   int lo, w;
-  int col[7];  // band row of diagonal ty - tx + 16 (dd - 3), relative to lo
+  int col[7];  // band row of diagonal 4 (ty - tx) + dd - 3, relative to lo
 };
 
 __device__ __forceinline__ void tile_geom(const Problem& p, int rsp, int rsn, int i0, int j0, int ty,
@@ -86,20 +104,20 @@ __device__ __forceinline__ void tile_geom(const Problem& p, int rsp, int rsn, in
     g.lo = p.idx[rlo + p.lt - 1];
     g.w = p.idx[rhi + p.lt - 1] - g.lo + 1;
 #pragma unroll
-    for (int dd = 0; dd < 7; ++dd) g.col[dd] = p.idx[i0 - j0 + ty - tx + 16 * (dd - 3) + p.lt - 1] - g.lo;
+    for (int dd = 0; dd < 7; ++dd) g.col[dd] = p.idx[i0 - j0 + 4 * (ty - tx) + dd - 3 + p.lt - 1] - g.lo;
   }
 }
 
-// dst[c * STRIDE + r] = fp32 of row r, column c (c < DC) of a [rows][ts]
+// dst[c * STRIDE + r'] = fp32 of row r, column c (c < DC) of a [rows][ts]
 // array starting at `base`, for r < rows; rows at or past `lim` read as 0.
-// Each thread moves 16-byte vectors; within a warp the transposed stores hit
-// 32 different banks (STRIDE = 1 modulo 32).
-template <typename T, int STRIDE>
+// SWZ: r' = r ^ swz(c) (chunk buffers), else r' = r (band buffers, odd
+// stride).  Each thread moves 16-byte vectors.
+template <typename T, int STRIDE, bool SWZ>
 __device__ __forceinline__ void stage_t(const T* __restrict__ base, size_t ts, int rows, int lim,
                                         float* dst) {
   constexpr int V = 16 / sizeof(T);  // elements per vector
   constexpr int VPR = DC / V;        // vectors per row
-  static_assert(STRIDE % 32 == 1, "conflict-free transposed stores");
+  static_assert(SWZ || STRIDE % 32 == 1, "conflict-free transposed stores");
   for (int e = threadIdx.x; e < rows * VPR; e += kThreads) {
     const int r = e / VPR, v = e % VPR;
     float f[V];
@@ -113,7 +131,10 @@ __device__ __forceinline__ void stage_t(const T* __restrict__ base, size_t ts, i
       for (int k = 0; k < V; ++k) f[k] = 0.f;
     }
 #pragma unroll
-    for (int k = 0; k < V; ++k) dst[(v * V + k) * STRIDE + r] = f[k];
+    for (int k = 0; k < V; ++k) {
+      const int c = v * V + k;
+      dst[c * STRIDE + (SWZ ? (r ^ swz<T>(c)) : r)] = f[k];
+    }
   }
 }
 
@@ -162,25 +183,25 @@ __device__ __forceinline__ void score_tile(const Problem& p, const T* __restrict
     if (kc) __syncthreads();
     const size_t qrow = (size_t)(start + i0) * ts + (size_t)h * D + kc;
     const size_t krow = (size_t)(start + j0) * ts + (size_t)h * D + kc;
-    stage_t<T, BM + 1>(gq + qrow, ts, BM, n - i0, Qs);
-    stage_t<T, BN + 1>(gk + krow, ts, BN, n - j0, Ks);
+    stage_t<T, CS, true>(gq + qrow, ts, BM, n - i0, Qs);
+    stage_t<T, CS, true>(gk + krow, ts, BN, n - j0, Ks);
     if (DP) {
-      stage_t<T, BM + 1>(gdo + qrow, ts, BM, n - i0, Gs);
-      stage_t<T, BN + 1>(gv + krow, ts, BN, n - j0, Vc);
+      stage_t<T, CS, true>(gdo + qrow, ts, BM, n - i0, Gs);
+      stage_t<T, CS, true>(gv + krow, ts, BN, n - j0, Vc);
     }
     if (!g.far) {
       const size_t prow = (size_t)g.lo * ts + (size_t)h * D + kc;
-      stage_t<T, WB + 1>(gpk + prow, ts, g.w, g.w, PKs);
-      stage_t<T, WB + 1>(gpq + prow, ts, g.w, g.w, PQs);
+      stage_t<T, WB + 1, false>(gpk + prow, ts, g.w, g.w, PKs);
+      stage_t<T, WB + 1, false>(gpq + prow, ts, g.w, g.w, PQs);
     }
     __syncthreads();
 #pragma unroll 2
     for (int c = 0; c < DC; ++c) {
-      float qa[4], kb[4];
-#pragma unroll
-      for (int a = 0; a < 4; ++a) qa[a] = Qs[c * (BM + 1) + ty + 16 * a];
-#pragma unroll
-      for (int b = 0; b < 4; ++b) kb[b] = Ks[c * (BN + 1) + tx + 16 * b];
+      const int m = swz<T>(c);
+      const float4 q4 = lds4(Qs + c * CS + ((4 * ty) ^ m));
+      const float4 k4 = lds4(Ks + c * CS + ((4 * tx) ^ m));
+      const float qa[4] = {q4.x, q4.y, q4.z, q4.w};
+      const float kb[4] = {k4.x, k4.y, k4.z, k4.w};
 #pragma unroll
       for (int a = 0; a < 4; ++a)
 #pragma unroll
@@ -201,11 +222,10 @@ __device__ __forceinline__ void score_tile(const Problem& p, const T* __restrict
           }
       }
       if (DP) {
-        float ga[4], vb[4];
-#pragma unroll
-        for (int a = 0; a < 4; ++a) ga[a] = Gs[c * (BM + 1) + ty + 16 * a];
-#pragma unroll
-        for (int b = 0; b < 4; ++b) vb[b] = Vc[c * (BN + 1) + tx + 16 * b];
+        const float4 g4 = lds4(Gs + c * CS + ((4 * ty) ^ m));
+        const float4 v4 = lds4(Vc + c * CS + ((4 * tx) ^ m));
+        const float ga[4] = {g4.x, g4.y, g4.z, g4.w};
+        const float vb[4] = {v4.x, v4.y, v4.z, v4.w};
 #pragma unroll
         for (int a = 0; a < 4; ++a)
 #pragma unroll
@@ -226,10 +246,10 @@ __device__ __forceinline__ void tile_logits(const float* sm, const TileGeom& g, 
   for (int a = 0; a < 4; ++a)
 #pragma unroll
     for (int b = 0; b < 4; ++b) {
-      const int jj = tx + 16 * b;
+      const int jj = 4 * tx + b;
       float v;
       if (g.far) {
-        const float al = g.far_pos ? rowA[BM + ty + 16 * a] : rowA[ty + 16 * a];
+        const float al = g.far_pos ? rowA[BM + 4 * ty + a] : rowA[4 * ty + a];
         const float be = g.far_pos ? colB[BN + jj] : colB[jj];
         v = fmaf(s[a][b], ks, al + be);
       } else {
@@ -240,11 +260,11 @@ __device__ __forceinline__ void tile_logits(const float* sm, const TileGeom& g, 
 }
 
 // Adds the tile's dS to the bucket sums.  G points at the table row of the
-// block's first query row (BY_ROW) or key, rows H * R floats apart; `lim` is
-// the number of rows inside the sequence.  Near tiles add each nonzero entry
-// to the global table; a far tile has one relative index (bucket 0 or
-// 2 span - 1), so its entries go to the per-thread sums `far` ([row or
-// column u][side]), flushed by the caller.
+// block's first query row (BY_ROW) or key, rows `row_stride` floats apart;
+// `lim` is the number of rows inside the sequence.  Near tiles add each
+// nonzero entry to the global table; a far tile has one relative index
+// (bucket 0 or 2 span - 1), so its entries go to the per-thread sums `far`
+// ([row or column u][side]), flushed by the caller.
 template <bool BY_ROW>
 __device__ __forceinline__ void bucket_sums(float* G, size_t row_stride, int lim, const TileGeom& g,
                                             const float (&ds)[4][4], float (&far)[4][2]) {
@@ -265,7 +285,7 @@ __device__ __forceinline__ void bucket_sums(float* G, size_t row_stride, int lim
     for (int a = 0; a < 4; ++a)
 #pragma unroll
       for (int b = 0; b < 4; ++b) {
-        const int row = BY_ROW ? ty + 16 * a : tx + 16 * b;
+        const int row = BY_ROW ? 4 * ty + a : 4 * tx + b;
         if (row < lim && ds[a][b] != 0.f)
           atomicAdd(G + (size_t)row * row_stride + g.lo + g.col[a - b + 3], ds[a][b]);
       }
@@ -275,9 +295,10 @@ __device__ __forceinline__ void bucket_sums(float* G, size_t row_stride, int lim
 // ---------------------------------------------------------------- query side
 template <typename T, int D>
 __global__ void __launch_bounds__(kThreads, D <= 64 ? 2 : 1) bwd_q_kernel(const BwdProblem b) {
-  extern __shared__ float sm[];
+  extern __shared__ float4 sm4[];
+  float* sm = reinterpret_cast<float*>(sm4);
   const Problem& p = b.f;
-  constexpr int NC = D / 16;  // output columns per thread
+  constexpr int NC = D / 16;  // output columns per thread: tx + 16 c
   const T* __restrict__ gk = static_cast<const T*>(p.k);
   const T* __restrict__ gv = static_cast<const T*>(p.v);
   const T* __restrict__ gdo = static_cast<const T*>(b.dout);
@@ -287,9 +308,8 @@ __global__ void __launch_bounds__(kThreads, D <= 64 ? 2 : 1) bwd_q_kernel(const 
   const int n_items = p.hdr->n_items;
   const int rsp = p.hdr->r_sat_pos, rsn = p.hdr->r_sat_neg;
   const float ks = p.kscale;
-  float* Vs = sm + BwdSmem::pass1;  // pass 1: [BN][D]
-  float* Ps = Vs + BN * D;          // pass 1: [BM][BN + 1]
-  float* tA = sm + BwdSmem::pk;     // pass 2: dS tile [BM][BN]
+  float* Vt = sm + BwdSmem::pass1;  // pass 1: V^T [D][CS]
+  float* tA = sm + BwdSmem::ta;     // pass 1: P tile, pass 2: dS tile [BM][CS]
   float* Ks = sm + BwdSmem::k;
 
   for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
@@ -316,7 +336,7 @@ __global__ void __launch_bounds__(kThreads, D <= 64 ? 2 : 1) bwd_q_kernel(const 
         float s[4][4], dp[4][4], x[4][4];
         score_tile<T, D, false>(p, gdo, scal_h, start, n, h, i0, j0, g, sm, s, dp);
         tile_logits(sm, g, n, j0, ks, s, x);
-        __syncthreads();  // V and P overwrite the band buffers
+        __syncthreads();  // V^T overwrites the band buffers
 #pragma unroll
         for (int a = 0; a < 4; ++a) {
           float mt = fmaxf(fmaxf(x[a][0], x[a][1]), fmaxf(x[a][2], x[a][3]));
@@ -329,45 +349,37 @@ __global__ void __launch_bounds__(kThreads, D <= 64 ? 2 : 1) bwd_q_kernel(const 
           l[a] *= corr;
 #pragma unroll
           for (int c = 0; c < NC; ++c) o[a][c] *= corr;
+          float pv[4];
 #pragma unroll
           for (int bb = 0; bb < 4; ++bb) {
-            const float pv = exp2f(x[a][bb] - base);
-            l[a] += pv;
-            Ps[(ty + 16 * a) * (BN + 1) + tx + 16 * bb] = pv;
+            pv[bb] = exp2f(x[a][bb] - base);
+            l[a] += pv[bb];
           }
+          *reinterpret_cast<float4*>(tA + (4 * ty + a) * CS + 4 * tx) = make_float4(pv[0], pv[1], pv[2], pv[3]);
         }
-        {
-          constexpr int V = 16 / sizeof(T), VPR = D / V;
-          for (int e = tid; e < BN * VPR; e += kThreads) {
-            const int j = e / VPR, v = e % VPR;
-            float4 f[V / 4];
-            if (j0 + j < n) {
-              const uint4 raw = *reinterpret_cast<const uint4*>(gv + (size_t)(start + j0 + j) * ts +
-                                                                (size_t)h * D + v * V);
-              const T* el = reinterpret_cast<const T*>(&raw);
+        // V^T of the key tile, column chunk by column chunk (the swizzle of a
+        // column depends only on its position inside its chunk)
 #pragma unroll
-              for (int k = 0; k < V / 4; ++k)
-                f[k] = make_float4(IO<T>::to_f(el[4 * k]), IO<T>::to_f(el[4 * k + 1]),
-                                   IO<T>::to_f(el[4 * k + 2]), IO<T>::to_f(el[4 * k + 3]));
-            } else {
-#pragma unroll
-              for (int k = 0; k < V / 4; ++k) f[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-            }
-#pragma unroll
-            for (int k = 0; k < V / 4; ++k) reinterpret_cast<float4*>(Vs + j * D + v * V)[k] = f[k];
-          }
-        }
+        for (int kc = 0; kc < D; kc += DC)
+          stage_t<T, CS, true>(gv + (size_t)(start + j0) * ts + (size_t)h * D + kc, ts, BN, n - j0,
+                               Vt + kc * CS);
         __syncthreads();
-#pragma unroll 4
-        for (int j = 0; j < BN; ++j) {
-          float pa[4];
+#pragma unroll 2
+        for (int j = 0; j < BN; j += 4) {
+          float4 p4[4];
 #pragma unroll
-          for (int a = 0; a < 4; ++a) pa[a] = Ps[(ty + 16 * a) * (BN + 1) + j];
+          for (int a = 0; a < 4; ++a) p4[a] = lds4(tA + (4 * ty + a) * CS + j);
 #pragma unroll
           for (int c = 0; c < NC; ++c) {
-            const float vv = Vs[j * D + tx + 16 * c];
+            const int col = tx + 16 * c;
+            const float4 v4 = lds4(Vt + col * CS + (j ^ swz<T>(col)));
 #pragma unroll
-            for (int a = 0; a < 4; ++a) o[a][c] = fmaf(pa[a], vv, o[a][c]);
+            for (int a = 0; a < 4; ++a) {
+              o[a][c] = fmaf(p4[a].x, v4.x, o[a][c]);
+              o[a][c] = fmaf(p4[a].y, v4.y, o[a][c]);
+              o[a][c] = fmaf(p4[a].z, v4.z, o[a][c]);
+              o[a][c] = fmaf(p4[a].w, v4.w, o[a][c]);
+            }
           }
         }
       }
@@ -379,7 +391,7 @@ __global__ void __launch_bounds__(kThreads, D <= 64 ? 2 : 1) bwd_q_kernel(const 
         float lt = l[a];
 #pragma unroll
         for (int off = 8; off > 0; off >>= 1) lt += __shfl_xor_sync(0xffffffffu, lt, off);
-        const int i = i0 + ty + 16 * a;
+        const int i = i0 + 4 * ty + a;
         const size_t t = (size_t)start + i;
         const bool in = i < n;
         const bool live = in && p.keybias[t] == 0.f;
@@ -418,32 +430,38 @@ __global__ void __launch_bounds__(kThreads, D <= 64 ? 2 : 1) bwd_q_kernel(const 
 #pragma unroll
           for (int bb = 0; bb < 4; ++bb)
             ds[a][bb] = b.sscale * exp2f(x[a][bb] - rL[a]) * (dp[a][bb] - rD[a]);
-        __syncthreads();  // the band buffers become the dS tile
+        // the dS tile (its previous readers passed the barriers of score_tile)
 #pragma unroll
         for (int a = 0; a < 4; ++a)
-#pragma unroll
-          for (int bb = 0; bb < 4; ++bb) tA[(ty + 16 * a) * BN + tx + 16 * bb] = ds[a][bb];
+          *reinterpret_cast<float4*>(tA + (4 * ty + a) * CS + 4 * tx) =
+              make_float4(ds[a][0], ds[a][1], ds[a][2], ds[a][3]);
         bucket_sums<true>(G, (size_t)H * R, n - i0, g, ds, far);
 #pragma unroll
         for (int kc = 0; kc < D; kc += DC) {
           __syncthreads();
-          stage_t<T, BN + 1>(gk + (size_t)(start + j0) * ts + (size_t)h * D + kc, ts, BN, n - j0, Ks);
+          stage_t<T, CS, true>(gk + (size_t)(start + j0) * ts + (size_t)h * D + kc, ts, BN, n - j0, Ks);
           __syncthreads();
-#pragma unroll 4
-          for (int j = 0; j < BN; ++j) {
-            const float k0 = Ks[tx * (BN + 1) + j], k1 = Ks[(tx + 16) * (BN + 1) + j];
+          const int m0 = swz<T>(tx), m1 = swz<T>(tx + 16);
+#pragma unroll 2
+          for (int j = 0; j < BN; j += 4) {
+            const float4 k0 = lds4(Ks + tx * CS + (j ^ m0));
+            const float4 k1 = lds4(Ks + (tx + 16) * CS + (j ^ m1));
 #pragma unroll
             for (int a = 0; a < 4; ++a) {
-              const float d = tA[(ty + 16 * a) * BN + j];
-              dq[a][kc / 16] = fmaf(d, k0, dq[a][kc / 16]);
-              dq[a][kc / 16 + 1] = fmaf(d, k1, dq[a][kc / 16 + 1]);
+              const float4 d4 = lds4(tA + (4 * ty + a) * CS + j);
+              float& q0 = dq[a][kc / 16];
+              float& q1 = dq[a][kc / 16 + 1];
+              q0 = fmaf(d4.x, k0.x, q0); q1 = fmaf(d4.x, k1.x, q1);
+              q0 = fmaf(d4.y, k0.y, q0); q1 = fmaf(d4.y, k1.y, q1);
+              q0 = fmaf(d4.z, k0.z, q0); q1 = fmaf(d4.z, k1.z, q1);
+              q0 = fmaf(d4.w, k0.w, q0); q1 = fmaf(d4.w, k1.w, q1);
             }
           }
         }
       }
 #pragma unroll
       for (int a = 0; a < 4; ++a) {
-        const int i = i0 + ty + 16 * a;
+        const int i = i0 + 4 * ty + a;
         // far-tile sums of the row: reduce over the 16 lanes that share it
 #pragma unroll
         for (int sd = 0; sd < 2; ++sd)
@@ -454,7 +472,7 @@ __global__ void __launch_bounds__(kThreads, D <= 64 ? 2 : 1) bwd_q_kernel(const 
 #pragma unroll
           for (int c = 0; c < NC; ++c) dst[tx + 16 * c] = dq[a][c];
           if (tx == 0) {
-            float* grow = G + (size_t)(ty + 16 * a) * H * R;
+            float* grow = G + (size_t)(4 * ty + a) * H * R;
             if (far[a][0] != 0.f) atomicAdd(grow, far[a][0]);
             if (far[a][1] != 0.f) atomicAdd(grow + R - 1, far[a][1]);
           }
@@ -467,9 +485,10 @@ __global__ void __launch_bounds__(kThreads, D <= 64 ? 2 : 1) bwd_q_kernel(const 
 // ------------------------------------------------------------------ key side
 template <typename T, int D>
 __global__ void __launch_bounds__(kThreads, D <= 64 ? 2 : 1) bwd_k_kernel(const BwdProblem b) {
-  extern __shared__ float sm[];
+  extern __shared__ float4 sm4[];
+  float* sm = reinterpret_cast<float*>(sm4);
   const Problem& p = b.f;
-  constexpr int NC = D / 16;
+  constexpr int NC = D / 16;  // output columns per thread: tx + 16 c
   const T* __restrict__ gq = static_cast<const T*>(p.q);
   const T* __restrict__ gdo = static_cast<const T*>(b.dout);
   const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
@@ -478,8 +497,8 @@ __global__ void __launch_bounds__(kThreads, D <= 64 ? 2 : 1) bwd_k_kernel(const 
   const int n_items = p.hdr->n_items;
   const int rsp = p.hdr->r_sat_pos, rsn = p.hdr->r_sat_neg;
   const float ks = p.kscale;
-  float* tA = sm + BwdSmem::pk;  // P tile [BM][BN]
-  float* tB = sm + BwdSmem::pq;  // dS tile [BM][BN]
+  float* tA = sm + BwdSmem::ta;  // P tile [BM][CS]
+  float* tB = sm + BwdSmem::tb;  // dS tile [BM][CS]
   float* Qs = sm + BwdSmem::q;
   float* Gs = sm + BwdSmem::g;
 
@@ -492,6 +511,7 @@ __global__ void __launch_bounds__(kThreads, D <= 64 ? 2 : 1) bwd_k_kernel(const 
       const int j0 = kb * kQBlock + sub * BN;
       if (j0 >= n) break;
       float* G = b.gp + ((size_t)(start + j0) * H + h) * R;
+      // thread rows of dK / dV: keys 4 ty + a; columns tx + 16 c
       float dk[4][NC], dv[4][NC], far[4][2];
 #pragma unroll
       for (int a = 0; a < 4; ++a) {
@@ -508,7 +528,7 @@ __global__ void __launch_bounds__(kThreads, D <= 64 ? 2 : 1) bwd_k_kernel(const 
         tile_logits(sm, g, n, j0, ks, s, x);
 #pragma unroll
         for (int a = 0; a < 4; ++a) {
-          const int i = i0 + ty + 16 * a;
+          const int i = i0 + 4 * ty + a;
           const size_t t = (size_t)start + i;
           const float rL = i < n ? b.lse[t * H + h] : INFINITY;
           const float rD = i < n ? b.drow[t * H + h] : 0.f;
@@ -518,42 +538,50 @@ __global__ void __launch_bounds__(kThreads, D <= 64 ? 2 : 1) bwd_k_kernel(const 
             ds[a][bb] = b.sscale * pe[a][bb] * (dp[a][bb] - rD);
           }
         }
-        __syncthreads();  // the band buffers become the P and dS tiles
+        // the P and dS tiles, by query row (their previous readers passed the
+        // barriers of score_tile)
 #pragma unroll
-        for (int a = 0; a < 4; ++a)
-#pragma unroll
-          for (int bb = 0; bb < 4; ++bb) {
-            tA[(ty + 16 * a) * BN + tx + 16 * bb] = pe[a][bb];
-            tB[(ty + 16 * a) * BN + tx + 16 * bb] = ds[a][bb];
-          }
+        for (int a = 0; a < 4; ++a) {
+          *reinterpret_cast<float4*>(tA + (4 * ty + a) * CS + 4 * tx) =
+              make_float4(pe[a][0], pe[a][1], pe[a][2], pe[a][3]);
+          *reinterpret_cast<float4*>(tB + (4 * ty + a) * CS + 4 * tx) =
+              make_float4(ds[a][0], ds[a][1], ds[a][2], ds[a][3]);
+        }
         bucket_sums<false>(G, (size_t)H * R, n - j0, g, ds, far);
-        // dK += dS^T.Q and dV += P^T.dO over this query block, chunk by chunk;
-        // thread rows are keys ty + 16 a
+        // dK += dS^T.Q and dV += P^T.dO over this query block, chunk by chunk
 #pragma unroll
         for (int kc = 0; kc < D; kc += DC) {
           __syncthreads();
           const size_t qrow = (size_t)(start + i0) * ts + (size_t)h * D + kc;
-          stage_t<T, BM + 1>(gq + qrow, ts, BM, n - i0, Qs);
-          stage_t<T, BM + 1>(gdo + qrow, ts, BM, n - i0, Gs);
+          stage_t<T, CS, true>(gq + qrow, ts, BM, n - i0, Qs);
+          stage_t<T, CS, true>(gdo + qrow, ts, BM, n - i0, Gs);
           __syncthreads();
-#pragma unroll 4
-          for (int i = 0; i < BM; ++i) {
-            const float q0 = Qs[tx * (BM + 1) + i], q1 = Qs[(tx + 16) * (BM + 1) + i];
-            const float g0 = Gs[tx * (BM + 1) + i], g1 = Gs[(tx + 16) * (BM + 1) + i];
+          const int m0 = swz<T>(tx), m1 = swz<T>(tx + 16);
+#pragma unroll 2
+          for (int i = 0; i < BM; i += 4) {
+            const float4 q0 = lds4(Qs + tx * CS + (i ^ m0)), q1 = lds4(Qs + (tx + 16) * CS + (i ^ m1));
+            const float4 g0 = lds4(Gs + tx * CS + (i ^ m0)), g1 = lds4(Gs + (tx + 16) * CS + (i ^ m1));
+            const float qa0[4] = {q0.x, q0.y, q0.z, q0.w}, qa1[4] = {q1.x, q1.y, q1.z, q1.w};
+            const float ga0[4] = {g0.x, g0.y, g0.z, g0.w}, ga1[4] = {g1.x, g1.y, g1.z, g1.w};
 #pragma unroll
-            for (int a = 0; a < 4; ++a) {
-              const float sv = tB[i * BN + ty + 16 * a], pv = tA[i * BN + ty + 16 * a];
-              dk[a][kc / 16] = fmaf(sv, q0, dk[a][kc / 16]);
-              dk[a][kc / 16 + 1] = fmaf(sv, q1, dk[a][kc / 16 + 1]);
-              dv[a][kc / 16] = fmaf(pv, g0, dv[a][kc / 16]);
-              dv[a][kc / 16 + 1] = fmaf(pv, g1, dv[a][kc / 16 + 1]);
+            for (int u = 0; u < 4; ++u) {
+              const float4 sv = lds4(tB + (i + u) * CS + 4 * ty);  // dS of query i + u, keys 4 ty..
+              const float4 pv = lds4(tA + (i + u) * CS + 4 * ty);
+              const float svs[4] = {sv.x, sv.y, sv.z, sv.w}, pvs[4] = {pv.x, pv.y, pv.z, pv.w};
+#pragma unroll
+              for (int a = 0; a < 4; ++a) {
+                dk[a][kc / 16] = fmaf(svs[a], qa0[u], dk[a][kc / 16]);
+                dk[a][kc / 16 + 1] = fmaf(svs[a], qa1[u], dk[a][kc / 16 + 1]);
+                dv[a][kc / 16] = fmaf(pvs[a], ga0[u], dv[a][kc / 16]);
+                dv[a][kc / 16 + 1] = fmaf(pvs[a], ga1[u], dv[a][kc / 16 + 1]);
+              }
             }
           }
         }
       }
 #pragma unroll
       for (int a = 0; a < 4; ++a) {
-        const int j = j0 + ty + 16 * a;
+        const int j = j0 + 4 * ty + a;
         if (j < n) {
           const size_t row = ((size_t)(start + j) * H + h) * D;
 #pragma unroll
@@ -563,14 +591,14 @@ __global__ void __launch_bounds__(kThreads, D <= 64 ? 2 : 1) bwd_k_kernel(const 
           }
         }
       }
-      // far-tile sums of key column tx + 16 u: the two half-warps hold
+      // far-tile sums of key column 4 tx + u: the two half-warps hold
       // neighbouring query rows of the same keys
 #pragma unroll
       for (int u = 0; u < 4; ++u)
 #pragma unroll
         for (int sd = 0; sd < 2; ++sd) {
           const float v = far[u][sd] + __shfl_xor_sync(0xffffffffu, far[u][sd], 16);
-          const int jj = tx + 16 * u;
+          const int jj = 4 * tx + u;
           if ((threadIdx.x & 16) == 0 && jj < n - j0 && v != 0.f)
             atomicAdd(G + (size_t)jj * H * R + (sd ? R - 1 : 0), v);
         }
