@@ -175,6 +175,51 @@ class ClockSampler:
                 "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows)}
 
 
+def _cpulist(text: str):
+    cpus = set()
+    for part in text.strip().split(","):
+        if "-" in part:
+            a, b = part.split("-")
+            cpus.update(range(int(a), int(b) + 1))
+        elif part:
+            cpus.add(int(part))
+    return cpus
+
+
+class GpuLocalCpus:
+    """Runs the process on the CPUs of the GPU's NUMA node while page-locked
+    host buffers are allocated and used, so that they sit in the memory the
+    GPU reaches without crossing to another socket (sysfs: the GPU's PCI
+    function and its node's cpulist); the previous affinity comes back on
+    exit.  `node` is None where the topology cannot be read."""
+
+    def __init__(self, device: int):
+        self.device = device
+        self.node = None
+        self.saved = None
+
+    def __enter__(self):
+        try:
+            p = torch.cuda.get_device_properties(self.device)
+            bus = "%04x:%02x:%02x.0" % (p.pci_domain_id, p.pci_bus_id, p.pci_device_id)
+            with open(f"/sys/bus/pci/devices/{bus}/numa_node") as f:
+                node = int(f.read())
+            if node >= 0:
+                with open(f"/sys/devices/system/node/node{node}/cpulist") as f:
+                    cpus = _cpulist(f.read()) & os.sched_getaffinity(0)
+                if cpus:
+                    self.saved = os.sched_getaffinity(0)
+                    os.sched_setaffinity(0, cpus)
+                    self.node = node
+        except (OSError, ValueError, AttributeError):
+            self.node = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.saved is not None:
+            os.sched_setaffinity(0, self.saved)
+
+
 def traffic_record(kernel_file: str):
     """DRAM bytes per launch of the dominant kernel from the committed ncu summary,
     valid only while the kernel source is unchanged since the capture."""
@@ -751,9 +796,12 @@ def main(argv=None):
     assert binding.df_attn_get_device_status(ws) == binding.DF_OK
 
     e2e = None
+    numa = GpuLocalCpus(local)
     if not args.no_e2e:
-        # the host-buffer entry point: page-locked inputs and output, the copies
-        # of each group of sequences overlapped with the kernels of another
+        numa.__enter__()
+        # the host-buffer entry point: page-locked inputs and output (allocated
+        # on the GPU's NUMA node), the copies of each group of sequences
+        # overlapped with the kernels of another
         pinned = {n: t.pin_memory() for n, t in host.items()}
         out_h = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
         h2d = sum(t.numel() * t.element_size() for t in pinned.values())
@@ -780,6 +828,7 @@ def main(argv=None):
         e2e_ms = e0.elapsed_time(e1) / args.steps
         assert binding.df_attn_get_device_status(scratch) == binding.DF_OK
         e2e = (e2e_ms, h2d, d2h)
+        numa.__exit__(None, None, None)
 
     # max over ranks
     ms, near_ms, far_ms, e2e_ms = max_over_ranks([ms, near_ms, far_ms, e2e[0] if e2e else 0.0],
@@ -845,7 +894,8 @@ def main(argv=None):
                                             "frac": oalgo / (oms * 1e-3) / 1e12 / peak}
     if e2e:
         line["e2e"] = {"value": job_throughput(world, flops_rank, e2e_ms) / 1e12, "unit": "TFLOP/s",
-                       "h2d_bytes_per_step": e2e[1], "d2h_bytes_per_step": e2e[2]}
+                       "h2d_bytes_per_step": e2e[1], "d2h_bytes_per_step": e2e[2],
+                       "host_numa_node": numa.node}
     clocks = clk.summary()
     line["clocks"] = clocks
     if rank == 0 and not args.no_cpu_baseline:

@@ -7,17 +7,20 @@
 // sequences and each group run as its own df_attn_fwd call with identical
 // results.  Three streams form a pipeline over two device slots:
 //
-//   copy-in stream   group g's q, k, v (and mask rows) host -> slot g % 2
-//   caller's stream  df_attn_fwd(group g) from slot g % 2
-//   copy-out stream  slot g % 2's output -> host
+//   copy-in stream      group g's q, k, v (and mask rows) host -> slot g % 2
+//   compute stream g%2  df_attn_fwd(group g) from slot g % 2, with the slot's
+//                       own workspace
+//   copy-out stream     slot g % 2's output -> host
 //
 // so the copy-in of group g + 1 and the copy-out of group g - 1 run while
-// group g computes.  A slot is refilled only after the forward that read it
-// has finished, and its output is overwritten only after the copy-out that
-// read it has finished (events).  The caller's stream waits for the last
-// copy-out before the call returns, so synchronising that stream completes
-// everything.  The two copy streams and the events are created once per
-// device and reused; a mutex serialises the enqueueing of concurrent calls.
+// group g computes, and the kernels of group g + 1 can start on the SMs that
+// group g's last work items leave idle.  A slot is refilled only after the
+// forward that read it has finished, and its output is overwritten only after
+// the copy-out that read it has finished (events).  Everything starts after
+// the work already on the caller's stream, which waits for the last copy-out
+// before the call returns, so synchronising that stream completes everything.
+// The streams and events are created once per device and reused; a mutex
+// serialises the enqueueing of concurrent calls.
 #include "df_common.cuh"
 
 #include <string.h>
@@ -31,6 +34,7 @@ namespace {
 struct Pipe {
   int device = -1;
   cudaStream_t in = nullptr, out = nullptr;
+  cudaStream_t comp[2] = {nullptr, nullptr};
   cudaEvent_t start = nullptr;
   cudaEvent_t loaded[2] = {nullptr, nullptr};    // slot inputs on the device
   cudaEvent_t computed[2] = {nullptr, nullptr};  // forward of the slot done
@@ -46,6 +50,8 @@ bool pipe_ready(Pipe& p) {
   if (p.device == dev) return true;
   if (cudaStreamCreateWithFlags(&p.in, cudaStreamNonBlocking) != cudaSuccess) return false;
   if (cudaStreamCreateWithFlags(&p.out, cudaStreamNonBlocking) != cudaSuccess) return false;
+  for (int i = 0; i < 2; ++i)
+    if (cudaStreamCreateWithFlags(&p.comp[i], cudaStreamNonBlocking) != cudaSuccess) return false;
   cudaEvent_t* evs[] = {&p.start, &p.loaded[0], &p.loaded[1], &p.computed[0], &p.computed[1],
                         &p.drained[0], &p.drained[1]};
   for (cudaEvent_t* e : evs)
@@ -57,7 +63,7 @@ bool pipe_ready(Pipe& p) {
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 struct HostLayout {
-  size_t ws, ws_bytes, pk, pq, cu, slot[2], q, k, v, o, mask, total;
+  size_t ws[2], ws_bytes, pk, pq, cu, slot[2], q, k, v, o, mask, total;
   long long cap_tokens;  // tokens one slot holds
   int cap_rows;          // padded: batch rows one slot holds
 };
@@ -75,9 +81,11 @@ HostLayout host_layout(int B, int H, int L, int d, int buckets, int max_rel, int
   l.cap_rows = (int)std::max<long long>(1, l.cap_tokens / L);
   const size_t row = (size_t)H * d * es;
   size_t off = 0;
-  l.ws = off;
   l.ws_bytes = df_attn_workspace_size(B, H, L, d, buckets, max_rel, span);
-  off = align256(off + l.ws_bytes);
+  for (int i = 0; i < 2; ++i) {  // one forward workspace per slot, the first at offset 0
+    l.ws[i] = off;
+    off = align256(off + l.ws_bytes);
+  }
   l.pk = off;
   off = align256(off + 2 * (size_t)span * row);
   l.pq = off;
@@ -177,7 +185,9 @@ extern "C" df_status df_attn_fwd_host(const void* q, const void* k, const void* 
   const size_t pos_bytes = 2 * (size_t)span * row;
   bool ok = cudaEventRecord(P.start, cs) == cudaSuccess &&
             cudaStreamWaitEvent(P.in, P.start, 0) == cudaSuccess &&
-            cudaStreamWaitEvent(P.out, P.start, 0) == cudaSuccess;
+            cudaStreamWaitEvent(P.out, P.start, 0) == cudaSuccess &&
+            cudaStreamWaitEvent(P.comp[0], P.start, 0) == cudaSuccess &&
+            cudaStreamWaitEvent(P.comp[1], P.start, 0) == cudaSuccess;
   ok = ok && cudaMemcpyAsync(base + lay.pk, pos_key, pos_bytes, cudaMemcpyHostToDevice, P.in) == cudaSuccess;
   ok = ok && cudaMemcpyAsync(base + lay.pq, pos_query, pos_bytes, cudaMemcpyHostToDevice, P.in) == cudaSuccess;
   if (packed && ok)
@@ -205,17 +215,19 @@ extern "C" df_status df_attn_fwd_host(const void* q, const void* k, const void* 
                                  cudaMemcpyHostToDevice, P.in) == cudaSuccess;
     ok = ok && cudaEventRecord(P.loaded[sl], P.in) == cudaSuccess;
     // the forward, once the inputs landed and the previous output left the slot
-    ok = ok && cudaStreamWaitEvent(cs, P.loaded[sl], 0) == cudaSuccess;
-    if (gi >= 2) ok = ok && cudaStreamWaitEvent(cs, P.drained[sl], 0) == cudaSuccess;
+    cudaStream_t comp = P.comp[sl];
+    ok = ok && cudaStreamWaitEvent(comp, P.loaded[sl], 0) == cudaSuccess;
+    if (gi >= 2) ok = ok && cudaStreamWaitEvent(comp, P.drained[sl], 0) == cudaSuccess;
     if (!ok) return DF_ERR_CUDA;
     const int Bg = g.s1 - g.s0;
     const int Tg = (int)(g.t1 - g.t0);
     st = df_attn_fwd(slot + lay.q, slot + lay.k, slot + lay.v, base + lay.pk, base + lay.pq,
                      packed ? nullptr : reinterpret_cast<const uint8_t*>(slot + lay.mask),
                      packed ? reinterpret_cast<const int32_t*>(base + lay.cu) + g.cu_off : nullptr, Bg, H, L,
-                     Tg, d, buckets, max_rel, span, dtype, slot + lay.o, base + lay.ws, lay.ws_bytes, stream);
+                     Tg, d, buckets, max_rel, span, dtype, slot + lay.o, base + lay.ws[sl], lay.ws_bytes,
+                     (df_stream_t)comp);
     if (st != DF_OK) return st;
-    ok = cudaEventRecord(P.computed[sl], cs) == cudaSuccess;
+    ok = cudaEventRecord(P.computed[sl], comp) == cudaSuccess;
     // copy out
     ok = ok && cudaStreamWaitEvent(P.out, P.computed[sl], 0) == cudaSuccess;
     if (bytes)

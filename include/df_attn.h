@@ -162,17 +162,21 @@ size_t df_attn_bwd_workspace_size(int B, int H, int L, int d, int buckets, int m
  * max(group_tokens, L) tokens (group_tokens = 0: max(B*L/4, L)), the first
  * groups ramping up from L tokens by doubling, and each group runs as one
  * df_attn_fwd call, with results identical to a single call on the whole
- * batch.  Two library-owned copy streams (created once per device)
- * pipeline the copy-in of group g + 1 and the copy-out of group g - 1 around
- * the forward of group g on `stream`; `stream` waits for the last copy-out, so
- * `out` is complete once `stream` is.  In packed mode cu_seqlens is validated
+ * batch.  Library-owned streams (two for copies, two for the forwards of
+ * alternate groups, created once per device) pipeline the copy-in of group
+ * g + 1 and the copy-out of group g - 1 around the forward of group g, and let
+ * the next group's kernels fill the SMs the previous group leaves idle; all
+ * of it starts after the work already on `stream`, which waits for the last
+ * copy-out, so `out` is complete once `stream` is.  In packed mode cu_seqlens is validated
  * on the host (cu_seqlens[0] = 0, cu_seqlens[B] = total_tokens, every length
  * in [0, L]).
  *
  *   scratch   device memory of df_attn_fwd_host_scratch_size() bytes, 256-byte
  *             aligned: two slots of q, k, v, out for one group, the relative
- *             embeddings and the forward's workspace, which sits at offset 0
- *             (df_attn_get_device_status(scratch, stream) reads its status)
+ *             embeddings and two forward workspaces of
+ *             df_attn_workspace_size(B, H, L, d, ...) bytes each, the first at
+ *             offset 0 and the second at that size rounded up to 256
+ *             (df_attn_get_device_status reads each one's status)
  *
  * Calls are serialised by a mutex while they enqueue; calls that share a
  * scratch buffer must be ordered by their streams.  Returns DF_ERR_CUDA if a
