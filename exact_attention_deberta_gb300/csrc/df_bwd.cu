@@ -294,7 +294,7 @@ __device__ __forceinline__ void bucket_sums(float* G, size_t row_stride, int lim
 
 // ---------------------------------------------------------------- query side
 template <typename T, int D>
-__global__ void __launch_bounds__(kThreads, D <= 64 ? 2 : 1) bwd_q_kernel(const BwdProblem b) {
+__global__ void __launch_bounds__(kThreads, 2) bwd_q_kernel(const BwdProblem b) {
   extern __shared__ float4 sm4[];
   float* sm = reinterpret_cast<float*>(sm4);
   const Problem& p = b.f;
@@ -484,7 +484,7 @@ __global__ void __launch_bounds__(kThreads, D <= 64 ? 2 : 1) bwd_q_kernel(const 
 
 // ------------------------------------------------------------------ key side
 template <typename T, int D>
-__global__ void __launch_bounds__(kThreads, D <= 64 ? 2 : 1) bwd_k_kernel(const BwdProblem b) {
+__global__ void __launch_bounds__(kThreads, 2) bwd_k_kernel(const BwdProblem b) {
   extern __shared__ float4 sm4[];
   float* sm = reinterpret_cast<float*>(sm4);
   const Problem& p = b.f;
