@@ -121,6 +121,57 @@ template <> struct IO<__half> {
   static __device__ __forceinline__ __half from_f(float x) { return __float2half_rn(x); }
 };
 
+// Staging of [rows][ts] token-major tiles into shared memory as fp32 with
+// 16-byte global loads (each row's columns start 16-byte aligned).
+// Transposed: dst[c * STRIDE + r] for columns c < C; with STRIDE = 1 modulo 32
+// the scalar stores of a warp fall in 32 different banks.
+template <typename T, int C, int STRIDE, int NT>
+__device__ __forceinline__ void stage_transposed(const T* __restrict__ base, size_t ts, int rows, int lim,
+                                                 float* dst) {
+  constexpr int V = 16 / sizeof(T), VPR = C / V;
+  static_assert(C % V == 0 && STRIDE % 32 == 1, "16-byte rows, conflict-free stores");
+  for (int e = threadIdx.x; e < rows * VPR; e += NT) {
+    const int r = e / VPR, v = e % VPR;
+    float f[V];
+    if (r < lim) {
+      const uint4 raw = *reinterpret_cast<const uint4*>(base + (size_t)r * ts + v * V);
+      const T* el = reinterpret_cast<const T*>(&raw);
+#pragma unroll
+      for (int k = 0; k < V; ++k) f[k] = IO<T>::to_f(el[k]);
+    } else {
+#pragma unroll
+      for (int k = 0; k < V; ++k) f[k] = 0.f;
+    }
+#pragma unroll
+    for (int k = 0; k < V; ++k) dst[(v * V + k) * STRIDE + r] = f[k];
+  }
+}
+
+// Row-major: dst[r * C + c] (dst 16-byte aligned), 16-byte loads and stores.
+template <typename T, int C, int NT>
+__device__ __forceinline__ void stage_rows(const T* __restrict__ base, size_t ts, int rows, int lim,
+                                           float* dst) {
+  constexpr int V = 16 / sizeof(T), VPR = C / V;
+  static_assert(C % V == 0 && V % 4 == 0, "16-byte rows");
+  for (int e = threadIdx.x; e < rows * VPR; e += NT) {
+    const int r = e / VPR, v = e % VPR;
+    float4 f[V / 4];
+    if (r < lim) {
+      const uint4 raw = *reinterpret_cast<const uint4*>(base + (size_t)r * ts + v * V);
+      const T* el = reinterpret_cast<const T*>(&raw);
+#pragma unroll
+      for (int k = 0; k < V / 4; ++k)
+        f[k] = make_float4(IO<T>::to_f(el[4 * k]), IO<T>::to_f(el[4 * k + 1]), IO<T>::to_f(el[4 * k + 2]),
+                           IO<T>::to_f(el[4 * k + 3]));
+    } else {
+#pragma unroll
+      for (int k = 0; k < V / 4; ++k) f[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int k = 0; k < V / 4; ++k) reinterpret_cast<float4*>(dst + (size_t)r * C + v * V)[k] = f[k];
+  }
+}
+
 // First device-side error wins; later ones are dropped.
 __device__ __forceinline__ void raise_device_error(df_ws_header* hdr, int code, int where) {
   if (atomicCAS(&hdr->status, 0, code) == 0) hdr->status_where = where;

@@ -115,10 +115,8 @@ __global__ void __launch_bounds__(kThreads) simt_fwd_kernel(Problem p) {
           colB[BN + e] = ok ? scal_h[3 * (size_t)p.t_pad + t] : -INFINITY;
           colB[2 * BN + e] = ok ? p.keybias[t] : -INFINITY;
         }
-        for (int e = tid; e < BN * D; e += kThreads) {
-          const int j = e / D, c = e % D;
-          Vs[e] = j0 + j < n ? IO<T>::load(gv + (start + j0 + j) * tok_stride + (size_t)h * D + c) : 0.f;
-        }
+        stage_rows<T, D, kThreads>(gv + (size_t)(start + j0) * tok_stride + (size_t)h * D, tok_stride, BN,
+                                   n - j0, Vs);
         float s[4][4], cp[4][4], pc[4][4];
 #pragma unroll
         for (int a = 0; a < 4; ++a)
@@ -127,19 +125,14 @@ __global__ void __launch_bounds__(kThreads) simt_fwd_kernel(Problem p) {
 
         for (int kc = 0; kc < D; kc += DC) {
           if (kc) __syncthreads();
-          for (int e = tid; e < BM * DC; e += kThreads) {
-            const int r = e / DC, c = e % DC;
-            const size_t off = (size_t)h * D + kc + c;
-            Qs[c * (BM + 1) + r] = i0 + r < n ? IO<T>::load(gq + (start + i0 + r) * tok_stride + off) : 0.f;
-            Ks[c * (BN + 1) + r] = j0 + r < n ? IO<T>::load(gk + (start + j0 + r) * tok_stride + off) : 0.f;
-          }
+          const size_t hc = (size_t)h * D + kc;
+          stage_transposed<T, DC, BM + 1, kThreads>(gq + (size_t)(start + i0) * tok_stride + hc, tok_stride,
+                                                   BM, n - i0, Qs);
+          stage_transposed<T, DC, BN + 1, kThreads>(gk + (size_t)(start + j0) * tok_stride + hc, tok_stride,
+                                                   BN, n - j0, Ks);
           if (!far) {
-            for (int e = tid; e < w * DC; e += kThreads) {
-              const int u = e / DC, c = e % DC;
-              const size_t off = (size_t)(lo + u) * tok_stride + (size_t)h * D + kc + c;
-              PKs[c * (WB + 1) + u] = IO<T>::load(gpk + off);
-              PQs[c * (WB + 1) + u] = IO<T>::load(gpq + off);
-            }
+            stage_transposed<T, DC, WB + 1, kThreads>(gpk + (size_t)lo * tok_stride + hc, tok_stride, w, w, PKs);
+            stage_transposed<T, DC, WB + 1, kThreads>(gpq + (size_t)lo * tok_stride + hc, tok_stride, w, w, PQs);
           }
           __syncthreads();
           if (far) {
