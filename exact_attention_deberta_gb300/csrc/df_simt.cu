@@ -70,13 +70,17 @@ __global__ void __launch_bounds__(kThreads) simt_fwd_kernel(Problem p) {
   const float ks = p.kscale;
   constexpr int NC = D / 16;  // output columns per thread
 
-  for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
-    const int4 item = p.items[it];
+  // one work unit per 64-row half of an item: a small problem still fills
+  // twice as many blocks
+  constexpr int kSubs = kQBlock / BM;
+  for (int u = blockIdx.x; u < n_items * kSubs; u += gridDim.x) {
+    const int4 item = p.items[u / kSubs];
     const int start = item.x, n = item.y, h = item.z, qb = item.w;
     const float* scal_h = p.scal + (size_t)h * 4 * p.t_pad;
-    for (int sub = 0; sub < kQBlock / BM; ++sub) {
+    {
+      const int sub = u % kSubs;
       const int i0 = qb * kQBlock + sub * BM;
-      if (i0 >= n) break;
+      if (i0 >= n) continue;
       __syncthreads();
       for (int e = tid; e < BM; e += kThreads) {
         const int t = start + i0 + e;
@@ -259,7 +263,7 @@ cudaError_t launch_typed(const Problem& p, cudaStream_t s) {
   cudaError_t e = cudaFuncSetAttribute(simt_fwd_kernel<T, D>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
   if (e != cudaSuccess) return e;
-  const int grid = std::min(p.max_items, num_sms() * 2);
+  const int grid = std::min(p.max_items * (kQBlock / BM), num_sms() * 2);
   if (grid <= 0) return cudaSuccess;
   simt_fwd_kernel<T, D><<<grid, kThreads, bytes, s>>>(p);
   return cudaGetLastError();
