@@ -312,14 +312,16 @@ __global__ void __launch_bounds__(kThreads, 2) bwd_q_kernel(const BwdProblem b) 
   float* tA = sm + BwdSmem::ta;     // pass 1: P tile, pass 2: dS tile [BM][CS]
   float* Ks = sm + BwdSmem::k;
 
-  for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
-    const int4 item = p.items[it];
+  // one work unit per 64-row half of an item
+  constexpr int kSubs = kQBlock / BM;
+  for (int u = blockIdx.x; u < n_items * kSubs; u += gridDim.x) {
+    const int4 item = p.items[u / kSubs];
     const int start = item.x, n = item.y, h = item.z, qb = item.w;
     const float* scal_h = p.scal + (size_t)h * 4 * p.t_pad;
     const int nkb = (n + BN - 1) / BN;
-    for (int sub = 0; sub < kQBlock / BM; ++sub) {
-      const int i0 = qb * kQBlock + sub * BM;
-      if (i0 >= n) break;
+    {
+      const int i0 = qb * kQBlock + (u % kSubs) * BM;
+      if (i0 >= n) continue;
       // ---- pass 1: the forward of these rows in fp32
       float m[4], l[4], o[4][NC];
 #pragma unroll
@@ -502,14 +504,16 @@ __global__ void __launch_bounds__(kThreads, 2) bwd_k_kernel(const BwdProblem b) 
   float* Qs = sm + BwdSmem::q;
   float* Gs = sm + BwdSmem::g;
 
-  for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
-    const int4 item = p.items[it];
+  // one work unit per 64-key half of an item
+  constexpr int kSubs = kQBlock / BN;
+  for (int u = blockIdx.x; u < n_items * kSubs; u += gridDim.x) {
+    const int4 item = p.items[u / kSubs];
     const int start = item.x, n = item.y, h = item.z, kb = item.w;
     const float* scal_h = p.scal + (size_t)h * 4 * p.t_pad;
     const int nqb = (n + BM - 1) / BM;
-    for (int sub = 0; sub < kQBlock / BN; ++sub) {
-      const int j0 = kb * kQBlock + sub * BN;
-      if (j0 >= n) break;
+    {
+      const int j0 = kb * kQBlock + (u % kSubs) * BN;
+      if (j0 >= n) continue;
       float* G = b.gp + ((size_t)(start + j0) * H + h) * R;
       // thread rows of dK / dV: keys 4 ty + a; columns tx + 16 c
       float dk[4][NC], dv[4][NC], far[4][2];
@@ -719,8 +723,9 @@ cudaError_t launch_typed(const BwdProblem& b, cudaStream_t s, cudaEvent_t ev0, c
   int occ_q = 0, occ_k = 0;
   cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ_q, bwd_q_kernel<T, D>, kThreads, bytes_q);
   cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ_k, bwd_k_kernel<T, D>, kThreads, bytes_k);
-  const int grid_q = std::min(p.max_items, num_sms() * std::max(occ_q, 1));
-  const int grid_k = std::min(p.max_items, num_sms() * std::max(occ_k, 1));
+  const int units = p.max_items * (kQBlock / BM);
+  const int grid_q = std::min(units, num_sms() * std::max(occ_q, 1));
+  const int grid_k = std::min(units, num_sms() * std::max(occ_k, 1));
   int n = 0;
   if (ev0) cudaEventRecord(ev0, s);
   if (grid_q > 0) {
