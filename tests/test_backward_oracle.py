@@ -177,3 +177,27 @@ def test_gradient_product_identity():
     lhs = np.sum(dk * k) - np.sum(dpq * pq)
     rhs = np.sum(dq * q) - np.sum(dpk * pk)
     assert abs(lhs - rhs) < 1e-10 * (1 + abs(lhs))
+
+
+def test_packed_and_padded_layouts_agree():
+    """The same sequences as padded batch rows and as a packed batch give the
+    same per-token gradients and the same position gradients."""
+    rng = np.random.default_rng(19)
+    lengths = [7, 12, 3]
+    L, H, d = 12, 2, 4
+    cu = np.concatenate([[0], np.cumsum(lengths)])
+    T = int(cu[-1])
+    q, k, v, w = (_rand(rng, T, H, d) for _ in range(4))
+    pk, pq = (_rand(rng, 2 * CFG["span"], H, d) for _ in range(2))
+    packed = backward_packed(q, k, v, pk, pq, w, cu, **CFG)
+    pad = lambda x: np.stack([np.concatenate([x[cu[b]:cu[b + 1]], np.zeros((L - n, H, d))])  # noqa: E731
+                              for b, n in enumerate(lengths)])
+    mask = np.zeros((len(lengths), L), dtype=np.uint8)
+    for b, n in enumerate(lengths):
+        mask[b, :n] = 1
+    padded = backward_padded(pad(q), pad(k), pad(v), pk, pq, pad(w), mask, **CFG)
+    for b, n in enumerate(lengths):
+        for g_pk, g_pd in zip(packed[:3], padded[:3]):
+            np.testing.assert_allclose(g_pd[b, :n], g_pk[cu[b]:cu[b + 1]], rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(padded[3], packed[3], rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(padded[4], packed[4], rtol=1e-12, atol=1e-12)
