@@ -3,8 +3,9 @@
 Small cases (several 64-row tiles, ragged tails, masked holes, empty and
 one-token sequences, near and far tiles, every dtype and head size) are
 compared element by element on every gradient.  At the long packed workload
-(16 x 8192 tokens, H = 12, d = 64) the oracle computes sampled rows of dQ and
-sampled keys of dK and dV one by one, and the position gradients are checked
+(16 x 8192 tokens, H = 12, d = 64, and H = 8, d = 128) the oracle computes
+sampled rows of dQ and sampled keys of dK and dV one by one, and the position
+gradients are checked
 through identities that hold at any size:
   sum_r dPK[r] = 0                      (a shift of every PK row moves no softmax)
   sum_j dV_j = sum_i dO_i               (softmax rows sum to one)
@@ -118,8 +119,9 @@ def _identities(x, dout, got, tol=TOL):
 
 
 @pytest.mark.slow
-def test_backward_long_packed_sampled(lib):
-    x = synth.make_inputs("long_packed_h12d64")
+@pytest.mark.parametrize("workload", ["long_packed_h12d64", "long_packed_h8d128"])
+def test_backward_long_packed_sampled(lib, workload):
+    x = synth.make_inputs(workload)
     dout = synth.grad_output(x)
     got = _run(lib, x, dout)
     for nm, g in zip(("dq", "dk", "dv", "dpk", "dpq"), got):

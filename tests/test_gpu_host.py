@@ -64,3 +64,12 @@ def test_host_forward_long_workload_groups(lib):
     ref = _device_out(lib, x)
     got = _host_out(lib, x, 16384, True)   # eight groups of two 8192-token sequences
     assert torch.equal(got.view(torch.int16), ref.view(torch.int16))
+
+
+def test_host_forward_head_size_32(lib):
+    """Head size 32 runs the d = 64 kernels on widened copies: the host-buffer
+    path must give the same bytes as the device call there too."""
+    x = synth.custom_inputs(layout="packed", dtype="bf16", H=4, d=32, lengths=[700, 1, 129, 0, 300], seed=11)
+    ref = _device_out(lib, x)
+    got = _host_out(lib, x, 0, True)
+    assert torch.equal(got.view(torch.int16), ref.view(torch.int16))
