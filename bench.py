@@ -211,7 +211,7 @@ class GpuLocalCpus:
                     self.saved = os.sched_getaffinity(0)
                     os.sched_setaffinity(0, cpus)
                     self.node = node
-        except (OSError, ValueError, AttributeError):
+        except Exception:  # no device, no sysfs entry, an unreadable topology: leave affinity alone
             self.node = None
         return self
 
