@@ -135,10 +135,10 @@ size_t df_attn_workspace_size(int B, int H, int L, int d, int buckets, int max_r
  *
  * Everything is computed in fp32 on CUDA cores: the forward is recomputed per
  * query block (row log-sum-exp and O, so `out` is not an input), the score
- * tiles are recomputed on the key side, and the position gradients are
- * reduced over fixed token ranges with no global atomics (the per-block
- * bucket sums use shared-memory atomics, so the last bits may differ from
- * run to run).  Returns once the work is enqueued.
+ * tiles are recomputed on the key side, the sums of dS by relative index are
+ * accumulated in the workspace with atomic adds (so the last bits may differ
+ * from run to run), and the position gradients are then reduced over fixed
+ * token ranges.  Returns once the work is enqueued.
  */
 df_status df_attn_bwd(const void* q, const void* k, const void* v,
                       const void* pos_key, const void* pos_query, const void* dout,
