@@ -278,6 +278,16 @@ def df_attn_fwd_noalloc(q, k, v, pos_key, pos_query, key_mask=None, cu_seqlens=N
     return out
 
 
+_lib.df_attn_noalloc_get_device_status.argtypes = [_vp]
+_lib.df_attn_noalloc_get_device_status.restype = _i
+
+
+def df_attn_noalloc_get_device_status(stream=None) -> int:
+    """Status word of the latest df_attn_fwd_noalloc call on the current device
+    (read and cleared; synchronises the stream)."""
+    return int(_lib.df_attn_noalloc_get_device_status(_stream(stream)))
+
+
 def df_attn_get_device_status(workspace, stream=None) -> int:
     return int(_lib.df_attn_get_device_status(_ptr(workspace), _stream(stream)))
 

@@ -120,6 +120,8 @@ __global__ void __launch_bounds__(kLinThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tslot;
+  // two fp32 accumulators of kBN columns each: columns 0 .. 2 kBN - 1
+  static_assert(tmem_region_fits(kBN, kBN, 512), "two accumulators in 512 columns");
 
   const int n_mb = (args.M + kBM - 1) / kBM, n_nb = args.N / kBN, nk = args.K / kBK;
   const int per_mb = args.n_out * n_nb;

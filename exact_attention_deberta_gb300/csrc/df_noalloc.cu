@@ -11,7 +11,13 @@
 //
 // The array holds DF_ATTN_NOALLOC_SCRATCH_BYTES on every GPU that loads the
 // library, for as long as the process lives.  Its device address is looked up
-// once per device, by the first call made with that device current.
+// once per device, by the first call made with that device current, and kept
+// for the life of the process (a device reset invalidates it: the entry points
+// here must not be used after cudaDeviceReset on that device).
+//
+// Errors the kernels raise on the device (a bounded wait that ran out, bad
+// cu_seqlens) land in the status word at the start of the shared array;
+// df_attn_noalloc_get_device_status reads and clears it.
 #include "df_common.cuh"
 
 #include <mutex>
@@ -60,4 +66,11 @@ extern "C" df_status df_attn_fwd_noalloc(const void* q, const void* k, const voi
   return df_attn_fwd(q, k, v, pos_key, pos_query, key_mask, cu_seqlens, B, H, L, total_tokens, d,
                      buckets, max_rel, span, dtype, out, scratch,
                      (size_t)DF_ATTN_NOALLOC_SCRATCH_BYTES, stream);
+}
+
+extern "C" df_status df_attn_noalloc_get_device_status(df_stream_t stream) {
+  void* scratch = nullptr;
+  const df_status st = scratch_on_current_device(&scratch);
+  if (st != DF_OK) return st;
+  return df_attn_get_device_status(scratch, stream);
 }

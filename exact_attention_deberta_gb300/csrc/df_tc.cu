@@ -117,6 +117,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tslot;
   const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+  // S 0-127, C band 128-255, P band 256-383, O 384-(384 + D - 1)
+  static_assert(tmem_region_fits(384, D, 512), "O accumulator in 512 columns");
   const uint32_t tS = tmem, tA = tmem + 128, tB = tmem + 256, tO = tmem + 384;
 
   uint32_t ph_q = 0, ph_kv = 0, ph_v = 0, ph_band = 0, ph_mma = 0;

@@ -19,6 +19,12 @@ struct TcMaps {
 
 constexpr uint32_t kAugBytes = 128 * 16 * 2;  // one 128-row x 16-column 16-bit box
 
+// Tensor-memory column maps are checked at compile time: every region (first
+// column, width in 32-bit columns) must end inside the kernel's allocation.
+constexpr bool tmem_region_fits(uint32_t first, uint32_t width, uint32_t alloc) {
+  return width > 0 && first + width <= alloc;
+}
+
 // Descriptor of a K-major 128-row operand with 16 elements (32 bytes) per row,
 // 32-byte swizzle: 8-row groups 256 bytes apart.
 __device__ __forceinline__ uint64_t aug_desc(const uint8_t* tile) {

@@ -156,7 +156,10 @@ __global__ void __launch_bounds__(kFarThreads, 1)
   // so neither the softmax nor QK(G + 2) waits for a P.V.  d = 128: one score
   // buffer per warpgroup (P overwrites it) and the two O.
   constexpr bool kTriS = D == 64;
-  const uint32_t tO_base = tmem + (kTriS ? 384u : 256u);
+  constexpr uint32_t kScoreBufs = kTriS ? 3u : 2u, kOFirst = kTriS ? 384u : 256u;
+  static_assert(tmem_region_fits(0, 128u * kScoreBufs, kOFirst), "score buffers below O");
+  static_assert(tmem_region_fits(kOFirst, 2u * D, 512), "two O accumulators in 512 columns");
+  const uint32_t tO_base = tmem + kOFirst;
   auto tS = [&](int b) { return tmem + 128u * b; };
   auto tO = [&](int b) { return tO_base + (uint32_t)D * b; };
 

@@ -90,8 +90,10 @@ def draw_lengths(w: Workload, rng: np.random.Generator) -> np.ndarray:
     return n
 
 
-def _normal(rng, shape, dtype: str) -> torch.Tensor:
+def _normal(rng, shape, dtype: str, scale: float = 1.0) -> torch.Tensor:
     x = rng.standard_normal(size=shape, dtype=np.float32)
+    if scale != 1.0:
+        x = x * np.float32(scale)
     return torch.from_numpy(x).to(DTYPES[dtype]).contiguous()
 
 
@@ -119,8 +121,11 @@ class Inputs:
         return [(b * self.w.L, int(n)) for b, n in enumerate(self.lengths)]
 
 
-def make_inputs(w: Workload | str, *, lengths: Optional[np.ndarray] = None) -> Inputs:
-    """Draw one workload.  ``lengths`` overrides the length law (tests)."""
+def make_inputs(w: Workload | str, *, lengths: Optional[np.ndarray] = None,
+                scale: float = 1.0) -> Inputs:
+    """Draw one workload.  ``lengths`` overrides the length law (tests);
+    ``scale`` multiplies the draws of Q, K, PK and PQ (not V) before the cast,
+    so that the logits grow by scale^2 (tests of large score magnitudes)."""
     if isinstance(w, str):
         w = WORKLOADS[w]
     rng = np.random.default_rng(w.seed)
@@ -141,11 +146,11 @@ def make_inputs(w: Workload | str, *, lengths: Optional[np.ndarray] = None) -> I
         mask = None
         cu = torch.zeros(n.size + 1, dtype=torch.int32)
         cu[1:] = torch.from_numpy(np.cumsum(n).astype(np.int32))
-    q = _normal(rng, shape, w.dtype)
-    k = _normal(rng, shape, w.dtype)
+    q = _normal(rng, shape, w.dtype, scale)
+    k = _normal(rng, shape, w.dtype, scale)
     v = _normal(rng, shape, w.dtype)
-    pk = _normal(rng, (P, H, d), w.dtype)
-    pq = _normal(rng, (P, H, d), w.dtype)
+    pk = _normal(rng, (P, H, d), w.dtype, scale)
+    pq = _normal(rng, (P, H, d), w.dtype, scale)
     return Inputs(w, n, q, k, v, pk, pq, mask, cu)
 
 
@@ -158,8 +163,9 @@ def grad_output(x: Inputs, salt: int = 1) -> torch.Tensor:
 
 def custom_inputs(*, layout: str, dtype: str, H: int, d: int, lengths, L: Optional[int] = None,
                   seed: int = 0, buckets: int = 256, max_rel: int = 512,
-                  span: Optional[int] = None) -> Inputs:
-    """Same recipe with explicit shapes (edge-case tests)."""
+                  span: Optional[int] = None, scale: float = 1.0) -> Inputs:
+    """Same recipe with explicit shapes (edge-case tests); ``scale`` as in
+    make_inputs."""
     lengths = np.asarray(lengths, dtype=np.int64)
     if span is None:
         span = buckets if buckets > 0 else max_rel
@@ -167,4 +173,4 @@ def custom_inputs(*, layout: str, dtype: str, H: int, d: int, lengths, L: Option
         L = int(lengths.max()) if lengths.size else 1
     w = Workload(f"custom_{layout}_{dtype}_H{H}d{d}", seed, layout, dtype, H, d, L,
                  int(lengths.size), "full", buckets, max_rel, span)
-    return make_inputs(w, lengths=lengths)
+    return make_inputs(w, lengths=lengths, scale=scale)

@@ -313,8 +313,12 @@ int df_attn_last_launch_count(void);
  *   - every call on a device shares the one array, which keeps the previous
  *     call's contents: calls that overlap on the GPU (other streams, other host
  *     threads) race on it and must be serialised by the caller;
- *   - the device-side status word lives in that shared array and is not
- *     reported through this entry point.
+ *   - the array's device address is kept for the life of the process: do not
+ *     call this entry point on a device after cudaDeviceReset;
+ *   - errors raised on the device (a bounded wait that ran out, bad
+ *     cu_seqlens) are recorded in the status word at the start of the shared
+ *     array, where each call's planning kernel resets it; read them with
+ *     df_attn_noalloc_get_device_status.
  * It calls no cudaMalloc, cudaFree or other allocating routine.
  */
 #define DF_ATTN_NOALLOC_SCRATCH_BYTES (64u << 20)
@@ -324,6 +328,14 @@ df_status df_attn_fwd_noalloc(const void* q, const void* k, const void* v,
                               int B, int H, int L, int total_tokens, int d,
                               int buckets, int max_rel, int span, df_dtype dtype,
                               void* out, df_stream_t stream);
+
+/* Device-side status of the latest df_attn_fwd_noalloc call on the current
+ * device: synchronises `stream`, reads the status word from the shared scratch
+ * array and clears it (the df_attn_get_device_status of that array).  Returns
+ * DF_OK, DF_ERR_DEVICE_TIMEOUT or DF_ERR_INVALID_ARG as the kernels recorded
+ * them, or DF_ERR_CUDA if the synchronisation or the copy fails.  Allocates
+ * nothing.  No counterpart in the pages, like df_attn_fwd_noalloc. */
+df_status df_attn_noalloc_get_device_status(df_stream_t stream);
 
 /* ---------------------------------------------------------------------------
  * Packing between the padded and the packed layout (DisentangledFlash 0.2.0

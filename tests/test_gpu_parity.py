@@ -205,15 +205,44 @@ def test_mask_holes_in_far_tiles(lib, dtype, d):
     assert_close(out.double().cpu().numpy(), ref, dtype, f"far-holes-{dtype}-d{d}")
 
 
+@pytest.mark.parametrize("dtype,d", [("bf16", 64), ("fp16", 64), ("bf16", 128), ("fp16", 128)])
 @pytest.mark.parametrize("buckets,max_rel,span", [(0, 300, 300), (32, 64, 32), (256, 512, 128), (16, 4096, 16)])
-def test_other_position_parameters(lib, buckets, max_rel, span):
-    x = synth.custom_inputs(layout="packed", dtype="bf16", H=2, d=64, lengths=[900, 64, 1500], L=1500,
-                            seed=buckets + max_rel, buckets=buckets, max_rel=max_rel, span=span)
+def test_other_position_parameters(lib, buckets, max_rel, span, dtype, d):
+    x = synth.custom_inputs(layout="packed", dtype=dtype, H=2, d=d, lengths=[900, 64, 1500], L=1500,
+                            seed=buckets + max_rel + d, buckets=buckets, max_rel=max_rel, span=span)
     out = run_gpu(lib, x)
     triples = sample_triples(x, 200, 7)
     ref = oracle_sampled(x, triples)
     keys = sorted(ref)
-    assert_close(gpu_rows(x, out, keys), np.stack([ref[k] for k in keys]), "bf16", "params")
+    assert_close(gpu_rows(x, out, keys), np.stack([ref[k] for k in keys]), dtype,
+                 f"params-{dtype}-d{d}")
+
+
+@pytest.mark.parametrize("scale", [4.0, 16.0])
+@pytest.mark.parametrize("dtype,d", [("bf16", 64), ("fp16", 64), ("bf16", 128), ("fp16", 128)])
+def test_large_logits(lib, dtype, d, scale):
+    """Q, K, PK and PQ drawn from N(0, scale^2) (V from N(0, 1)): logits reach
+    thousands of raw score units, so the position terms must keep their
+    precision on near tiles as well as far ones.  Every row of a packed batch
+    whose longest sequence has near and far tiles."""
+    x = synth.custom_inputs(layout="packed", dtype=dtype, H=2, d=d, lengths=[1800, 700, 129], L=1800,
+                            seed=int(scale) + d, scale=scale)
+    out = run_gpu(lib, x)
+    assert_close(out.double().cpu().numpy(), oracle_full(x), dtype, f"scale{scale:g}-{dtype}-d{d}")
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_beyond_8192_tokens(lib, d):
+    """A 16384-token sequence (and a short one) in packed mode: sampled rows,
+    tile edges included, against the oracle."""
+    x = synth.custom_inputs(layout="packed", dtype="bf16", H=2, d=d, lengths=[16384, 300], L=16384,
+                            seed=40 + d)
+    out = run_gpu(lib, x)
+    triples = sample_triples(x, 96, 11)
+    triples += [(0, 1, 8191), (0, 0, 8192), (0, 1, 16383), (0, 0, 16256)]
+    ref = oracle_sampled(x, triples)
+    keys = sorted(ref)
+    assert_close(gpu_rows(x, out, keys), np.stack([ref[k] for k in keys]), "bf16", f"L16384-d{d}")
 
 
 def test_packed_matches_padded(lib):
