@@ -21,8 +21,11 @@ constexpr int kQBlock = 128;
 // Keys per far tile of the tensor-core path.
 constexpr int kKBlock = 128;
 // Stand-in for -inf in the key-term block (raw score units): it must stay
-// finite because the MMA multiplies the unused side's terms by 0.
-constexpr float kMaskedKeyTerm = -30000.f;
+// finite because the MMA multiplies the unused side's terms by 0.  A masked key
+// carries it in both the high and the low part of each side, so the score MMA
+// adds 2 x (-65504): the key's weight underflows to 0 as long as the raw scores
+// |Q.K + Q.PK + K.PQ| of the row stay well below 131008.
+constexpr float kMaskedKeyTerm = -65504.f;
 
 // Workspace views and call parameters handed to every kernel.
 struct Problem {

@@ -89,9 +89,9 @@ __device__ void scalar_block(const Problem& p, int blk) {
     const float c0 = valid ? b0 : kMaskedKeyTerm, c1 = valid ? b1 : kMaskedKeyTerm;
     const T h0 = IO<T>::from_f(c0), h1 = IO<T>::from_f(c1);
     v[0] = h0;
-    v[1] = IO<T>::from_f(valid ? c0 - IO<T>::to_f(h0) : 0.f);
+    v[1] = IO<T>::from_f(valid ? c0 - IO<T>::to_f(h0) : kMaskedKeyTerm);
     v[2] = h1;
-    v[3] = IO<T>::from_f(valid ? c1 - IO<T>::to_f(h1) : 0.f);
+    v[3] = IO<T>::from_f(valid ? c1 - IO<T>::to_f(h1) : kMaskedKeyTerm);
 #pragma unroll
     for (int e = 4; e < 16; ++e) v[e] = IO<T>::from_f(0.f);
     uint4* dst = reinterpret_cast<uint4*>(static_cast<T*>(p.kaug) + ((size_t)t * H + h) * 16);

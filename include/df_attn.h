@@ -93,6 +93,15 @@ typedef enum { DF_BF16 = 0, DF_FP16 = 1, DF_FP32 = 2 } df_dtype;
  *                      workspace must not overlap in time)
  *   stream             CUDA stream for every launch
  *
+ * Precision (bf16 / fp16): Q.K^T and both position terms are accumulated and
+ * added in fp32 on every tile; P is rounded to the I/O type for P.V; the output
+ * is rounded from fp32.  Magnitude limit: a masked key inside a tile whose
+ * position terms are saturated (padded mode with holes in the mask) is removed
+ * by adding -131008 to its raw score (a finite stand-in for -inf), so the
+ * result is exact while the raw scores |Q_i.K_j + Q_i.PK + K_j.PQ| of a row stay
+ * well below 131008; keys past a sequence's last valid token are removed
+ * exactly.  NaN / Inf inputs are out of contract.
+ *
  * Returns DF_OK once the work is enqueued; errors raised on the device are
  * reported by df_attn_get_device_status().
  */
@@ -243,7 +252,8 @@ typedef struct {
   int diag_m0;
   /* Key-term block of far tiles (16-bit I/O types): [Tpad][H][16] in the I/O
    * type, per key the raw p2c products K.PQ[0] and K.PQ[2span-1], each as a
-   * high and a low part (hi + lo), then zeros; masked keys hold -30000.  Below
+   * high and a low part (hi + lo), then zeros; masked keys hold -65504 in each
+   * part (the score MMA adds hi + lo = -131008).  Below
    * it, kaug_sel: [256][16] selector rows (1, 1, 0, ...) and (0, 0, 1, 1, ...). */
   size_t kaug;
   size_t kaug_sel;
