@@ -59,14 +59,16 @@ __device__ __forceinline__ uint64_t vtile_desc(uint32_t v_addr, int ks) {
 // distances i - j in [i0 - j0 - 127, i0 - j0 + 127] are not all saturated).
 // The near blocks form one run [*jlo, *jhi); blocks before it are saturated on
 // the positive side (idx = 2 span - 1), blocks after it on the negative side.
+// Block jb is saturated on the positive side iff i0 - 128 jb - 127 >= rsp, i.e.
+// jb <= floor((i0 - 127 - rsp) / 128); it is short of saturation on the
+// negative side iff i0 - 128 jb + 127 > rsn, i.e. jb < ceil((i0 + 127 - rsn) / 128).
+// (Arithmetic right shifts give the floor of a negative numerator.)
 __device__ __forceinline__ void near_block_range(int i0, int nkb, int rsp, int rsn, int* jlo,
                                                  int* jhi) {
-  int lo = 0, hi = 0;
-  for (int jb = 0; jb < nkb; ++jb) {
-    const int j0 = jb * 128;
-    if (i0 - j0 - 127 >= rsp) lo = jb + 1;      // saturated positive side
-    if (i0 - j0 + 127 > rsn) hi = jb + 1;       // not saturated on the negative side
-  }
+  int lo = ((i0 - 127 - rsp) >> 7) + 1;
+  int hi = -((rsn - i0 - 127) >> 7);
+  lo = lo < 0 ? 0 : (lo > nkb ? nkb : lo);
+  hi = hi < 0 ? 0 : (hi > nkb ? nkb : hi);
   *jlo = lo;
   *jhi = hi > lo ? hi : lo;
 }

@@ -87,8 +87,14 @@ struct Smem {
   static constexpr uint32_t bars = red + 4 * 128 * 4;
   static constexpr int kBars = 19;
   static constexpr uint32_t misc = bars + kBars * 8;   // abort flag, TMEM slot
-  static constexpr uint32_t bytes = misc + 16;
+  static constexpr uint32_t next = (misc + 16 + 15) & ~15u;  // int4: the next work item
+  static constexpr uint32_t bytes = next + 16;
 };
+// 16-byte vector accesses: the key-bias row (float4), the next item (int4) and
+// the skew buffers' rows
+static_assert(Smem::col % 16 == 0 && Smem::next % 16 == 0 && Smem::cw % 16 == 0 &&
+                  Smem::pw % 16 == 0,
+              "16-byte aligned vector regions");
 static_assert(Smem::bytes <= 227 * 1024, "near-tile shared memory");
 static_assert(Smem::bars % 8 == 0 && Smem::e % 1024 == 0, "alignment");
 
@@ -230,8 +236,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++pv_n;
       };
 
+      // the next work item is read one item ahead
+      int4 next_item = blockIdx.x < n_items ? p.items[blockIdx.x] : make_int4(0, 0, 0, 0);
       for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
-        const int4 item = p.items[it];
+        const int4 item = next_item;
+        if (it + (int)gridDim.x < n_items) next_item = p.items[it + gridDim.x];
         const int start = item.x, n = item.y, h = item.z, ib = item.w;
         const int nkb = (n + kTile - 1) / kTile;
         int jlo, jhi;
@@ -391,8 +400,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr uint32_t kAll = 0xffffffffu;
     bool alive = true;
     uint32_t gt = 0;  // tiles of this CTA so far (each has five products and one P.V)
+    // Thread 0 reads the next work item during the current one and leaves it in
+    // shared memory (published by the last barrier of the item).
+    int4* s_next = reinterpret_cast<int4*>(sm + SL::next);
     for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
-      const int4 item = p.items[it];
+      const int4 item = it == (int)blockIdx.x ? p.items[it] : *s_next;
+      const int4 ahead = ctid == 0 && it + (int)gridDim.x < n_items ? p.items[it + gridDim.x]
+                                                                      : make_int4(0, 0, 0, 0);
       const int start = item.x, n = item.y, h = item.z, i0 = item.w * kTile;
       const int nkb = (n + kTile - 1) / kTile;
       int jlo, jhi;
@@ -537,7 +551,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         d4[0] = make_uint4(w[0], w[1], w[2], w[3]);
         d4[1] = make_uint4(w[4], w[5], w[6], w[7]);
       }
-      // sRed and sCol are rewritten by the next item only after this barrier
+      if (ctid == 0) *s_next = ahead;
+      // sRed, sCol and the next item are rewritten / read only after this barrier
       named_sync(1, kComputeThreads);
     }
   }
