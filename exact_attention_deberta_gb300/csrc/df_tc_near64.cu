@@ -40,6 +40,15 @@
 //               products, gather, run the online softmax and write P into TMEM;
 //   warp 16     control: TMA loads (Q, K, V, the diagonal-table halves
 //               through a two-buffer ring) and every tcgen05.mma, one thread.
+// No barrier of the whole CTA inside a tile: the compute warps hand the skew
+// buffers over by lane quarter.  Quarter q's drains fill the rows 32 q .. +31
+// of Cw and the key columns 32 q .. +31 of Pw; a warp gathers from its own
+// quarter's rows and its column group's keys, so it waits for those two
+// quarters' drains only, and a quarter drains the next tile once the gathers
+// that read its rows and its columns are done.  The row maximum and sum are
+// exchanged between the four warps of a row quarter only.
+// A masked or absent key is masked through its P row: the P drains add the
+// key's bias (0 or -inf) to every position term they store for it.
 // The compute warps do not spill (only the control thread keeps a few
 // counters in local memory), so no destination register of an asynchronous
 // tensor-memory load is spilled or reused before its wait.
@@ -82,17 +91,15 @@ struct Smem {
   static constexpr uint32_t e = v + kBoxBytes;         // [2] diagonal-table halves
   static constexpr uint32_t cw = e + 2 * kBoxBytes;    // fp32 [128][132]
   static constexpr uint32_t pw = cw + 128 * kRowB;     // fp32 [128][132]
-  static constexpr uint32_t col = pw + 128 * kRowB;    // float [128] key bias
-  static constexpr uint32_t red = col + 128 * 4;       // float [4][128]
-  static constexpr uint32_t bars = red + 4 * 128 * 4;
-  static constexpr int kBars = 19;
+  static constexpr uint32_t red = pw + 128 * kRowB;    // float [3][4][128]: row max / sum exchange
+  static constexpr uint32_t bars = red + 3 * 4 * 128 * 4;
+  static constexpr int kBars = 30;
   static constexpr uint32_t misc = bars + kBars * 8;   // abort flag, TMEM slot
-  static constexpr uint32_t next = (misc + 16 + 15) & ~15u;  // int4: the next work item
-  static constexpr uint32_t bytes = next + 16;
+  static constexpr uint32_t next = (misc + 16 + 15) & ~15u;  // int4 [2]: the next work item
+  static constexpr uint32_t bytes = next + 32;
 };
-// 16-byte vector accesses: the key-bias row (float4), the next item (int4) and
-// the skew buffers' rows
-static_assert(Smem::col % 16 == 0 && Smem::next % 16 == 0 && Smem::cw % 16 == 0 &&
+// 16-byte vector accesses: the next item (int4) and the skew buffers' rows
+static_assert(Smem::next % 16 == 0 && Smem::cw % 16 == 0 &&
                   Smem::pw % 16 == 0,
               "16-byte aligned vector regions");
 static_assert(Smem::bytes <= 227 * 1024, "near-tile shared memory");
@@ -132,7 +139,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* sK = sm + SL::k;
   uint8_t* sV = sm + SL::v;
   uint8_t* sE = sm + SL::e;
-  float* sCol = reinterpret_cast<float*>(sm + SL::col);
   float* sRed = reinterpret_cast<float*>(sm + SL::red);
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + SL::bars);
   uint64_t* q_full = bars + 0;
@@ -147,6 +153,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* p_full = bars + 15;     // P of the tile in TMEM (one arrival per compute warp)
   uint64_t* pv_done = bars + 16;    // P.V of the tile done (O, P and V free)
   uint64_t* bar_end = bars + 17;    // every MMA done (exit)
+  // Tile hand-offs between compute warps, by lane quarter q (rows 32 q .. +31,
+  // keys 32 q .. +31): the quarter's drains are stored (its C rows and P
+  // columns); the gathers of the quarter's rows are done; the gathers of its
+  // key columns are done.  One phase per tile; every thread of the four
+  // contributing warps arrives.
+  uint64_t* drained = bars + 18;    // [4]
+  uint64_t* row_read = bars + 22;   // [4]
+  uint64_t* col_read = bars + 26;   // [4]
   volatile int* s_abort = reinterpret_cast<volatile int*>(sm + SL::misc);
   uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + SL::misc + 4);
 
@@ -155,6 +169,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int b = 0; b < SL::kBars; ++b) mbar_init(bars + b, 1);
     for (int s = 0; s < 3; ++s) mbar_init(slot_empty + s, kComputeWarps);
     mbar_init(p_full, kComputeWarps);
+    for (int q = 0; q < 4; ++q) {
+      mbar_init(drained + q, 128);
+      mbar_init(row_read + q, 128);
+      mbar_init(col_read + q, 128);
+    }
     *s_abort = 0;
     mbar_fence_init();
   }
@@ -343,7 +362,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // t = 128 half + c.
     // (Addresses wrap modulo 2^32 where a run starts outside the row; only the
     // stores inside it are made.)
-    auto store_run = [&](int kind, int first, const uint32_t* r) {
+    auto store_run = [&](int kind, int first, const uint32_t* r, float kbias) {
       const int t0 = 128 * (kind >> 1) + 8 * first;
       if ((kind & 1) == 0) {
         // C lane rho: diagonal t0 + e goes to key j = rho + 127 - t0 - e of row rho
@@ -351,17 +370,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t a0 = cw + kRowB * rho + 4u * (uint32_t)j0;
 #pragma unroll
         for (int e = 0; e < 8; ++e)
-          if ((unsigned)(j0 - e) < 128u) sts32(a0 - 4u * e, r[e]);
+          sts32_below(a0 - 4u * e, r[e], (uint32_t)(j0 - e), 128u);
       } else {
         // P lane rho (key): diagonal t0 + e goes to row i = t0 + e - 127 + rho, key rho
         const int i0 = t0 - 127 + rho;
         const uint32_t a0 = pw + kRowB * (uint32_t)i0 + 4u * rho;
 #pragma unroll
         for (int e = 0; e < 8; ++e)
-          if ((unsigned)(i0 + e) < 128u) sts32(a0 + kRowB * e, r[e]);
+          sts32_below(a0 + kRowB * e, __float_as_uint(__uint_as_float(r[e]) + kbias), (uint32_t)(i0 + e), 128u);
       }
     };
-    auto drain = [&](int kind, uint32_t slot_col) {
+    auto drain = [&](int kind, uint32_t slot_col, float kbias) {
       int first, count;
       drain_run(kind, qd, g, &first, &count);
       const uint32_t src = tmem + slot_col + lane_off + 8u * first;
@@ -370,7 +389,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld32(src, r);
         tmem_ld_wait(r);
 #pragma unroll
-        for (int part = 0; part < 4; ++part) store_run(kind, first + part, r + 8 * part);
+        for (int part = 0; part < 4; ++part) store_run(kind, first + part, r + 8 * part, kbias);
       } else if (count >= 2) {
         uint32_t r[16];
         tmem_ld16(src, r);
@@ -379,17 +398,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld8(src + 16, r8);
           tmem_ld_wait(r);
           tmem_ld_wait(r8);
-          store_run(kind, first + 2, r8);
+          store_run(kind, first + 2, r8, kbias);
         } else {
           tmem_ld_wait(r);
         }
-        store_run(kind, first, r);
-        store_run(kind, first + 1, r + 8);
+        store_run(kind, first, r, kbias);
+        store_run(kind, first + 1, r + 8, kbias);
       } else {
         uint32_t r[8];
         tmem_ld8(src, r);
         tmem_ld_wait(r);
-        store_run(kind, first, r);
+        store_run(kind, first, r, kbias);
       }
     };
 
@@ -400,68 +419,81 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr uint32_t kAll = 0xffffffffu;
     bool alive = true;
     uint32_t gt = 0;  // tiles of this CTA so far (each has five products and one P.V)
-    // Thread 0 reads the next work item during the current one and leaves it in
-    // shared memory (published by the last barrier of the item).
-    int4* s_next = reinterpret_cast<int4*>(sm + SL::next);
-    for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
-      const int4 item = it == (int)blockIdx.x ? p.items[it] : *s_next;
-      const int4 ahead = ctid == 0 && it + (int)gridDim.x < n_items ? p.items[it + gridDim.x]
-                                                                      : make_int4(0, 0, 0, 0);
+    // Thread 0 copies the next work item into shared memory while the current
+    // one runs (an asynchronous copy: no register is held for it); the last
+    // barrier of the item publishes it.  Two slots by item parity: the copy for
+    // item c + 1 must not overwrite the slot that item c is still being read
+    // from.
+    int4* s_next = reinterpret_cast<int4*>(sm + SL::next);  // [2]
+    uint32_t ic = 0;  // items of this CTA so far
+    for (int it = blockIdx.x; it < n_items; it += gridDim.x, ++ic) {
+      const int4 item = it == (int)blockIdx.x ? p.items[it] : s_next[ic & 1];
+      if (ctid == 0 && it + (int)gridDim.x < n_items) {
+        // the other slot was last read at the start of item c - 1, before that
+        // item's last barrier
+        asm volatile("cp.async.ca.shared.global [%0], [%1], 16;\n\tcp.async.commit_group;" ::"r"(
+                         smem_u32(s_next + ((ic + 1) & 1))),
+                     "l"(p.items + it + gridDim.x)
+                     : "memory");
+      }
       const int start = item.x, n = item.y, h = item.z, i0 = item.w * kTile;
       const int nkb = (n + kTile - 1) / kTile;
       int jlo, jhi;
       near_block_range(i0, nkb, rsp, rsn, &jlo, &jhi);
       const int nt = jhi - jlo;
-      if (nt <= 0) continue;
-      const bool has_far = jlo > 0 || jhi < nkb;
-      const int i = i0 + rho;
-      const size_t tok = (size_t)start + i;
-      const bool row_in = i < n;
-      const bool row_out = row_in && p.keybias[tok] == 0.f;
-      auto fetch_col = [&](int t) -> float {
-        const int j = (jlo + t) * kTile + ctid;
-        return ctid < kTile ? (j < n ? p.keybias[(size_t)start + j] : -INFINITY) : 0.f;
-      };
-      if (ctid < kTile) sCol[ctid] = fetch_col(0);
-      float col_next = nt > 1 ? fetch_col(1) : 0.f;
+      if (nt <= 0) {  // (no item of the plan is empty) keep the next-item copy ordered
+        if (ctid == 0) asm volatile("cp.async.wait_all;" ::: "memory");
+        named_sync(1, kComputeThreads);
+        continue;
+      }
       float m_run = -INFINITY, l_run = 0.f;  // l_run: this warp's 32 columns only
 
       for (int t = 0; t < nt; ++t, ++gt) {
         const uint32_t x0 = 5u * gt;
+        // key bias (0, or -inf for a masked or absent key) of this lane's P row,
+        // key rho of the tile: the P drains add it to every position term of that
+        // key, which masks the key in every score row
+        const int jk = (jlo + t) * kTile + rho;
+        const float kbias = jk < n ? p.keybias[(size_t)start + jk] : -INFINITY;
+        // the quarter's C rows and P columns are free once the previous tile's
+        // gathers that read them are done
+        if (gt > 0)
+          alive = __all_sync(kAll, alive && wait_ph(row_read + qd, (gt - 1) & 1, 288) &&
+                                       wait_ph(col_read + qd, (gt - 1) & 1, 289));
         // ---- the four position products, drained in ring order
 #pragma unroll 1
         for (int kind = 0; kind < 4; ++kind) {
           const uint32_t x = x0 + kind, s = x % 3;
           alive = __all_sync(kAll, alive && wait_ph(slot_full + s, (x / 3) & 1, 290 + kind));
           tc_fence_after();
-          if (alive) drain(kind, s * kSlotCols);
+          if (alive) drain(kind, s * kSlotCols, kbias);
           tc_fence_before();
           __syncwarp();
           if (alive && lane == 0) mbar_arrive(slot_empty + s);
         }
-        named_sync(1, kComputeThreads);  // every drain of the tile is visible
+        if (alive) mbar_arrive(drained + qd);  // every lane: its stores are published
         // ---- S, then the position terms of this thread's 32 elements
         float x[32];
         {
           const uint32_t xs = x0 + 4, s = xs % 3;
           alive = __all_sync(kAll, alive && wait_ph(slot_full + s, (xs / 3) & 1, 294));
           tc_fence_after();
-          uint32_t r[32];
-          tmem_ld32(tmem + s * kSlotCols + lane_off + 32 * g, r);  // whole warp; unused unless alive
-          tmem_ld_wait(r);
+#pragma unroll
+          for (int hf = 0; hf < 2; ++hf) {
+            uint32_t r[16];
+            tmem_ld16(tmem + s * kSlotCols + lane_off + 32 * g + 16 * hf, r);  // whole warp
+            tmem_ld_wait(r);
+#pragma unroll
+            for (int e = 0; e < 16; ++e) x[16 * hf + e] = __uint_as_float(r[e]) * ks;
+          }
           tc_fence_before();
           __syncwarp();
           if (alive && lane == 0) mbar_arrive(slot_empty + s);
-          const float* cb = sCol + 32 * g;
-#pragma unroll
-          for (int e = 0; e < 32; e += 4) {
-            const float4 c4 = *reinterpret_cast<const float4*>(cb + e);
-            x[e + 0] = fmaf(__uint_as_float(r[e + 0]), ks, c4.x);
-            x[e + 1] = fmaf(__uint_as_float(r[e + 1]), ks, c4.y);
-            x[e + 2] = fmaf(__uint_as_float(r[e + 2]), ks, c4.z);
-            x[e + 3] = fmaf(__uint_as_float(r[e + 3]), ks, c4.w);
-          }
         }
+        // the C row of this thread (quarter qd) and the P columns of its keys
+        // (quarter g) are stored
+        alive = __all_sync(kAll, alive && wait_ph(drained + qd, gt & 1, 297) &&
+                                     (g == qd || wait_ph(drained + g, gt & 1, 298)));
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
           const uint4 c4 = lds128(gC + 16u * k), p4 = lds128(gP + 16u * k);
@@ -472,14 +504,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
 
         // ---- online softmax (log2 units); row maximum over the four column groups
+        if (alive) {  // every lane: its reads of Cw row rho and Pw columns 32 g .. +31 are done
+          mbar_arrive(row_read + qd);
+          mbar_arrive(col_read + g);
+        }
         float mt = -INFINITY;
 #pragma unroll
         for (int e = 0; e < 32; ++e) mt = fmaxf(mt, x[e]);
-        sRed[g * 128 + rho] = mt;
-        named_sync(1, kComputeThreads);  // also: every gather of the tile is done
-        if (ctid < kTile && t + 1 < nt) sCol[ctid] = col_next;
-        if (t + 2 < nt) col_next = fetch_col(t + 2);
-        mt = fmaxf(fmaxf(sRed[rho], sRed[128 + rho]), fmaxf(sRed[256 + rho], sRed[384 + rho]));
+        float* red = sRed + 512 * (gt & 1);
+        red[g * 128 + rho] = mt;
+        named_sync(2 + qd, 128);  // the four warps of the row quarter
+        mt = fmaxf(fmaxf(red[rho], red[128 + rho]), fmaxf(red[256 + rho], red[384 + rho]));
         // Re-base only when the maximum grows by more than 2^8 (exact: numerator and
         // denominator share the stale base).  All four warps of a row agree.
         float scale = 1.f;
@@ -523,13 +558,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       // ---- epilogue: final rows, or the partial state for the far-tile kernel
       alive = __all_sync(kAll, alive && wait_ph(pv_done, (gt - 1) & 1, 296));
       tc_fence_after();
-      sRed[g * 128 + rho] = l_run;
-      named_sync(1, kComputeThreads);
-      const float l_tot = (sRed[rho] + sRed[128 + rho]) + (sRed[256 + rho] + sRed[384 + rho]);
+      float* red = sRed + 1024;
+      red[g * 128 + rho] = l_run;
+      named_sync(2 + qd, 128);
+      const float l_tot = (red[rho] + red[128 + rho]) + (red[256 + rho] + red[384 + rho]);
       uint32_t r[16];
       tmem_ld16(tO + lane_off + 16 * g, r);
       tmem_ld_wait(r);
       const bool store = alive && *s_abort == 0;
+      const bool has_far = jlo > 0 || jhi < nkb;
+      const int i = i0 + rho;
+      const size_t tok = (size_t)start + i;
+      const bool row_in = i < n;
       if (has_far) {
         if (row_in && store) {
           float* dst = partial_o(p) + (tok * p.H + h) * kD + 16 * g;
@@ -538,7 +578,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             *reinterpret_cast<uint4*>(dst + e) = make_uint4(r[e], r[e + 1], r[e + 2], r[e + 3]);
           if (g == 0) partial_ml(p)[tok * p.H + h] = make_float2(m_run, l_tot);
         }
-      } else if (row_out && store) {
+      } else if (row_in && store && p.keybias[tok] == 0.f) {
         const float inv = l_tot > 0.f ? 1.f / l_tot : 0.f;
         uint32_t w[8];
 #pragma unroll
@@ -551,8 +591,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         d4[0] = make_uint4(w[0], w[1], w[2], w[3]);
         d4[1] = make_uint4(w[4], w[5], w[6], w[7]);
       }
-      if (ctid == 0) *s_next = ahead;
-      // sRed, sCol and the next item are rewritten / read only after this barrier
+      if (ctid == 0) asm volatile("cp.async.wait_all;" ::: "memory");
+      // the next item is read, and the sum exchange rewritten, only after this barrier
       named_sync(1, kComputeThreads);
     }
   }

@@ -347,6 +347,16 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
 __device__ __forceinline__ void sts32(uint32_t addr, uint32_t v) {
   asm volatile("st.shared.b32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }
+// Store made only when idx < bound (unsigned): a predicated store, so that a
+// warp whose lanes disagree does not branch.
+__device__ __forceinline__ void sts32_below(uint32_t addr, uint32_t v, uint32_t idx, uint32_t bound) {
+  asm volatile(
+      "{\n\t.reg .pred q;\n\t"
+      "setp.lt.u32 q, %2, %3;\n\t"
+      "@q st.shared.b32 [%0], %1;\n\t}\n" ::"r"(addr),
+      "r"(v), "r"(idx), "r"(bound)
+      : "memory");
+}
 __device__ __forceinline__ void sts16_lo(uint32_t addr, uint32_t v) {
   asm volatile("st.shared.b16 [%0], %1;" ::"r"(addr), "h"((uint16_t)(v & 0xFFFFu)) : "memory");
 }
