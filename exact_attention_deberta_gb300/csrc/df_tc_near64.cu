@@ -71,7 +71,7 @@ constexpr int kD = 64;
 constexpr int kTile = 128;
 constexpr int kComputeWarps = 16;
 constexpr int kComputeThreads = kComputeWarps * 32;
-constexpr int kThreads = kComputeThreads + 32;
+constexpr int kThreads = kComputeThreads + 64;  // + the MMA warp and the load warp
 constexpr uint32_t kRowW = 132;           // words per Cw / Pw row: 128 keys + 4 of padding
 constexpr uint32_t kRowB = kRowW * 4;     // 528 bytes
 static_assert((kRowW + 1) % 2 == 1 && (kRowB / 16) % 2 == 1, "conflict-free drains and gathers");
@@ -79,21 +79,24 @@ static_assert((kRowW + 1) % 2 == 1 && (kRowB / 16) % 2 == 1, "conflict-free drai
 // Tensor-memory columns.
 constexpr uint32_t kSlots = 3, kSlotCols = 128;
 constexpr uint32_t kColO = kSlots * kSlotCols;  // 384
-constexpr uint32_t kColP = kColO + kD;          // 448
+constexpr uint32_t kColQ = kColO + kD;          // 448: Q (16-bit pairs), the A operand of C0, C1, S
 static_assert(tmem_region_fits(0, kSlots * kSlotCols, kColO), "product ring below O");
-static_assert(tmem_region_fits(kColO, kD, kColP), "O below P");
-static_assert(tmem_region_fits(kColP, kTile / 2, 512), "P (16-bit pairs) inside 512 columns");
+static_assert(tmem_region_fits(kColO, kD, kColQ), "O below Q");
+static_assert(tmem_region_fits(kColQ, kD / 2, 512), "Q inside 512 columns");
+// P of a tile (16-bit pairs) overwrites its S: column group c's 32 keys at
+// columns 32 c .. 32 c + 15 of the S slot
+static_assert(32 * (kTile / 32 - 1) + 16 <= kSlotCols, "P inside the S slot");
+constexpr uint32_t kRing = 3;                   // diagonal-table halves in flight
 
 struct Smem {
-  static constexpr uint32_t q = 0;                     // Q tile
-  static constexpr uint32_t k = q + kBoxBytes;         // K tile
+  static constexpr uint32_t k = 0;                     // K tile
   static constexpr uint32_t v = k + kBoxBytes;         // V tile
-  static constexpr uint32_t e = v + kBoxBytes;         // [2] diagonal-table halves
-  static constexpr uint32_t cw = e + 2 * kBoxBytes;    // fp32 [128][132]
+  static constexpr uint32_t e = v + kBoxBytes;         // [kRing] diagonal-table halves
+  static constexpr uint32_t cw = e + kRing * kBoxBytes;  // fp32 [128][132]
   static constexpr uint32_t pw = cw + 128 * kRowB;     // fp32 [128][132]
   static constexpr uint32_t red = pw + 128 * kRowB;    // float [3][4][128]: row max / sum exchange
   static constexpr uint32_t bars = red + 3 * 4 * 128 * 4;
-  static constexpr int kBars = 30;
+  static constexpr int kBars = 31;
   static constexpr uint32_t misc = bars + kBars * 8;   // abort flag, TMEM slot
   static constexpr uint32_t next = (misc + 16 + 15) & ~15u;  // int4 [2]: the next work item
   static constexpr uint32_t bytes = next + 32;
@@ -135,32 +138,30 @@ __global__ void __launch_bounds__(kThreads, 1)
     return;
   }
   uint8_t* sm = smem_raw;
-  uint8_t* sQ = sm + SL::q;
   uint8_t* sK = sm + SL::k;
   uint8_t* sV = sm + SL::v;
   uint8_t* sE = sm + SL::e;
   float* sRed = reinterpret_cast<float*>(sm + SL::red);
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + SL::bars);
-  uint64_t* q_full = bars + 0;
-  uint64_t* q_empty = bars + 1;     // every MMA reading Q done (last S of the item)
-  uint64_t* k_full = bars + 2;
-  uint64_t* k_empty = bars + 3;     // S of the tile done (its last reader of K)
-  uint64_t* v_full = bars + 4;
-  uint64_t* e_full = bars + 5;      // [2]
-  uint64_t* e_empty = bars + 7;     // [2] the product that read the half is done
-  uint64_t* slot_full = bars + 9;   // [3] product in the slot computed
-  uint64_t* slot_empty = bars + 12; // [3] product drained (one arrival per compute warp)
-  uint64_t* p_full = bars + 15;     // P of the tile in TMEM (one arrival per compute warp)
-  uint64_t* pv_done = bars + 16;    // P.V of the tile done (O, P and V free)
-  uint64_t* bar_end = bars + 17;    // every MMA done (exit)
+  uint64_t* q_full = bars + 0;      // Q of the item in TMEM (one arrival per compute warp)
+  uint64_t* k_full = bars + 1;
+  uint64_t* k_empty = bars + 2;     // S of the tile done (its last reader of K)
+  uint64_t* v_full = bars + 3;
+  uint64_t* e_full = bars + 4;      // [kRing]
+  uint64_t* e_empty = bars + 7;     // [kRing] the product that read the half is done
+  uint64_t* slot_full = bars + 10;  // [3] product in the slot computed
+  uint64_t* slot_empty = bars + 13; // [3] product drained (one arrival per compute warp)
+  uint64_t* p_full = bars + 16;     // P of the tile in TMEM (one arrival per compute warp)
+  uint64_t* pv_done = bars + 17;    // P.V of the tile done (O, P and V free)
+  uint64_t* bar_end = bars + 18;    // every MMA done (exit)
   // Tile hand-offs between compute warps, by lane quarter q (rows 32 q .. +31,
   // keys 32 q .. +31): the quarter's drains are stored (its C rows and P
   // columns); the gathers of the quarter's rows are done; the gathers of its
   // key columns are done.  One phase per tile; every thread of the four
   // contributing warps arrives.
-  uint64_t* drained = bars + 18;    // [4]
-  uint64_t* row_read = bars + 22;   // [4]
-  uint64_t* col_read = bars + 26;   // [4]
+  uint64_t* drained = bars + 19;    // [4]
+  uint64_t* row_read = bars + 23;   // [4]
+  uint64_t* col_read = bars + 27;   // [4]
   volatile int* s_abort = reinterpret_cast<volatile int*>(sm + SL::misc);
   uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + SL::misc + 4);
 
@@ -169,6 +170,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int b = 0; b < SL::kBars; ++b) mbar_init(bars + b, 1);
     for (int s = 0; s < 3; ++s) mbar_init(slot_empty + s, kComputeWarps);
     mbar_init(p_full, kComputeWarps);
+    mbar_init(q_full, kComputeWarps);
     for (int q = 0; q < 4; ++q) {
       mbar_init(drained + q, 128);
       mbar_init(row_read + q, 128);
@@ -185,72 +187,68 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tslot;
-  const uint32_t tO = tmem + kColO, tP = tmem + kColP;
+  const uint32_t tO = tmem + kColO, tQ = tmem + kColQ;
 
   const int n_items = p.hdr->n_items;
   const int rsp = p.hdr->r_sat_pos, rsn = p.hdr->r_sat_neg;
   const unsigned long long budget = p.wait_budget;
   df_ws_header* hdr = p.hdr;
 
+  auto wt = [&](uint64_t* bar, uint32_t parity, int where) {
+    return wait_or_abort(bar, parity, budget, s_abort, hdr, where);
+  };
   if (warp == kComputeWarps) {
-    // ================================================================ control
+    // ================================================================ MMA issue
     if (lane == 0) {
-      tma_prefetch_desc(&maps.q);
-      tma_prefetch_desc(&maps.k);
-      tma_prefetch_desc(&maps.v);
-      tma_prefetch_desc(&maps.dpk);
-      tma_prefetch_desc(&maps.dpq);
-      auto wt = [&](uint64_t* bar, uint32_t parity, int where) {
-        return wait_or_abort(bar, parity, budget, s_abort, hdr, where);
-      };
-      // Loads and products actually issued.  The n-th load or commit on a
-      // barrier completes its phase n, parity n & 1.
-      uint32_t q_n = 0, k_n = 0, v_n = 0, e_n = 0, ec_n = 0, pp = 0, pv_n = 0;
+      // Products and P.V issued, tables consumed.  The n-th commit on a barrier
+      // completes its phase n, parity n & 1.
+      uint32_t ec_n = 0, pp = 0, pv_n = 0, k_n = 0, v_n = 0, q_n = 0, g_n = 0;
       bool have_prev = false, prev_first = false;
-      const uint64_t dq = kmajor_desc(sQ, 0), dk = kmajor_desc(sK, 0);
+      const uint64_t dk = kmajor_desc(sK, 0);
       const uint32_t dv_addr = smem_u32(sV);
 
-      // Diagonal-table half into the ring buffer e_n & 1, once the product that
-      // read that buffer before (two loads back) is done.
-      auto e_load = [&](const CUtensorMap* map, int head, int row, int where) {
-        const uint32_t b = e_n & 1;
-        bool ok = !*s_abort;
-        if (ok && e_n >= 2) ok = wt(e_empty + b, ((e_n >> 1) - 1) & 1, where);
-        if (ok) {
-          mbar_expect_tx(e_full + b, kBoxBytes);
-          tma_load_2d(sE + b * kBoxBytes, map, head * kD, row, e_full + b);
-          ++e_n;
-        }
-      };
-      // Position product `kind` (0 C0, 1 P0, 2 C1, 3 P1) into the next ring slot.
+      // Position product `kind` (0 C0, 1 P0, 2 C1, 3 P1) into the next ring slot:
+      // C = Q.table (Q from tensor memory), P = K.table.
       auto issue_pos = [&](int kind, int where) {
-        const uint32_t x = pp, s = x % 3, b = ec_n & 1;
+        const uint32_t x = pp, s = x % 3, b = ec_n % kRing;
         bool ok = !*s_abort;
         if (ok && x >= 3) ok = wt(slot_empty + s, ((x / 3) - 1) & 1, where);
-        ok = wt(e_full + b, (ec_n >> 1) & 1, where + 1) && ok;
+        // C1 takes the slot of the previous tile's S, where P lived until its
+        // P.V was done
+        if (ok && kind == 2 && g_n > 0) ok = wt(pv_done, (g_n - 1) & 1, where + 2);
+        ok = wt(e_full + b, (ec_n / kRing) & 1, where + 1) && ok;
         if (!ok) return;
         tc_fence_after();
-        const uint64_t da = (kind & 1) ? dk : dq;
         const uint64_t db = kmajor_desc(sE + b * kBoxBytes, 0);
         const uint32_t d = tmem + s * kSlotCols;
+        if (kind & 1) {
 #pragma unroll
-        for (int k = 0; k < kD / 16; ++k)
-          mma_ss(d, da + kmajor_step(k), db + kmajor_step(k), kIdescQK, k > 0);
+          for (int k = 0; k < kD / 16; ++k)
+            mma_ss(d, dk + kmajor_step(k), db + kmajor_step(k), kIdescQK, k > 0);
+        } else {
+#pragma unroll
+          for (int k = 0; k < kD / 16; ++k)
+            mma_ts(d, tQ + 8 * k, db + kmajor_step(k), kIdescQK, k > 0 ? 1u : 0u);
+        }
         mma_commit(slot_full + s);
         mma_commit(e_empty + b);
         ++pp;
         ++ec_n;
       };
-      // O (+)= P.V of the previous tile.
+      // O (+)= P.V of the previous tile; P is in that tile's S slot, warp
+      // column group c at columns 32 c .. 32 c + 15 (16-bit pairs).
       auto issue_pv = [&](bool first, int where) {
         bool ok = wt(p_full, pv_n & 1, where);
-        ok = wt(v_full, (v_n - 1) & 1, where + 1) && ok;
+        ok = wt(v_full, v_n & 1, where + 1) && ok;
         if (!ok) return;
+        ++v_n;
         tc_fence_after();
+        const uint32_t ps = tmem + ((5u * pv_n + 4u) % 3u) * kSlotCols;
         const uint64_t dv = vtile_desc(dv_addr, 0);
 #pragma unroll
         for (int k = 0; k < kTile / 16; ++k)
-          mma_ts(tO, tP + 8 * k, dv + vtile_step(k), kIdescPV, (!first || k > 0) ? 1u : 0u);
+          mma_ts(tO, ps + 32 * (k >> 1) + 8 * (k & 1), dv + vtile_step(k), kIdescPV,
+                 (!first || k > 0) ? 1u : 0u);
         mma_commit(pv_done);
         ++pv_n;
       };
@@ -260,53 +258,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
         const int4 item = next_item;
         if (it + (int)gridDim.x < n_items) next_item = p.items[it + gridDim.x];
-        const int start = item.x, n = item.y, h = item.z, ib = item.w;
+        const int n = item.y, ib = item.w;
         const int nkb = (n + kTile - 1) / kTile;
         int jlo, jhi;
         near_block_range(ib * kTile, nkb, rsp, rsn, &jlo, &jhi);
         const int nt = jhi - jlo;
         if (nt <= 0) continue;
-        // Q of this item, once every MMA of the previous item that read Q is done
-        if (q_n > 0) wt(q_empty, (q_n - 1) & 1, 300);
-        if (!*s_abort) {
-          mbar_expect_tx(q_full, kBoxBytes);
-          tma_load_2d(sQ, &maps.q, h * kD, start + ib * kTile, q_full);
-          ++q_n;
-        }
         for (int t = 0; t < nt; ++t) {
-          const int kb = jlo + t;
-          int drow = (ib - kb - p.diag_m0) * 256;   // first row of the tile's diagonal tables
-          if (ib - kb - p.diag_m0 < 0 || ib - kb - p.diag_m0 >= p.n_diag) {
-            raise_device_error(hdr, DF_ERR_INVALID_ARG, 261);
-            drow = 0;
+          // The previous tile's P.V goes first at an item's first tile: the
+          // compute warps store this item's Q once that P.V is done.
+          if (t == 0) {
+            if (have_prev) issue_pv(prev_first, 320);
+            wt(q_full, q_n & 1, 304);
+            ++q_n;
           }
-          e_load(&maps.dpk, h, drow, 301);              // C0
-          e_load(&maps.dpq, h, drow, 302);              // P0
-          // K of the tile, once S of the previous tile (its last reader) is done
-          if (k_n > 0) wt(k_empty, (k_n - 1) & 1, 303);
-          if (!*s_abort) {
-            mbar_expect_tx(k_full, kBoxBytes);
-            tma_load_2d(sK, &maps.k, h * kD, start + kb * kTile, k_full);
-            ++k_n;
-          }
-          if (t == 0) wt(q_full, (q_n - 1) & 1, 304);
           issue_pos(0, 310);
-          wt(k_full, (k_n - 1) & 1, 305);
+          wt(k_full, k_n & 1, 305);
+          ++k_n;
           issue_pos(1, 312);
-          e_load(&maps.dpk, h, drow + 128, 306);        // C1, after C0 is done
-          e_load(&maps.dpq, h, drow + 128, 307);        // P1, after P0 is done
-          // C1 takes the slot of the previous S, free once the softmax has read it;
-          // P1 the slot of C0, free once C0 is drained (after that softmax ends)
+          if (t > 0) issue_pv(prev_first, 320);
           issue_pos(2, 314);
-          if (have_prev) issue_pv(prev_first, 320);
           issue_pos(3, 316);
-          // V of the tile, once the previous P.V is done
-          if (v_n > 0) wt(pv_done, (pv_n - 1) & 1, 308);
-          if (!*s_abort) {
-            mbar_expect_tx(v_full, kBoxBytes);
-            tma_load_2d(sV, &maps.v, h * kD, start + kb * kTile, v_full);
-            ++v_n;
-          }
           // S = Q.K^T into the next slot
           {
             const uint32_t x = pp, s = x % 3;
@@ -317,30 +289,102 @@ __global__ void __launch_bounds__(kThreads, 1)
               const uint32_t d = tmem + s * kSlotCols;
 #pragma unroll
               for (int k = 0; k < kD / 16; ++k)
-                mma_ss(d, dq + kmajor_step(k), dk + kmajor_step(k), kIdescQK, k > 0);
+                mma_ts(d, tQ + 8 * k, dk + kmajor_step(k), kIdescQK, k > 0 ? 1u : 0u);
               mma_commit(slot_full + s);
               mma_commit(k_empty);
-              if (t == nt - 1) mma_commit(q_empty);
               ++pp;
             }
           }
+          ++g_n;
           have_prev = true;
           prev_first = t == 0;
         }
       }
       if (have_prev) issue_pv(prev_first, 322);
-      // no copy or MMA may still be in flight when the CTA leaves
-      if (q_n) mbar_wait(q_full, (q_n - 1) & 1, kDrainBudget);
-      if (k_n) mbar_wait(k_full, (k_n - 1) & 1, kDrainBudget);
-      if (v_n) mbar_wait(v_full, (v_n - 1) & 1, kDrainBudget);
-      for (uint32_t b = 0; b < 2; ++b) {
-        if (e_n > b) {
-          const uint32_t x = e_n - 1 - ((e_n - 1 - b) & 1);  // last load into buffer b
-          mbar_wait(e_full + b, (x >> 1) & 1, kDrainBudget);
-        }
-      }
+      // no MMA may still be in flight when the CTA leaves
       mma_commit(bar_end);
       mbar_wait(bar_end, 0, kDrainBudget);
+    }
+  } else if (warp == kComputeWarps + 1) {
+    // ================================================================ loads
+    // One thread issues every TMA load, in the order in which the MMAs free
+    // the buffers (C0, P0, C1, P1 of a tile through a ring of kRing table
+    // buffers; K once the previous S is done; V one tile late, once the P.V
+    // before it is done), so that no load waits behind another's condition.
+    if (lane == 0) {
+      tma_prefetch_desc(&maps.k);
+      tma_prefetch_desc(&maps.v);
+      tma_prefetch_desc(&maps.dpk);
+      tma_prefetch_desc(&maps.dpq);
+      uint32_t k_n = 0, v_n = 0, e_n = 0;
+      int v_head = 0, v_row = 0;
+      bool v_pending = false;
+      auto e_load = [&](const CUtensorMap* map, int head, int row, int where) {
+        const uint32_t b = e_n % kRing;
+        bool ok = !*s_abort;
+        if (ok && e_n >= kRing) ok = wt(e_empty + b, ((e_n / kRing) - 1) & 1, where);
+        if (ok) {
+          mbar_expect_tx(e_full + b, kBoxBytes);
+          tma_load_2d(sE + b * kBoxBytes, map, head * kD, row, e_full + b);
+          ++e_n;
+        }
+      };
+      // V of the previous tile, once the P.V before it is done
+      auto v_load = [&](int where) {
+        bool ok = !*s_abort;
+        if (ok && v_n > 0) ok = wt(pv_done, (v_n - 1) & 1, where);
+        if (ok) {
+          mbar_expect_tx(v_full, kBoxBytes);
+          tma_load_2d(sV, &maps.v, v_head * kD, v_row, v_full);
+          ++v_n;
+        }
+        v_pending = false;
+      };
+      int4 next_item = blockIdx.x < n_items ? p.items[blockIdx.x] : make_int4(0, 0, 0, 0);
+      for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
+        const int4 item = next_item;
+        if (it + (int)gridDim.x < n_items) next_item = p.items[it + gridDim.x];
+        const int start = item.x, n = item.y, h = item.z, ib = item.w;
+        const int nkb = (n + kTile - 1) / kTile;
+        int jlo, jhi;
+        near_block_range(ib * kTile, nkb, rsp, rsn, &jlo, &jhi);
+        const int nt = jhi - jlo;
+        if (nt <= 0) continue;
+        for (int t = 0; t < nt; ++t) {
+          const int kb = jlo + t;
+          int drow = (ib - kb - p.diag_m0) * 256;   // first row of the tile's diagonal tables
+          if (ib - kb - p.diag_m0 < 0 || ib - kb - p.diag_m0 >= p.n_diag) {
+            raise_device_error(hdr, DF_ERR_INVALID_ARG, 261);
+            drow = 0;
+          }
+          e_load(&maps.dpk, h, drow, 301);              // C0
+          e_load(&maps.dpq, h, drow, 302);              // P0
+          if (v_pending) v_load(308);
+          e_load(&maps.dpk, h, drow + 128, 306);        // C1
+          // K of the tile, once S of the previous tile (its last reader) is done
+          bool ok = !*s_abort;
+          if (ok && k_n > 0) ok = wt(k_empty, (k_n - 1) & 1, 303);
+          if (ok) {
+            mbar_expect_tx(k_full, kBoxBytes);
+            tma_load_2d(sK, &maps.k, h * kD, start + kb * kTile, k_full);
+            ++k_n;
+          }
+          e_load(&maps.dpq, h, drow + 128, 307);        // P1
+          v_head = h;
+          v_row = start + kb * kTile;
+          v_pending = true;
+        }
+      }
+      if (v_pending) v_load(309);
+      // no copy may still be in flight when the CTA leaves
+      if (k_n) mbar_wait(k_full, (k_n - 1) & 1, kDrainBudget);
+      if (v_n) mbar_wait(v_full, (v_n - 1) & 1, kDrainBudget);
+      for (uint32_t b = 0; b < kRing; ++b) {
+        if (e_n > b) {
+          const uint32_t x = b + kRing * ((e_n - 1 - b) / kRing);  // last load into buffer b
+          mbar_wait(e_full + b, (x / kRing) & 1, kDrainBudget);
+        }
+      }
     }
   } else {
     // ================================================================ compute
@@ -446,6 +490,27 @@ __global__ void __launch_bounds__(kThreads, 1)
         named_sync(1, kComputeThreads);
         continue;
       }
+      // Q rows of the item into tensor memory, the A operand of C0, C1 and S
+      // (every MMA that read the previous item's Q is done: this warp waited
+      // for that item's last S).  Warp (qd, g) stores columns 8 g .. 8 g + 7
+      // (elements 16 g .. 16 g + 15) of its quarter's rows; rows past the
+      // tensor's end are zero.
+      {
+        const long long row = (long long)start + i0 + rho;
+        uint32_t r[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+        if (row < (long long)p.T) {
+          const uint4* src =
+              reinterpret_cast<const uint4*>(static_cast<const T*>(p.q) + ((size_t)row * p.H + h) * kD + 16 * g);
+          const uint4 a0 = src[0], a1 = src[1];
+          r[0] = a0.x; r[1] = a0.y; r[2] = a0.z; r[3] = a0.w;
+          r[4] = a1.x; r[5] = a1.y; r[6] = a1.z; r[7] = a1.w;
+        }
+        tmem_st8(tQ + lane_off + 8 * g, r);
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (alive && lane == 0) mbar_arrive(q_full);
+      }
       float m_run = -INFINITY, l_run = 0.f;  // l_run: this warp's 32 columns only
 
       for (int t = 0; t < nt; ++t, ++gt) {
@@ -547,7 +612,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             r[e] = BF16 ? pack_bf16x2(p0, p1) : pack_f16x2(p0, p1);
           }
           l_run += acc.x + acc.y;
-          if (alive) tmem_st16(tP + lane_off + 16 * g, r);
+          // P over this warp's own S columns (read above by this warp only)
+          if (alive) tmem_st16(tmem + ((x0 + 4u) % 3u) * kSlotCols + lane_off + 32 * g, r);
         }
         tmem_st_wait();
         tc_fence_before();
