@@ -124,6 +124,22 @@ __device__ __forceinline__ void drain_run(int kind, int qd, int g, int* first, i
   *count = len;
 }
 
+// Skew stores of one 8-diagonal run, each made only when its key (row) lies
+// in 0 .. 127.  C: value e to key j0 - e of the lane's row, i.e. byte offset
+// 4 (7 - e) from the run's lowest key (a7); P: value e to row i0 + e of the
+// lane's key column (offset kRowB e from a0).  The base addresses stay inside
+// the shared window even where a run starts outside the tile.
+__device__ __forceinline__ void st_run_c(uint32_t a7, const uint32_t* r, int j0) {
+#define DFA_C(e) sts32_below_at<4 * (7 - e)>(a7, r[e], (uint32_t)(j0 - (e)), 128u);
+  DFA_C(0) DFA_C(1) DFA_C(2) DFA_C(3) DFA_C(4) DFA_C(5) DFA_C(6) DFA_C(7)
+#undef DFA_C
+}
+__device__ __forceinline__ void st_run_p(uint32_t a0, const uint32_t* v, int i0) {
+#define DFA_P(e) sts32_below_at<(int)kRowB * e>(a0, v[e], (uint32_t)(i0 + (e)), 128u);
+  DFA_P(0) DFA_P(1) DFA_P(2) DFA_P(3) DFA_P(4) DFA_P(5) DFA_P(6) DFA_P(7)
+#undef DFA_P
+}
+
 template <bool BF16>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_near64_kernel(const Problem p, const __grid_constant__ TcMaps maps) {
@@ -388,6 +404,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ================================================================ compute
+    constexpr uint32_t kAll = 0xffffffffu;
     const int g = warp >> 2;             // score columns 32 g .. 32 g + 31
     const int qd = warp & 3;             // TMEM lane quarter
     const int rho = qd * 32 + lane;      // TMEM lane: query row (C, S, O) or key row (P)
@@ -410,49 +427,30 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int t0 = 128 * (kind >> 1) + 8 * first;
       if ((kind & 1) == 0) {
         // C lane rho: diagonal t0 + e goes to key j = rho + 127 - t0 - e of row rho
+        // (addresses from the lowest key of the run, j0 - 7)
         const int j0 = rho + 127 - t0;
-        const uint32_t a0 = cw + kRowB * rho + 4u * (uint32_t)j0;
-#pragma unroll
-        for (int e = 0; e < 8; ++e)
-          sts32_below(a0 - 4u * e, r[e], (uint32_t)(j0 - e), 128u);
+        const uint32_t a7 = cw + kRowB * rho + 4u * (uint32_t)(j0 - 7);
+        st_run_c(a7, r, j0);
       } else {
         // P lane rho (key): diagonal t0 + e goes to row i = t0 + e - 127 + rho, key rho
         const int i0 = t0 - 127 + rho;
         const uint32_t a0 = pw + kRowB * (uint32_t)i0 + 4u * rho;
+        uint32_t v[8];
 #pragma unroll
-        for (int e = 0; e < 8; ++e)
-          sts32_below(a0 + kRowB * e, __float_as_uint(__uint_as_float(r[e]) + kbias), (uint32_t)(i0 + e), 128u);
+        for (int e = 0; e < 8; ++e) v[e] = __float_as_uint(__uint_as_float(r[e]) + kbias);
+        st_run_p(a0, v, i0);
       }
     };
     auto drain = [&](int kind, uint32_t slot_col, float kbias) {
       int first, count;
       drain_run(kind, qd, g, &first, &count);
       const uint32_t src = tmem + slot_col + lane_off + 8u * first;
-      if (count == 4) {
-        uint32_t r[32];
-        tmem_ld32(src, r);
-        tmem_ld_wait(r);
-#pragma unroll
-        for (int part = 0; part < 4; ++part) store_run(kind, first + part, r + 8 * part, kbias);
-      } else if (count >= 2) {
-        uint32_t r[16];
-        tmem_ld16(src, r);
-        if (count == 3) {
-          uint32_t r8[8];
-          tmem_ld8(src + 16, r8);
-          tmem_ld_wait(r);
-          tmem_ld_wait(r8);
-          store_run(kind, first + 2, r8, kbias);
-        } else {
-          tmem_ld_wait(r);
-        }
-        store_run(kind, first, r, kbias);
-        store_run(kind, first + 1, r + 8, kbias);
-      } else {
+#pragma unroll 1
+      for (int q = 0; q < count; ++q) {
         uint32_t r[8];
-        tmem_ld8(src, r);
+        tmem_ld8(src + 8u * q, r);
         tmem_ld_wait(r);
-        store_run(kind, first, r, kbias);
+        store_run(kind, first + q, r, kbias);
       }
     };
 
@@ -460,7 +458,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     // is warp-collective: the whole warp issues it or none of it does), and
     // once a wait has failed (the CTA is aborting) the warp arrives on no
     // barrier again.
-    constexpr uint32_t kAll = 0xffffffffu;
     bool alive = true;
     uint32_t gt = 0;  // tiles of this CTA so far (each has five products and one P.V)
     // Thread 0 copies the next work item into shared memory while the current
@@ -537,7 +534,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (alive && lane == 0) mbar_arrive(slot_empty + s);
         }
         if (alive) mbar_arrive(drained + qd);  // every lane: its stores are published
-        // ---- S, then the position terms of this thread's 32 elements
+        // ---- S, then the position terms of this thread's 32 elements: raw
+        // scores (Q.K + C + P), scaled to log2 units only inside the exponent
         float x[32];
         {
           const uint32_t xs = x0 + 4, s = xs % 3;
@@ -549,7 +547,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_ld16(tmem + s * kSlotCols + lane_off + 32 * g + 16 * hf, r);  // whole warp
             tmem_ld_wait(r);
 #pragma unroll
-            for (int e = 0; e < 16; ++e) x[16 * hf + e] = __uint_as_float(r[e]) * ks;
+            for (int e = 0; e < 16; ++e) x[16 * hf + e] = __uint_as_float(r[e]);
           }
           tc_fence_before();
           __syncwarp();
@@ -562,10 +560,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
           const uint4 c4 = lds128(gC + 16u * k), p4 = lds128(gP + 16u * k);
-          x[4 * k + 0] = fmaf(__uint_as_float(c4.x) + __uint_as_float(p4.x), ks, x[4 * k + 0]);
-          x[4 * k + 1] = fmaf(__uint_as_float(c4.y) + __uint_as_float(p4.y), ks, x[4 * k + 1]);
-          x[4 * k + 2] = fmaf(__uint_as_float(c4.z) + __uint_as_float(p4.z), ks, x[4 * k + 2]);
-          x[4 * k + 3] = fmaf(__uint_as_float(c4.w) + __uint_as_float(p4.w), ks, x[4 * k + 3]);
+          const float2 a = add2(make_float2(__uint_as_float(c4.x), __uint_as_float(c4.y)),
+                                make_float2(__uint_as_float(p4.x), __uint_as_float(p4.y)));
+          const float2 b = add2(make_float2(__uint_as_float(c4.z), __uint_as_float(c4.w)),
+                                make_float2(__uint_as_float(p4.z), __uint_as_float(p4.w)));
+          const float2 s0 = add2(make_float2(x[4 * k + 0], x[4 * k + 1]), a);
+          const float2 s1 = add2(make_float2(x[4 * k + 2], x[4 * k + 3]), b);
+          x[4 * k + 0] = s0.x;
+          x[4 * k + 1] = s0.y;
+          x[4 * k + 2] = s1.x;
+          x[4 * k + 3] = s1.y;
         }
 
         // ---- online softmax (log2 units); row maximum over the four column groups
@@ -575,7 +579,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         float mt = -INFINITY;
 #pragma unroll
-        for (int e = 0; e < 32; ++e) mt = fmaxf(mt, x[e]);
+        for (int e = 0; e < 32; e += 2) mt = fmax3(mt, x[e], x[e + 1]);
+        mt *= ks;  // log2 units (ks > 0: the maximum commutes with the scaling)
         float* red = sRed + 512 * (gt & 1);
         red[g * 128 + rho] = mt;
         named_sync(2 + qd, 128);  // the four warps of the row quarter
@@ -604,10 +609,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         {
           uint32_t r[16];
           float2 acc = make_float2(0.f, 0.f);
+          const float2 ks2 = make_float2(ks, ks), nmb = make_float2(-mb, -mb);
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
-            const float p0 = ex2(x[2 * e] - mb);
-            const float p1 = ex2(x[2 * e + 1] - mb);
+            const float2 arg = fma2(make_float2(x[2 * e], x[2 * e + 1]), ks2, nmb);
+            const float p0 = ex2(arg.x);
+            const float p1 = ex2(arg.y);
             acc = add2(acc, make_float2(p0, p1));
             r[e] = BF16 ? pack_bf16x2(p0, p1) : pack_f16x2(p0, p1);
           }

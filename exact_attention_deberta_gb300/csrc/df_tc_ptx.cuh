@@ -362,6 +362,20 @@ __device__ __forceinline__ void sts32_below(uint32_t addr, uint32_t v, uint32_t 
       "r"(v), "r"(idx), "r"(bound)
       : "memory");
 }
+// The same two stores at a compile-time byte offset from `addr`.
+template <int OFF>
+__device__ __forceinline__ void sts32_at(uint32_t addr, uint32_t v) {
+  asm volatile("st.shared.b32 [%0+%2], %1;" ::"r"(addr), "r"(v), "n"(OFF) : "memory");
+}
+template <int OFF>
+__device__ __forceinline__ void sts32_below_at(uint32_t addr, uint32_t v, uint32_t idx, uint32_t bound) {
+  asm volatile(
+      "{\n\t.reg .pred q;\n\t"
+      "setp.lt.u32 q, %2, %3;\n\t"
+      "@q st.shared.b32 [%0+%4], %1;\n\t}\n" ::"r"(addr),
+      "r"(v), "r"(idx), "r"(bound), "n"(OFF)
+      : "memory");
+}
 __device__ __forceinline__ void sts16_lo(uint32_t addr, uint32_t v) {
   asm volatile("st.shared.b16 [%0], %1;" ::"r"(addr), "h"((uint16_t)(v & 0xFFFFu)) : "memory");
 }
