@@ -466,6 +466,31 @@ __global__ void __launch_bounds__(kThreads, 1)
     // item c + 1 must not overwrite the slot that item c is still being read
     // from.
     int4* s_next = reinterpret_cast<int4*>(sm + SL::next);  // [2]
+    // Q rows of an item into tensor memory, the A operand of C0, C1 and S
+    // (every MMA that read the previous item's Q is done: this warp waited for
+    // that item's last S).  Warp (qd, g) stores columns 8 g .. 8 g + 7 (elements
+    // 16 g .. 16 g + 15) of its quarter's rows; rows past the tensor's end are
+    // zero.  Nothing for an item without tiles (the MMA warp skips it too).
+    auto q_row = [&](const int4& w) { return (long long)w.x + w.w * kTile + rho; };
+    auto store_q = [&](const int4& w) {
+      int lo, hi;
+      near_block_range(w.w * kTile, (w.y + kTile - 1) / kTile, rsp, rsn, &lo, &hi);
+      if (hi <= lo) return;
+      const long long row = q_row(w);
+      uint32_t r[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+      if (row < (long long)p.T) {
+        const uint4* src = reinterpret_cast<const uint4*>(static_cast<const T*>(p.q) +
+                                                          ((size_t)row * p.H + w.z) * kD + 16 * g);
+        const uint4 a0 = src[0], a1 = src[1];
+        r[0] = a0.x; r[1] = a0.y; r[2] = a0.z; r[3] = a0.w;
+        r[4] = a1.x; r[5] = a1.y; r[6] = a1.z; r[7] = a1.w;
+      }
+      tmem_st8(tQ + lane_off + 8 * g, r);
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (alive && lane == 0) mbar_arrive(q_full);
+    };
     uint32_t ic = 0;  // items of this CTA so far
     for (int it = blockIdx.x; it < n_items; it += gridDim.x, ++ic) {
       const int4 item = it == (int)blockIdx.x ? p.items[it] : s_next[ic & 1];
@@ -482,32 +507,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       int jlo, jhi;
       near_block_range(i0, nkb, rsp, rsn, &jlo, &jhi);
       const int nt = jhi - jlo;
-      if (nt <= 0) {  // (no item of the plan is empty) keep the next-item copy ordered
+      if (nt <= 0) {  // (no item of the plan is empty) the item's end, without tiles
         if (ctid == 0) asm volatile("cp.async.wait_all;" ::: "memory");
         named_sync(1, kComputeThreads);
+        if (it + (int)gridDim.x < n_items) store_q(s_next[(ic + 1) & 1]);
         continue;
       }
-      // Q rows of the item into tensor memory, the A operand of C0, C1 and S
-      // (every MMA that read the previous item's Q is done: this warp waited
-      // for that item's last S).  Warp (qd, g) stores columns 8 g .. 8 g + 7
-      // (elements 16 g .. 16 g + 15) of its quarter's rows; rows past the
-      // tensor's end are zero.
-      {
-        const long long row = (long long)start + i0 + rho;
-        uint32_t r[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
-        if (row < (long long)p.T) {
-          const uint4* src =
-              reinterpret_cast<const uint4*>(static_cast<const T*>(p.q) + ((size_t)row * p.H + h) * kD + 16 * g);
-          const uint4 a0 = src[0], a1 = src[1];
-          r[0] = a0.x; r[1] = a0.y; r[2] = a0.z; r[3] = a0.w;
-          r[4] = a1.x; r[5] = a1.y; r[6] = a1.z; r[7] = a1.w;
-        }
-        tmem_st8(tQ + lane_off + 8 * g, r);
-        tmem_st_wait();
-        tc_fence_before();
-        __syncwarp();
-        if (alive && lane == 0) mbar_arrive(q_full);
-      }
+      if (it == (int)blockIdx.x) store_q(item);  // later items' Q are stored ahead
       float m_run = -INFINITY, l_run = 0.f;  // l_run: this warp's 32 columns only
 
       for (int t = 0; t < nt; ++t, ++gt) {
@@ -628,6 +634,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (alive && lane == 0) mbar_arrive(p_full);
       }
 
+      // the next item's descriptor is read only after this barrier
+      if (ctid == 0) asm volatile("cp.async.wait_all;" ::: "memory");
+      named_sync(1, kComputeThreads);
+      // the next item's Q rows into L1 while the epilogue runs
+      if (it + (int)gridDim.x < n_items) {
+        const int4 nx = s_next[(ic + 1) & 1];
+        const long long row = q_row(nx);
+        if (row < (long long)p.T)
+          asm volatile("prefetch.global.L1 [%0];" ::"l"(static_cast<const T*>(p.q) +
+                                                        ((size_t)row * p.H + nx.z) * kD + 16 * g));
+      }
       // ---- epilogue: final rows, or the partial state for the far-tile kernel
       alive = __all_sync(kAll, alive && wait_ph(pv_done, (gt - 1) & 1, 296));
       tc_fence_after();
@@ -664,9 +681,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         d4[0] = make_uint4(w[0], w[1], w[2], w[3]);
         d4[1] = make_uint4(w[4], w[5], w[6], w[7]);
       }
-      if (ctid == 0) asm volatile("cp.async.wait_all;" ::: "memory");
-      // the next item is read, and the sum exchange rewritten, only after this barrier
-      named_sync(1, kComputeThreads);
+      // the next item's Q (its rows were prefetched into L1 before the epilogue)
+      if (it + (int)gridDim.x < n_items) store_q(s_next[(ic + 1) & 1]);
     }
   }
 
