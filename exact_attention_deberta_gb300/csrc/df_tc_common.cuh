@@ -107,8 +107,7 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity,
       raise_device_error(hdr, DF_ERR_DEVICE_TIMEOUT, where);
       return false;
     }
-    // sleep until the phase completes (at most ~20 us between budget checks)
-    if (ptx::mbar_try_wait_sleep(bar, parity, 20000u)) return true;
+    if (ptx::mbar_try_wait(bar, parity)) return true;
   }
 }
 

@@ -468,23 +468,31 @@ __global__ void __launch_bounds__(kThreads, 1)
     int4* s_next = reinterpret_cast<int4*>(sm + SL::next);  // [2]
     // Q rows of an item into tensor memory, the A operand of C0, C1 and S
     // (every MMA that read the previous item's Q is done: this warp waited for
-    // that item's last S).  Warp (qd, g) stores columns 8 g .. 8 g + 7 (elements
-    // 16 g .. 16 g + 15) of its quarter's rows; rows past the tensor's end are
-    // zero.  Nothing for an item without tiles (the MMA warp skips it too).
+    // that item's last S).  The rows come from global memory whole (warp
+    // (qd, g) reads rows 32 qd + 8 g .. + 7, 128 bytes each) into the idle Pw
+    // buffer; after the quarter's barrier each lane takes columns 8 g .. 8 g + 7
+    // (elements 16 g .. 16 g + 15) of its own row into tensor memory.  Rows past
+    // the tensor's end are zero.  Nothing for an item without tiles (the MMA
+    // warp skips it too).
     auto q_row = [&](const int4& w) { return (long long)w.x + w.w * kTile + rho; };
+    const uint32_t qs = smem_u32(sm + SL::pw);
     auto store_q = [&](const int4& w) {
       int lo, hi;
       near_block_range(w.w * kTile, (w.y + kTile - 1) / kTile, rsp, rsn, &lo, &hi);
       if (hi <= lo) return;
-      const long long row = q_row(w);
-      uint32_t r[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
-      if (row < (long long)p.T) {
-        const uint4* src = reinterpret_cast<const uint4*>(static_cast<const T*>(p.q) +
-                                                          ((size_t)row * p.H + w.z) * kD + 16 * g);
-        const uint4 a0 = src[0], a1 = src[1];
-        r[0] = a0.x; r[1] = a0.y; r[2] = a0.z; r[3] = a0.w;
-        r[4] = a1.x; r[5] = a1.y; r[6] = a1.z; r[7] = a1.w;
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        const int rr = 32 * qd + 8 * g + 4 * k + (lane >> 3);
+        const long long row = (long long)w.x + w.w * kTile + rr;
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (row < (long long)p.T)
+          v = *reinterpret_cast<const uint4*>(static_cast<const T*>(p.q) + ((size_t)row * p.H + w.z) * kD +
+                                              8 * (lane & 7));
+        sts128(qs + kRowB * rr + 16 * (lane & 7), v);
       }
+      named_sync(2 + qd, 128);  // the quarter's 32 rows are staged
+      const uint4 a0 = lds128(qs + kRowB * rho + 32 * g), a1 = lds128(qs + kRowB * rho + 32 * g + 16);
+      const uint32_t r[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
       tmem_st8(tQ + lane_off + 8 * g, r);
       tmem_st_wait();
       tc_fence_before();
@@ -637,7 +645,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       // the next item's descriptor is read only after this barrier
       if (ctid == 0) asm volatile("cp.async.wait_all;" ::: "memory");
       named_sync(1, kComputeThreads);
-      // the next item's Q rows into L1 while the epilogue runs
+      // the next item's Q rows (one 128-byte line each) into L1 while the
+      // epilogue runs
       if (it + (int)gridDim.x < n_items) {
         const int4 nx = s_next[(ic + 1) & 1];
         const long long row = q_row(nx);
@@ -652,34 +661,61 @@ __global__ void __launch_bounds__(kThreads, 1)
       red[g * 128 + rho] = l_run;
       named_sync(2 + qd, 128);
       const float l_tot = (red[rho] + red[128 + rho]) + (red[256 + rho] + red[384 + rho]);
-      uint32_t r[16];
-      tmem_ld16(tO + lane_off + 16 * g, r);
-      tmem_ld_wait(r);
       const bool store = alive && *s_abort == 0;
       const bool has_far = jlo > 0 || jhi < nkb;
-      const int i = i0 + rho;
-      const size_t tok = (size_t)start + i;
-      const bool row_in = i < n;
-      if (has_far) {
-        if (row_in && store) {
-          float* dst = partial_o(p) + (tok * p.H + h) * kD + 16 * g;
+      // O (divided by the row sum for final rows) goes through the idle Cw
+      // buffer, so that the stores to global memory are whole rows: after the
+      // quarter's barrier each warp writes 8 rows of its quarter.
+      const uint32_t os = smem_u32(sm + SL::cw);
+      {
+        const float sc = has_far ? 1.f : (l_tot > 0.f ? 1.f / l_tot : 0.f);
+        uint32_t r[16];
+        tmem_ld16(tO + lane_off + 16 * g, r);
+        tmem_ld_wait(r);
 #pragma unroll
-          for (int e = 0; e < 16; e += 4)
-            *reinterpret_cast<uint4*>(dst + e) = make_uint4(r[e], r[e + 1], r[e + 2], r[e + 3]);
-          if (g == 0) partial_ml(p)[tok * p.H + h] = make_float2(m_run, l_tot);
-        }
-      } else if (row_in && store && p.keybias[tok] == 0.f) {
-        const float inv = l_tot > 0.f ? 1.f / l_tot : 0.f;
-        uint32_t w[8];
+        for (int e = 0; e < 16; e += 4)
+          sts128(os + kRowB * rho + 64 * g + 4 * e,
+                 make_uint4(__float_as_uint(__uint_as_float(r[e]) * sc),
+                            __float_as_uint(__uint_as_float(r[e + 1]) * sc),
+                            __float_as_uint(__uint_as_float(r[e + 2]) * sc),
+                            __float_as_uint(__uint_as_float(r[e + 3]) * sc)));
+      }
+      if (has_far && g == 0 && store && i0 + rho < n)
+        partial_ml(p)[((size_t)start + i0 + rho) * p.H + h] = make_float2(m_run, l_tot);
+      named_sync(2 + qd, 128);  // the quarter's 32 rows are staged
+      if (store) {
+        if (has_far) {
+          // un-normalised fp32 rows (256 bytes): lanes 0-15 one row, 16-31 the next
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const float o0 = __uint_as_float(r[2 * e]) * inv;
-          const float o1 = __uint_as_float(r[2 * e + 1]) * inv;
-          w[e] = BF16 ? pack_bf16x2(o0, o1) : pack_f16x2(o0, o1);
+          for (int k = 0; k < 4; ++k) {
+            const int rr = 32 * qd + 8 * g + 2 * k + (lane >> 4);
+            const uint4 v = lds128(os + kRowB * rr + 16 * (lane & 15));
+            if (i0 + rr < n)
+              *reinterpret_cast<uint4*>(partial_o(p) + ((size_t)start + i0 + rr) * p.H * kD + h * kD +
+                                        4 * (lane & 15)) = v;
+          }
+        } else {
+          // final rows in the I/O type (128 bytes): lanes 8 a .. 8 a + 7 one row
+#pragma unroll
+          for (int k = 0; k < 2; ++k) {
+            const int rr = 32 * qd + 8 * g + 4 * k + (lane >> 3);
+            const uint32_t a = os + kRowB * rr + 32 * (lane & 7);
+            const uint4 v0 = lds128(a), v1 = lds128(a + 16);
+            const size_t tok = (size_t)start + i0 + rr;
+            if (i0 + rr < n && p.keybias[tok] == 0.f) {
+              uint4 w;
+              w.x = BF16 ? pack_bf16x2(__uint_as_float(v0.x), __uint_as_float(v0.y))
+                         : pack_f16x2(__uint_as_float(v0.x), __uint_as_float(v0.y));
+              w.y = BF16 ? pack_bf16x2(__uint_as_float(v0.z), __uint_as_float(v0.w))
+                         : pack_f16x2(__uint_as_float(v0.z), __uint_as_float(v0.w));
+              w.z = BF16 ? pack_bf16x2(__uint_as_float(v1.x), __uint_as_float(v1.y))
+                         : pack_f16x2(__uint_as_float(v1.x), __uint_as_float(v1.y));
+              w.w = BF16 ? pack_bf16x2(__uint_as_float(v1.z), __uint_as_float(v1.w))
+                         : pack_f16x2(__uint_as_float(v1.z), __uint_as_float(v1.w));
+              *reinterpret_cast<uint4*>(static_cast<T*>(p.out) + (tok * p.H + h) * kD + 8 * (lane & 7)) = w;
+            }
+          }
         }
-        uint4* d4 = reinterpret_cast<uint4*>(static_cast<T*>(p.out) + (tok * p.H + h) * kD + 16 * g);
-        d4[0] = make_uint4(w[0], w[1], w[2], w[3]);
-        d4[1] = make_uint4(w[4], w[5], w[6], w[7]);
       }
       // the next item's Q (its rows were prefetched into L1 before the epilogue)
       if (it + (int)gridDim.x < n_items) store_q(s_next[(ic + 1) & 1]);

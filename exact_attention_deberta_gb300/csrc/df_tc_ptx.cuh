@@ -379,6 +379,11 @@ __device__ __forceinline__ void sts32_below_at(uint32_t addr, uint32_t v, uint32
 __device__ __forceinline__ void sts16_lo(uint32_t addr, uint32_t v) {
   asm volatile("st.shared.b16 [%0], %1;" ::"r"(addr), "h"((uint16_t)(v & 0xFFFFu)) : "memory");
 }
+__device__ __forceinline__ void sts128(uint32_t addr, uint4 v) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z),
+               "r"(v.w)
+               : "memory");
+}
 __device__ __forceinline__ uint4 lds128(uint32_t addr) {
   uint4 v;
   asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
