@@ -185,7 +185,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int i = i0 + row;
     const size_t tok = (size_t)start + i;
     const bool row_in = i < n;
-    const bool row_out = row_in && p.keybias[tok] == 0.f;
     float m_run = -INFINITY, l_run = 0.f;  // l_run: this warpgroup's columns only
 
     // raw index-table entries and the key bias of a tile, fetched one tile ahead
@@ -374,44 +373,68 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (failed_at) break;
 
-    // epilogue: final rows, or the partial state for the far-tile kernel
+    // epilogue: final rows, or the partial state for the far-tile kernel.  O
+    // (divided by the row sum for final rows) goes through the idle band
+    // buffer as fp32 rows of D words, 16-byte chunk c of row r at chunk
+    // (c + r) mod (D / 4) (conflict-free both ways), so that the stores to
+    // global memory are whole rows: warp w then writes rows 16 w .. 16 w + 15.
     sRed[half * 128 + row] = l_run;
     __syncthreads();
     const float l_tot = sRed[row] + sRed[128 + row];
+    constexpr int kCpr = D / 4;  // 16-byte chunks per staged row
+    const uint32_t os = smem_u32(Cs);
     {
+      const float sc = has_far ? 1.f : (l_tot > 0.f ? 1.f / l_tot : 0.f);
       uint32_t r[32];
-      if (has_far) {
-        float* dst = partial_o(p) + (tok * p.H + h) * D + half * (D / 2);
 #pragma unroll
-        for (int c = 0; c < D / 64; ++c) {
-          tmem_ld32(tO + lane_off + half * (D / 2) + 32 * c, r);
-          tmem_ld_wait(r);
-          if (row_in) {
+      for (int c = 0; c < D / 64; ++c) {
+        tmem_ld32(tO + lane_off + half * (D / 2) + 32 * c, r);
+        tmem_ld_wait(r);
 #pragma unroll
-            for (int e = 0; e < 32; e += 4)
-              *reinterpret_cast<uint4*>(dst + 32 * c + e) = make_uint4(r[e], r[e + 1], r[e + 2], r[e + 3]);
-          }
+        for (int e = 0; e < 32; e += 4) {
+          const int ch = (half * (D / 2) + 32 * c + e) / 4;
+          sts128(os + 16u * (uint32_t)(row * kCpr + (ch + row) % kCpr),
+                 make_uint4(__float_as_uint(__uint_as_float(r[e]) * sc),
+                            __float_as_uint(__uint_as_float(r[e + 1]) * sc),
+                            __float_as_uint(__uint_as_float(r[e + 2]) * sc),
+                            __float_as_uint(__uint_as_float(r[e + 3]) * sc)));
         }
-        if (row_in && half == 0) partial_ml(p)[tok * p.H + h] = make_float2(m_run, l_tot);
-      } else {
-        const float inv = l_tot > 0.f ? 1.f / l_tot : 0.f;
-        T* dst = static_cast<T*>(p.out) + (tok * p.H + h) * D + half * (D / 2);
+      }
+    }
+    if (has_far && row_in && half == 0) partial_ml(p)[tok * p.H + h] = make_float2(m_run, l_tot);
+    __syncthreads();  // every row is staged
+    {
+      const int lane = tid & 31;
+#pragma unroll 1
+      for (int k = 0; k < 16; ++k) {
+        const int rr = 16 * warp + k;  // staged row
+        const int ir = i0 + rr;
+        const size_t tr = (size_t)start + ir;
+        if (has_far) {
+          // fp32 row of D words: lanes take 16-byte chunks
+          if (ir < n) {
 #pragma unroll
-        for (int c = 0; c < D / 64; ++c) {
-          tmem_ld32(tO + lane_off + half * (D / 2) + 32 * c, r);
-          tmem_ld_wait(r);
-          if (row_out) {
-            uint32_t w[16];
-#pragma unroll
-            for (int e = 0; e < 16; ++e) {
-              const float o0 = __uint_as_float(r[2 * e]) * inv;
-              const float o1 = __uint_as_float(r[2 * e + 1]) * inv;
-              w[e] = BF16 ? pack_bf16x2(o0, o1) : pack_f16x2(o0, o1);
+            for (int c = lane; c < kCpr; c += 32) {
+              const uint4 v = lds128(os + 16u * (uint32_t)(rr * kCpr + (c + rr) % kCpr));
+              *reinterpret_cast<uint4*>(partial_o(p) + (tr * p.H + h) * D + 4 * c) = v;
             }
-            uint4* d4 = reinterpret_cast<uint4*>(dst + 32 * c);
+          }
+        } else if (ir < n && p.keybias[tr] == 0.f) {
+          // row of D values of the I/O type: lanes take 8 values (two chunks)
 #pragma unroll
-            for (int e = 0; e < 4; ++e)
-              d4[e] = make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
+          for (int c = 2 * lane; c < kCpr; c += 64) {
+            const uint4 v0 = lds128(os + 16u * (uint32_t)(rr * kCpr + (c + rr) % kCpr));
+            const uint4 v1 = lds128(os + 16u * (uint32_t)(rr * kCpr + (c + 1 + rr) % kCpr));
+            uint4 w;
+            w.x = BF16 ? pack_bf16x2(__uint_as_float(v0.x), __uint_as_float(v0.y))
+                       : pack_f16x2(__uint_as_float(v0.x), __uint_as_float(v0.y));
+            w.y = BF16 ? pack_bf16x2(__uint_as_float(v0.z), __uint_as_float(v0.w))
+                       : pack_f16x2(__uint_as_float(v0.z), __uint_as_float(v0.w));
+            w.z = BF16 ? pack_bf16x2(__uint_as_float(v1.x), __uint_as_float(v1.y))
+                       : pack_f16x2(__uint_as_float(v1.x), __uint_as_float(v1.y));
+            w.w = BF16 ? pack_bf16x2(__uint_as_float(v1.z), __uint_as_float(v1.w))
+                       : pack_f16x2(__uint_as_float(v1.z), __uint_as_float(v1.w));
+            *reinterpret_cast<uint4*>(static_cast<T*>(p.out) + (tr * p.H + h) * D + 4 * c) = w;
           }
         }
       }
