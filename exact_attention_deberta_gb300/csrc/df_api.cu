@@ -80,14 +80,16 @@ void near_offsets(int L, int buckets, int max_rel, int span, int lt, int* m0, in
 // for sequences of at most L tokens.  The largest offset is 128 (nkb - 1); a
 // margin of 2 in r covers a last-ulp difference between host and device logs,
 // so "no" here is "no" on the device too.
-bool far_tiles_possible(int L, int buckets, int max_rel, int span, int lt) {
+// Whether a tile of `tile` queries x `tile` keys of some sequence (length <= L)
+// can lie wholly beyond a saturation point (a far tile).
+bool far_tiles_possible(int L, int buckets, int max_rel, int span, int lt, int tile) {
   const int top = 2 * span - 1;
   int rsp = lt + kQBlock, rsn = -(lt + kQBlock);
   for (int r = 0; r < lt; ++r)
     if (host_rel_index(r, buckets, max_rel, span) == top) { rsp = r; break; }
   for (int r = 0; r > -lt; --r)
     if (host_rel_index(r, buckets, max_rel, span) == 0) { rsn = r; break; }
-  const int reach = 128 * ((L + kKBlock - 1) / kKBlock - 1) - 127;
+  const int reach = tile * ((L + tile - 1) / tile - 1) - (tile - 1);
   return reach >= rsp - 2 || -reach <= rsn + 2;
 }
 
@@ -250,7 +252,10 @@ df_status build_problem(const void* q, const void* k, const void* v, const void*
   const unsigned long long wb = g_wait_budget.load();
   P.wait_budget = wb ? wb : kDefaultWaitBudget;
   P.zero_out = 1;
-  P.far_possible = far_tiles_possible(L, buckets, max_rel, span, lay.lt) ? 1 : 0;
+  P.far_possible = far_tiles_possible(L, buckets, max_rel, span, lay.lt, kKBlock) ? 1 : 0;
+  // the strict-fp32 kernel and the backward classify 64 x 64 tiles, which reach
+  // farther than 128 x 128 ones
+  P.scal_needed = far_tiles_possible(L, buckets, max_rel, span, lay.lt, 64) ? 1 : 0;
   return DF_OK;
 }
 
@@ -316,6 +321,7 @@ df_status df_attn_plan(const void* q, const void* k, const void* pos_key, const 
                                total_tokens, d, buckets, max_rel, span, dtype, out, workspace,
                                workspace_bytes, false, &p);
   if (st != DF_OK) return st;
+  p.scal_needed = 1;  // the planning call always writes every planner output
   return launch_plan(p, (cudaStream_t)stream) == cudaSuccess ? DF_OK : DF_ERR_CUDA;
 }
 

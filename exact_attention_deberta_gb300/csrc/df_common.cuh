@@ -66,6 +66,8 @@ struct Problem {
   unsigned long long wait_budget;
   int zero_out;               // the planner zeroes the output rows of masked tokens
   int far_possible;           // 0: no tile of any sequence (length <= L) is a far tile
+  int scal_needed;            // 0: no 64 x 64 tile is far either, so no kernel reads the
+                              //    per-token scalars or the key-term block
 };
 
 // Views of the backward pass (gradients in fp32).

@@ -61,6 +61,16 @@ __device__ void scalar_block(const Problem& p, int blk) {
   if (h == 0) p.keybias[t] = valid ? 0.f : -INFINITY;
   float a0 = 0.f, a1 = 0.f, b0 = 0.f, b1 = 0.f;
   const size_t row = ((size_t)t * H + h) * d;
+  // No far tile at all (every sequence shorter than the saturation distance):
+  // no kernel reads the scalars or the key-term block, only the key bias and
+  // the zeroed padded rows remain.
+  if (!p.scal_needed) {
+    if (!valid && in_range && p.zero_out) {
+      uint4* o4 = reinterpret_cast<uint4*>(static_cast<T*>(p.out) + row);
+      for (int v = 0; v < d * (int)sizeof(T) / 16; ++v) o4[v] = make_uint4(0u, 0u, 0u, 0u);
+    }
+    return;
+  }
   if (valid) {
     constexpr int kVec = 16 / sizeof(T);
     const uint4* q4 = reinterpret_cast<const uint4*>(static_cast<const T*>(p.q) + row);
