@@ -87,6 +87,7 @@ static_assert(tmem_region_fits(kColQ, kD / 2, 512), "Q inside 512 columns");
 // columns 32 c .. 32 c + 15 of the S slot
 static_assert(32 * (kTile / 32 - 1) + 16 <= kSlotCols, "P inside the S slot");
 constexpr uint32_t kRing = 3;                   // diagonal-table halves in flight
+constexpr uint32_t kItemRing = 4;               // work items handed from the load warp to the others
 
 struct Smem {
   static constexpr uint32_t k = 0;                     // K tile
@@ -96,13 +97,14 @@ struct Smem {
   static constexpr uint32_t pw = cw + 128 * kRowB;     // fp32 [128][132]
   static constexpr uint32_t red = pw + 128 * kRowB;    // float [3][4][128]: row max / sum exchange
   static constexpr uint32_t bars = red + 3 * 4 * 128 * 4;
-  static constexpr int kBars = 31;
+  static constexpr int kBars = 31 + 2 * kItemRing;
   static constexpr uint32_t misc = bars + kBars * 8;   // abort flag, TMEM slot
-  static constexpr uint32_t next = (misc + 16 + 15) & ~15u;  // int4 [2]: the next work item
-  static constexpr uint32_t bytes = next + 32;
+  static constexpr uint32_t next = (misc + 16 + 15) & ~15u;  // int4: the compute warps' next item
+  static constexpr uint32_t ring = next + 16;                // int4 [kItemRing]: items handed out
+  static constexpr uint32_t bytes = ring + 16 * kItemRing;
 };
 // 16-byte vector accesses: the next item (int4) and the skew buffers' rows
-static_assert(Smem::next % 16 == 0 && Smem::cw % 16 == 0 &&
+static_assert(Smem::next % 16 == 0 && Smem::ring % 16 == 0 && Smem::cw % 16 == 0 &&
                   Smem::pw % 16 == 0,
               "16-byte aligned vector regions");
 static_assert(Smem::bytes <= 227 * 1024, "near-tile shared memory");
@@ -178,6 +180,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* drained = bars + 19;    // [4]
   uint64_t* row_read = bars + 23;   // [4]
   uint64_t* col_read = bars + 27;   // [4]
+  // Work items: the load warp takes the next item of the list (a global
+  // counter, longest items first) and hands it to the MMA warp and the compute
+  // warps through a ring of kItemRing slots; a slot is free again once both
+  // have read it.  An item with n < 0 ends the CTA's list.
+  uint64_t* item_full = bars + 31;  // [kItemRing]
+  uint64_t* item_empty = bars + 31 + kItemRing;  // [kItemRing] (MMA thread and compute thread 0)
+  int4* s_ring = reinterpret_cast<int4*>(sm + SL::ring);
   volatile int* s_abort = reinterpret_cast<volatile int*>(sm + SL::misc);
   uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + SL::misc + 4);
 
@@ -187,6 +196,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s = 0; s < 3; ++s) mbar_init(slot_empty + s, kComputeWarps);
     mbar_init(p_full, kComputeWarps);
     mbar_init(q_full, kComputeWarps);
+    for (uint32_t s = 0; s < kItemRing; ++s) mbar_init(item_empty + s, 2);
     for (int q = 0; q < 4; ++q) {
       mbar_init(drained + q, 128);
       mbar_init(row_read + q, 128);
@@ -269,11 +279,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++pv_n;
       };
 
-      // the next work item is read one item ahead
-      int4 next_item = blockIdx.x < n_items ? p.items[blockIdx.x] : make_int4(0, 0, 0, 0);
-      for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
-        const int4 item = next_item;
-        if (it + (int)gridDim.x < n_items) next_item = p.items[it + gridDim.x];
+      for (uint32_t ic = 0;; ++ic) {
+        const uint32_t slot = ic % kItemRing;
+        if (!wt(item_full + slot, (ic / kItemRing) & 1, 341)) break;
+        const int4 item = s_ring[slot];
+        mbar_arrive(item_empty + slot);
+        if (item.y < 0) break;
         const int n = item.y, ib = item.w;
         const int nkb = (n + kTile - 1) / kTile;
         int jlo, jhi;
@@ -356,10 +367,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         v_pending = false;
       };
-      int4 next_item = blockIdx.x < n_items ? p.items[blockIdx.x] : make_int4(0, 0, 0, 0);
-      for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
-        const int4 item = next_item;
-        if (it + (int)gridDim.x < n_items) next_item = p.items[it + gridDim.x];
+      for (uint32_t ic = 0;; ++ic) {
+        // the next item of the list, claimed once its ring slot is free and
+        // handed to the other roles
+        const uint32_t slot = ic % kItemRing;
+        if (ic >= kItemRing && !wt(item_empty + slot, ((ic / kItemRing) - 1) & 1, 340)) break;
+        if (*s_abort) break;
+        const int it = atomicAdd(&hdr->next_item, 1);
+        const int4 item = it < n_items ? p.items[it] : make_int4(-1, -1, -1, -1);
+        s_ring[slot] = item;
+        mbar_arrive(item_full + slot);  // release: the slot's contents are visible to its waiters
+        if (item.y < 0) break;
         const int start = item.x, n = item.y, h = item.z, ib = item.w;
         const int nkb = (n + kTile - 1) / kTile;
         int jlo, jhi;
@@ -460,12 +478,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     // barrier again.
     bool alive = true;
     uint32_t gt = 0;  // tiles of this CTA so far (each has five products and one P.V)
-    // Thread 0 copies the next work item into shared memory while the current
-    // one runs (an asynchronous copy: no register is held for it); the last
-    // barrier of the item publishes it.  Two slots by item parity: the copy for
-    // item c + 1 must not overwrite the slot that item c is still being read
-    // from.
-    int4* s_next = reinterpret_cast<int4*>(sm + SL::next);  // [2]
+    // Compute thread 0 takes each work item from the load warp's ring and
+    // leaves it in s_cur; the compute warps read it after a barrier of all of
+    // them, so that every warp runs the same list.  A failed wait ends the list.
+    int4* s_cur = reinterpret_cast<int4*>(sm + SL::next);
+    uint32_t ir = 0;  // items taken from the ring (thread 0)
+    auto take_item = [&]() {
+      const uint32_t slot = ir % kItemRing;
+      int4 w = make_int4(-1, -1, -1, -1);
+      if (wait_or_abort(item_full + slot, (ir / kItemRing) & 1, budget, s_abort, hdr, 342)) {
+        w = s_ring[slot];
+        mbar_arrive(item_empty + slot);
+      }
+      ++ir;
+      *s_cur = w;
+    };
     // Q rows of an item into tensor memory, the A operand of C0, C1 and S
     // (every MMA that read the previous item's Q is done: this warp waited for
     // that item's last S).  The rows come from global memory whole (warp
@@ -477,6 +504,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto q_row = [&](const int4& w) { return (long long)w.x + w.w * kTile + rho; };
     const uint32_t qs = smem_u32(sm + SL::pw);
     auto store_q = [&](const int4& w) {
+      if (w.y < 0) return;  // the end of the list
       int lo, hi;
       near_block_range(w.w * kTile, (w.y + kTile - 1) / kTile, rsp, rsn, &lo, &hi);
       if (hi <= lo) return;
@@ -499,29 +527,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (alive && lane == 0) mbar_arrive(q_full);
     };
-    uint32_t ic = 0;  // items of this CTA so far
-    for (int it = blockIdx.x; it < n_items; it += gridDim.x, ++ic) {
-      const int4 item = it == (int)blockIdx.x ? p.items[it] : s_next[ic & 1];
-      if (ctid == 0 && it + (int)gridDim.x < n_items) {
-        // the other slot was last read at the start of item c - 1, before that
-        // item's last barrier
-        asm volatile("cp.async.ca.shared.global [%0], [%1], 16;\n\tcp.async.commit_group;" ::"r"(
-                         smem_u32(s_next + ((ic + 1) & 1))),
-                     "l"(p.items + it + gridDim.x)
-                     : "memory");
-      }
+    if (ctid == 0) take_item();
+    named_sync(1, kComputeThreads);
+    for (bool first = true;; first = false) {
+      const int4 item = *s_cur;
+      if (item.y < 0) break;
       const int start = item.x, n = item.y, h = item.z, i0 = item.w * kTile;
       const int nkb = (n + kTile - 1) / kTile;
       int jlo, jhi;
       near_block_range(i0, nkb, rsp, rsn, &jlo, &jhi);
       const int nt = jhi - jlo;
       if (nt <= 0) {  // (no item of the plan is empty) the item's end, without tiles
-        if (ctid == 0) asm volatile("cp.async.wait_all;" ::: "memory");
+        named_sync(1, kComputeThreads);  // every thread has read s_cur
+        if (ctid == 0) take_item();
         named_sync(1, kComputeThreads);
-        if (it + (int)gridDim.x < n_items) store_q(s_next[(ic + 1) & 1]);
+        store_q(*s_cur);  // nothing for the end marker or an empty item
         continue;
       }
-      if (it == (int)blockIdx.x) store_q(item);  // later items' Q are stored ahead
+      if (first) store_q(item);  // later items' Q are stored ahead
       float m_run = -INFINITY, l_run = 0.f;  // l_run: this warp's 32 columns only
 
       for (int t = 0; t < nt; ++t, ++gt) {
@@ -642,13 +665,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (alive && lane == 0) mbar_arrive(p_full);
       }
 
-      // the next item's descriptor is read only after this barrier
-      if (ctid == 0) asm volatile("cp.async.wait_all;" ::: "memory");
+      // the next item, taken while the tiles ran; read after this barrier (every
+      // thread read the current one before its first tile)
+      if (ctid == 0) take_item();
       named_sync(1, kComputeThreads);
+      const int4 nx = *s_cur;
       // the next item's Q rows (one 128-byte line each) into L1 while the
       // epilogue runs
-      if (it + (int)gridDim.x < n_items) {
-        const int4 nx = s_next[(ic + 1) & 1];
+      if (nx.y >= 0) {
         const long long row = q_row(nx);
         if (row < (long long)p.T)
           asm volatile("prefetch.global.L1 [%0];" ::"l"(static_cast<const T*>(p.q) +
@@ -718,7 +742,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       // the next item's Q (its rows were prefetched into L1 before the epilogue)
-      if (it + (int)gridDim.x < n_items) store_q(s_next[(ic + 1) & 1]);
+      if (nx.y >= 0) store_q(nx);
     }
   }
 

@@ -267,7 +267,10 @@ typedef struct {
   int32_t r_sat_pos;     /* smallest r with idx(r) = 2 span - 1 (>= L if none) */
   int32_t r_sat_neg;     /* largest r with idx(r) = 0 (<= -L if none)          */
   int32_t n_seqs;        /* sequences seen                                    */
-  int32_t reserved[10];
+  int32_t next_item;     /* near-tile kernel: next work item to hand out (its
+                            CTAs take items from the list in order, longest
+                            first, as each one finishes its previous item)   */
+  int32_t reserved[9];
 } df_ws_header;
 
 df_status df_attn_workspace_layout(int B, int H, int L, int d, int buckets, int max_rel, int span,
