@@ -141,7 +141,7 @@ __device__ void build_worklist(const Problem& p) {
   const bool in_smem = B <= kSmemSeqs;
   // The status word reports the latest call: this block is the only one of the
   // planning kernel that can raise, so it clears the word before anything else.
-  if (threadIdx.x == 0) { p.hdr->status = 0; p.hdr->status_where = 0; p.hdr->next_item = 0; }
+  if (threadIdx.x == 0) { p.hdr->status = 0; p.hdr->status_where = 0; p.hdr->next_item = 0; p.hdr->next_far_item = 0; }
   __syncthreads();
   if (p.packed) {
     for (int s = threadIdx.x; s < B; s += blockDim.x) {

@@ -144,7 +144,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   float* Cs = reinterpret_cast<float*>(sR);
   float* Ps = reinterpret_cast<float*>(sRp);
 
-  for (int it = blockIdx.x; it < n_items && failed_at == 0; it += gridDim.x) {
+  // Work items are handed out dynamically, in list order (longest first): thread
+  // 0 claims the next one from the counter in the workspace header (reset by
+  // the planner) as the CTA finishes its previous item.
+  volatile int* s_it = reinterpret_cast<volatile int*>(tslot + 1);
+  for (;;) {
+    if (tid == 0) *s_it = atomicAdd(&p.hdr->next_item, 1);
+    __syncthreads();
+    const int it = *s_it;
+    __syncthreads();  // every thread has read it before thread 0 claims the next
+    if (it >= n_items || failed_at != 0) break;
     const int4 item = p.items[it];
     const int start = item.x, n = item.y, h = item.z, i0 = item.w * kTile;
     const int nkb = (n + kTile - 1) / kTile;

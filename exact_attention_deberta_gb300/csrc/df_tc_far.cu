@@ -45,6 +45,7 @@ namespace {
 using namespace ptx;
 
 constexpr int kFarThreads = 384;
+constexpr uint32_t kFarItemRing = 4;  // work items handed from warp 0 to the other roles
 
 template <int D>
 struct FarSmem {
@@ -59,9 +60,11 @@ struct FarSmem {
   static constexpr uint32_t bars = ml + 2 * 128 * 16;
   // q_full[2], q_empty[2], k_full[S], k_empty[S], v_full[S], v_empty[S], s_full[3],
   // p_full[2][2], o_final, drain[3], buf_free[3], sel_full
-  static constexpr int kBars = 4 + 4 * kStages + 3 + 4 + 4 + 3 + 1;
-  static constexpr uint32_t misc = bars + kBars * 8;                 // abort flag, tmem slot
-  static constexpr uint32_t bytes = misc + 16;
+  static constexpr int kBars = 4 + 4 * kStages + 3 + 4 + 4 + 3 + 1 + 2 * kFarItemRing;
+  static constexpr uint32_t misc = bars + kBars * 8;                 // abort flag, tmem slot,
+                                                                     // softmax's current item
+  static constexpr uint32_t ring = misc + 16;                        // int [kFarItemRing]
+  static constexpr uint32_t bytes = ring + 4 * kFarItemRing;
   static constexpr uint32_t alloc = bytes + 1024;
 };
 
@@ -117,6 +120,15 @@ __global__ void __launch_bounds__(kFarThreads, 1)
   uint64_t* drain = o_final + 1;         // [3]: one per MMA-issuing thread
   uint64_t* buf_free = drain + 3;  // [3] d = 64: the P.V that read the buffer is done
   uint64_t* sel_full = buf_free + 3;  // selector blocks landed
+  // Work items: warp 0 claims the next item of the list (a global counter,
+  // longest items first) when a ring slot is free and hands its index to the
+  // other roles through the ring; a slot is free again once every consumer
+  // (warp 1, warps 2 and 3 at d = 64 or warp 2 at d = 128, and the softmax
+  // warpgroups' reader) has read it.  Index -1 ends the CTA's list.
+  uint64_t* item_full = sel_full + 1;                // [kFarItemRing]
+  uint64_t* item_empty = item_full + kFarItemRing;   // [kFarItemRing]
+  volatile int* s_ring = reinterpret_cast<volatile int*>(sm + SL::ring);
+  volatile int* s_cur = reinterpret_cast<volatile int*>(sm + SL::misc + 8);
   volatile int* s_abort = reinterpret_cast<volatile int*>(sm + SL::misc);
   uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + SL::misc + 4);
 
@@ -135,6 +147,10 @@ __global__ void __launch_bounds__(kFarThreads, 1)
     mbar_init(o_final, 1);  // d = 128: every P.V of the item done (d = 64 waits per tile)
     for (int b = 0; b < 3; ++b) mbar_init(drain + b, 1);
     mbar_init(sel_full, 1);
+    for (uint32_t b = 0; b < kFarItemRing; ++b) {
+      mbar_init(item_full + b, 1);
+      mbar_init(item_empty + b, D == 64 ? 4 : 3);
+    }
     *s_abort = 0;
     mbar_fence_init();
     tma_prefetch_desc(&maps.q);
@@ -167,6 +183,28 @@ __global__ void __launch_bounds__(kFarThreads, 1)
   const int rsp = p.hdr->r_sat_pos, rsn = p.hdr->r_sat_neg;
   const unsigned long long budget = p.wait_budget;
   df_ws_header* hdr = p.hdr;
+  // warp 0: claim and hand out the c-th item; -1 at the end of the list (or
+  // once the CTA aborts)
+  auto claim_item = [&](uint32_t c) -> int {
+    const uint32_t slot = c % kFarItemRing;
+    if (c >= kFarItemRing &&
+        !wait_or_abort(item_empty + slot, ((c / kFarItemRing) - 1) & 1, budget, s_abort, hdr, 330))
+      return -1;
+    if (*s_abort) return -1;
+    int it = atomicAdd(&hdr->next_far_item, 1);
+    if (it >= n_items) it = -1;
+    s_ring[slot] = it;
+    mbar_arrive(item_full + slot);  // release: the slot is visible to its waiters
+    return it;
+  };
+  // any other role (one thread): the c-th item handed out
+  auto take_item = [&](uint32_t c) -> int {
+    const uint32_t slot = c % kFarItemRing;
+    if (!wait_or_abort(item_full + slot, (c / kFarItemRing) & 1, budget, s_abort, hdr, 331)) return -1;
+    const int it = s_ring[slot];
+    mbar_arrive(item_empty + slot);
+    return it;
+  };
 
   if (warp == 0 || (!kTriS && warp == 2)) {
     // ------------------------------------------------------------ TMA producers
@@ -183,7 +221,9 @@ __global__ void __launch_bounds__(kFarThreads, 1)
         tma_load_2d(sSel, &maps.kaug_sel, 0, 0, sel_full);
         tma_load_2d(sSel + kAugBytes, &maps.kaug_sel, 0, 128, sel_full);
       }
-      for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
+      for (uint32_t ci = 0;; ++ci) {
+        const int it = is_k ? claim_item(ci) : take_item(ci);
+        if (it < 0) break;
         const ItemGeom ig = item_geom(p, it, rsp, rsn);
         if (ig.nt == 0) continue;
         if (is_k) {
@@ -243,7 +283,9 @@ __global__ void __launch_bounds__(kFarThreads, 1)
       uint32_t pn[2] = {0, 0};  // tiles of warpgroup b whose P has been consumed
       const bool sel_ok = !qk_role || wait_or_abort(sel_full, 0, budget, s_abort, hdr, 316);
       const uint32_t kv_addr = smem_u32(sKV);
-      for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
+      for (uint32_t ci = 0;; ++ci) {
+        const int it = take_item(ci);
+        if (it < 0) break;
         const ItemGeom ig = item_geom(p, it, rsp, rsn);
         if (ig.nt == 0) continue;
         const bool has_partial = ig.jhi > ig.jlo;
@@ -327,9 +369,23 @@ __global__ void __launch_bounds__(kFarThreads, 1)
     // this warpgroup's O, in a register
     const uint32_t tOw = tO_base + (uint32_t)D * wg + lane_off;
     uint32_t sc = 0, ic = 0, own = 0, gbase = 0;  // gbase: CTA tiles before the item
-    for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
+    // Thread 0 of the warpgroups takes each item from the ring and leaves it in
+    // s_cur; all 256 threads read it after their barrier, so that they run the
+    // same list (a failed wait ends it for all of them).
+    const bool reader = warp == 4 && lane == 0;
+    uint32_t ci = 0;
+    if (reader) *s_cur = take_item(ci++);
+    named_sync(3, 256);
+    for (;;) {
+      const int it = *s_cur;
+      if (it < 0) break;
       const ItemGeom ig = item_geom(p, it, rsp, rsn);
-      if (ig.nt == 0) continue;
+      if (ig.nt == 0) {  // (no item of the plan is empty) the item's end, without tiles
+        named_sync(3, 256);  // every thread has read s_cur
+        if (reader) *s_cur = take_item(ci++);
+        named_sync(3, 256);
+        continue;
+      }
       const bool has_partial = ig.jhi > ig.jlo;
       const int i = ig.i0 + row;
       const bool row_in = i < ig.n;
@@ -523,8 +579,10 @@ __global__ void __launch_bounds__(kFarThreads, 1)
         }
       }
       tc_fence_before();
-      named_sync(3, 256);
+      named_sync(3, 256);  // (also: every thread has read s_cur)
       gbase += ig.nt;
+      if (reader) *s_cur = take_item(ci++);
+      named_sync(3, 256);
     }
   }
 

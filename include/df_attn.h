@@ -270,7 +270,8 @@ typedef struct {
   int32_t next_item;     /* near-tile kernel: next work item to hand out (its
                             CTAs take items from the list in order, longest
                             first, as each one finishes its previous item)   */
-  int32_t reserved[9];
+  int32_t next_far_item; /* the same for the far-tile kernel                 */
+  int32_t reserved[8];
 } df_ws_header;
 
 df_status df_attn_workspace_layout(int B, int H, int L, int d, int buckets, int max_rel, int span,
