@@ -42,22 +42,45 @@ struct Pipe {
 };
 
 std::mutex g_mu;
-Pipe g_pipe;
+// One set of streams and events per device, created on the device's first
+// call and kept for the process (calls on several devices each use their own).
+constexpr int kMaxDevices = 64;
+Pipe g_pipes[kMaxDevices];
 
-bool pipe_ready(Pipe& p) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return false;
-  if (p.device == dev) return true;
-  if (cudaStreamCreateWithFlags(&p.in, cudaStreamNonBlocking) != cudaSuccess) return false;
-  if (cudaStreamCreateWithFlags(&p.out, cudaStreamNonBlocking) != cudaSuccess) return false;
-  for (int i = 0; i < 2; ++i)
-    if (cudaStreamCreateWithFlags(&p.comp[i], cudaStreamNonBlocking) != cudaSuccess) return false;
+void destroy_pipe(Pipe& p) {
+  cudaStream_t* ss[] = {&p.in, &p.out, &p.comp[0], &p.comp[1]};
+  for (cudaStream_t* st : ss)
+    if (*st) cudaStreamDestroy(*st);
   cudaEvent_t* evs[] = {&p.start, &p.loaded[0], &p.loaded[1], &p.computed[0], &p.computed[1],
                         &p.drained[0], &p.drained[1]};
   for (cudaEvent_t* e : evs)
-    if (cudaEventCreateWithFlags(e, cudaEventDisableTiming) != cudaSuccess) return false;
+    if (*e) cudaEventDestroy(*e);
+  p = Pipe{};
+}
+
+// The current device's pipe, or nullptr.  A pipe is published (device set)
+// only once every stream and event of it exists; a partial one is destroyed.
+Pipe* pipe_for_current_device() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  Pipe& slot = g_pipes[dev];
+  if (slot.device == dev) return &slot;
+  Pipe p;
+  bool ok = cudaStreamCreateWithFlags(&p.in, cudaStreamNonBlocking) == cudaSuccess &&
+            cudaStreamCreateWithFlags(&p.out, cudaStreamNonBlocking) == cudaSuccess;
+  for (int i = 0; ok && i < 2; ++i)
+    ok = cudaStreamCreateWithFlags(&p.comp[i], cudaStreamNonBlocking) == cudaSuccess;
+  cudaEvent_t* evs[] = {&p.start, &p.loaded[0], &p.loaded[1], &p.computed[0], &p.computed[1],
+                        &p.drained[0], &p.drained[1]};
+  for (cudaEvent_t* e : evs)
+    if (ok) ok = cudaEventCreateWithFlags(e, cudaEventDisableTiming) == cudaSuccess;
+  if (!ok) {
+    destroy_pipe(p);
+    return nullptr;
+  }
   p.device = dev;
-  return true;
+  slot = p;
+  return &slot;
 }
 
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
@@ -177,8 +200,9 @@ extern "C" df_status df_attn_fwd_host(const void* q, const void* k, const void* 
   }
 
   std::lock_guard<std::mutex> lock(g_mu);
-  if (!pipe_ready(g_pipe)) return DF_ERR_CUDA;
-  Pipe& P = g_pipe;
+  Pipe* pp = pipe_for_current_device();
+  if (!pp) return DF_ERR_CUDA;
+  Pipe& P = *pp;
   cudaStream_t cs = (cudaStream_t)stream;
   char* base = static_cast<char*>(scratch);
   const size_t row = (size_t)H * d * es;
