@@ -901,7 +901,7 @@ def main(argv=None):
         # has the same dense rate as bf16)
         bound, peak, unit = "tensor", float(peaks["bf16_tflops"]), "TFLOP/s"
         near_algo, far_algo = tile_flops(lengths, H, d, span, rsp, rsn)
-        near_file = "df_tc_near64.cu" if d in (32, 64) else "df_tc.cu"
+        near_file = "df_tc_near64.cu" if d in (32, 64) else "df_tc_near128.cu"
         if far_ms >= near_ms:
             kernel_file, kname, algo, kern_ms = "df_tc_far.cu", "tc_far_kernel", far_algo, far_ms
             other = ("tc_near_kernel", near_algo, near_ms)

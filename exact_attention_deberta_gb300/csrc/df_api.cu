@@ -114,7 +114,7 @@ Layout make_layout(int B, int H, int L, int d, int buckets, int max_rel, int spa
   off = align256(off + (size_t)l.t_pad * sizeof(float));
   l.partial = off;
   off = align256(off + T * H * (size_t)(d + 2) * sizeof(float));
-  if (d == 64) near_offsets(L, buckets, max_rel, span, l.lt, &l.diag_m0, &l.n_diag);
+  if (d == 64 || d == 128) near_offsets(L, buckets, max_rel, span, l.lt, &l.diag_m0, &l.n_diag);
   const size_t diag_bytes = (size_t)l.n_diag * 256 * H * d * 2;
   l.diag_pk = off;
   off = align256(off + diag_bytes);

@@ -53,7 +53,7 @@ struct Problem {
   int max_items;
   int t_pad;
   int lt;                     // index-table half width: idx of r at r + lt - 1, |r| < lt
-  // diagonal position tables (d = 64): row (m - diag_m0) * 256 + t holds
+  // diagonal position tables (d = 64, 128): row (m - diag_m0) * 256 + t holds
   // PK / PQ[idx(128 m - 127 + t)], [rows][H][d] in the I/O type
   void* diag_pk;
   void* diag_pq;

@@ -206,7 +206,7 @@ __device__ void build_worklist(const Problem& p) {
   }
 }
 
-// ---- diagonal position tables (near tiles of the d = 64 tensor-core kernel) ----
+// ---- diagonal position tables (near tiles of the 16-bit tensor-core kernels) ----
 // For tile offset m and diagonal t, row (m - diag_m0) * 256 + t of each table is
 // the PK (PQ) row at idx(128 m - 127 + t): with them the position products of a
 // near tile come out of the MMA already indexed by diagonal.  A block copies

@@ -13,7 +13,7 @@ constexpr unsigned long long kDrainBudget = 1ull << 31;
 
 struct TcMaps {
   CUtensorMap q, k, v, pk, pq;
-  CUtensorMap dpk, dpq;        // diagonal position tables (d = 64)
+  CUtensorMap dpk, dpq;        // diagonal position tables (near tiles)
   CUtensorMap kaug, kaug_sel;  // far tiles: key-term block and selector rows (16 wide)
 };
 
@@ -88,6 +88,7 @@ __device__ __forceinline__ float ex2(float x) {
 
 cudaError_t launch_far(const Problem& p, const TcMaps& maps, cudaStream_t s);
 cudaError_t launch_near64(const Problem& p, const TcMaps& maps, cudaStream_t s);
+cudaError_t launch_near128(const Problem& p, const TcMaps& maps, cudaStream_t s);
 
 // Bounded wait that also gives up as soon as another role of the CTA has
 // aborted.  On a timeout it records DF_ERR_DEVICE_TIMEOUT and raises the CTA's

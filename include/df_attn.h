@@ -241,7 +241,7 @@ typedef struct {
   int max_items;     /* capacity of the work-item list                        */
   int t_pad;         /* Tpad = round_up(B*L + 128, 128)                       */
   int table_half;    /* round_up(L, 128) + 128: the table covers |r| < table_half */
-  /* Diagonal position tables (d = 64 only; 0 bytes otherwise).  For every tile
+  /* Diagonal position tables (d = 64 and 128; 0 bytes otherwise).  For every tile
    * offset m in [diag_m0, diag_m0 + n_diag) -- query block minus key block of a
    * near tile -- and every diagonal t in [0, 256): row (m - diag_m0) * 256 + t
    * holds PK[idx(128 m - 127 + t)] (diag_pk) and PQ[idx(128 m - 127 + t)]

@@ -83,6 +83,7 @@ def test_diagonal_table_range(binding, buckets, max_rel, span, L):
     index function), with at most one offset of slack on each side."""
     from oracle import rel_index
     lay = binding.df_attn_workspace_layout(3, 4, L, 64, buckets=buckets, max_rel=max_rel, span=span)
+    lay128 = binding.df_attn_workspace_layout(3, 4, L, 128, buckets=buckets, max_rel=max_rel, span=span)
     nkb = (L + 127) // 128
     top = 2 * span - 1
     near = []
@@ -95,8 +96,9 @@ def test_diagonal_table_range(binding, buckets, max_rel, span, L):
     assert n <= len(near) + 2
     rows = n * 256 * 4 * 64 * 2
     assert lay["diag_pq"] - lay["diag_pk"] >= rows and lay["total"] - lay["diag_pq"] >= rows
-    assert binding.df_attn_workspace_layout(3, 4, L, 128, buckets=buckets, max_rel=max_rel,
-                                            span=span)["n_diag"] == 0
+    # head size 128: the same offsets, rows twice as wide
+    assert (lay128["diag_m0"], lay128["n_diag"]) == (m0, n)
+    assert lay128["diag_pq"] - lay128["diag_pk"] >= 2 * rows and lay128["total"] - lay128["diag_pq"] >= 2 * rows
 
 
 def _fwd_raw(binding, **over):

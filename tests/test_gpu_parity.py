@@ -89,7 +89,7 @@ def test_plan_worklist_and_scalars(lib, name):
         assert torch.all(o == 0)
 
 
-@pytest.mark.parametrize("name", ["v3base_padded_bf16", "packed_varlen_h12d64"])
+@pytest.mark.parametrize("name", ["v3base_padded_bf16", "packed_varlen_h12d64", "packed_varlen_h6d128"])
 def test_plan_diagonal_tables(lib, name):
     """Row (m - diag_m0) * 256 + t of the diagonal tables is PK / PQ at
     idx(128 m - 127 + t), byte for byte."""
