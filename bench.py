@@ -266,9 +266,10 @@ class GpuLocalCpus:
             os.sched_setaffinity(0, self.saved)
 
 
-def traffic_record(kernel_file: str):
-    """DRAM bytes per launch of the dominant kernel from the committed ncu summary,
-    valid only while the kernel source is unchanged since the capture."""
+def traffic_record(kernel_file: str, workload: str):
+    """DRAM bytes per launch of the dominant kernel on this workload from the
+    committed ncu summary (entries keyed "<source file>@<workload>"), valid only
+    while the kernel source is unchanged since the capture."""
     rec = os.path.join(ROOT, "profiles", "traffic.json")
     src = os.path.join(ROOT, "exact_attention_deberta_gb300", "csrc", kernel_file)
     if not (os.path.exists(rec) and os.path.exists(src)):
@@ -277,8 +278,8 @@ def traffic_record(kernel_file: str):
         data = json.load(f)
     with open(src, "rb") as f:
         digest = hashlib.sha256(f.read()).hexdigest()[:16]
-    entry = data.get(kernel_file)
-    if not entry or entry.get("source_sha256_16") != digest:
+    entry = data.get(f"{kernel_file}@{workload}")
+    if not entry or entry.get("source_sha256_16") != digest or entry.get("workload") != workload:
         return None
     return entry
 
@@ -914,7 +915,7 @@ def main(argv=None):
         kernel_file, kname = "df_simt.cu", "simt_fwd_kernel"
         algo, kern_ms, other = algorithmic_flops(lengths, H, d, span), far_ms, None
     achieved = algo / (kern_ms * 1e-3) / 1e12
-    tr = traffic_record(kernel_file)
+    tr = traffic_record(kernel_file, x.w.name)
     line = {
         "metric": "disentangled-attn fwd TFLOP/s (8*L^2*d/head)",
         "value": value,
