@@ -11,40 +11,27 @@
 //
 // The array holds DF_ATTN_NOALLOC_SCRATCH_BYTES on every GPU that loads the
 // library, for as long as the process lives.  Its device address is looked up
-// once per device, by the first call made with that device current, and kept
-// for the life of the process (a device reset invalidates it: the entry points
-// here must not be used after cudaDeviceReset on that device).
+// on every call with the caller's device current, so a reset of the device
+// (which reloads the module) never leaves a stale address behind.
 //
 // Errors the kernels raise on the device (a bounded wait that ran out, bad
 // cu_seqlens) land in the status word at the start of the shared array;
 // df_attn_noalloc_get_device_status reads and clears it.
 #include "df_common.cuh"
 
-#include <mutex>
-
 namespace {
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[DF_ATTN_NOALLOC_SCRATCH_BYTES];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_scratch_mu;
-void* g_scratch_addr[kMaxDevices] = {};
-
-// Device address of the scratch array on the current device.  The host-side name
-// g_noalloc_scratch is only a stand-in for the symbol and must never reach a
-// kernel; cudaGetSymbolAddress turns it into the device address.
+// Device address of the scratch array on the current device, looked up on
+// every call (cheap once the module is loaded), so that no address outlives a
+// reset of the device's primary context.  The host-side name g_noalloc_scratch
+// is only a stand-in for the symbol and must never reach a kernel;
+// cudaGetSymbolAddress turns it into the device address.
 df_status scratch_on_current_device(void** addr) {
-  int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess) return DF_ERR_CUDA;
-  if (dev < 0 || dev >= kMaxDevices) return DF_ERR_UNSUPPORTED;
-  std::lock_guard<std::mutex> lock(g_scratch_mu);
-  if (g_scratch_addr[dev] == nullptr) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr)
-      return DF_ERR_CUDA;
-    g_scratch_addr[dev] = p;
-  }
-  *addr = g_scratch_addr[dev];
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) return DF_ERR_CUDA;
+  *addr = p;
   return DF_OK;
 }
 

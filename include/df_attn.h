@@ -322,13 +322,12 @@ int df_attn_last_launch_count(void);
  *     exits;
  *   - a problem whose df_attn_workspace_size() exceeds that size is rejected
  *     with DF_ERR_WORKSPACE and nothing is enqueued;
- *   - the first call on each device looks the array's device address up (once,
- *     with that device current); make that first call before any stream capture;
+ *   - every call looks the array's device address up with the caller's device
+ *     current; the first call on a device loads the library's module there, so
+ *     make it before any stream capture;
  *   - every call on a device shares the one array, which keeps the previous
  *     call's contents: calls that overlap on the GPU (other streams, other host
  *     threads) race on it and must be serialised by the caller;
- *   - the array's device address is kept for the life of the process: do not
- *     call this entry point on a device after cudaDeviceReset;
  *   - errors raised on the device (a bounded wait that ran out, bad
  *     cu_seqlens) are recorded in the status word at the start of the shared
  *     array, where each call's planning kernel resets it; read them with
