@@ -17,21 +17,32 @@ namespace {
 
 constexpr int kPlanThreads = 256;
 
-// ---- a1: one entry of the index table, plus the two saturation points -------
+// ---- a1: the index table, plus the two saturation points ----------------------
 // r_sat_pos = smallest r with idx(r) = 2 span - 1, r_sat_neg = largest r with
 // idx(r) = 0.  idx is non-decreasing in r, so each point has exactly one writer.
-__device__ void index_entry(const Problem& p, int e) {
-  const int lt = p.lt;
+// One warp per kTableRun = 30 consecutive entries: lane l evaluates entry
+// base + l - 1, so that lanes 1..30 find both neighbours that the saturation
+// tests compare with in the adjacent lanes, and lanes 0 and 31 only supply
+// them.  Every lane evaluates exactly one double-precision bucket; GB300's
+// FP64 pipe is slow, so the table is spread over many one-warp blocks rather
+// than whole 256-thread blocks that would queue on a few SMs.
+constexpr int kTableRun = 30;
+
+__device__ void index_run(const Problem& p, int blk) {
+  const int lane = threadIdx.x;
+  if (lane >= 32) return;
+  const int lt = p.lt, n = 2 * lt - 1, top = 2 * p.span - 1;
+  const int e = blk * kTableRun + lane - 1;
   const int r = e - (lt - 1);
-  const int top = 2 * p.span - 1;
   const int u = rel_index(r, p.buckets, p.max_rel, p.span);
+  const int prev = __shfl_up_sync(0xffffffffu, u, 1);    // idx(r - 1)
+  const int next = __shfl_down_sync(0xffffffffu, u, 1);  // idx(r + 1)
+  if (lane == 0 || lane == 31 || e >= n) return;
   p.idx[e] = u;
-  if (u == top && (r == -(lt - 1) || rel_index(r - 1, p.buckets, p.max_rel, p.span) != top))
-    p.hdr->r_sat_pos = r;
-  if (r == lt - 1 && u != top) p.hdr->r_sat_pos = lt + kQBlock;  // never within reach
-  if (u == 0 && (r == lt - 1 || rel_index(r + 1, p.buckets, p.max_rel, p.span) != 0))
-    p.hdr->r_sat_neg = r;
-  if (r == -(lt - 1) && u != 0) p.hdr->r_sat_neg = -(lt + kQBlock);
+  if (u == top && (e == 0 || prev != top)) p.hdr->r_sat_pos = r;
+  if (e == n - 1 && u != top) p.hdr->r_sat_pos = lt + kQBlock;  // never within reach
+  if (u == 0 && (e == n - 1 || next != 0)) p.hdr->r_sat_neg = r;
+  if (e == 0 && u != 0) p.hdr->r_sat_neg = -(lt + kQBlock);
 }
 
 // ---- per-token position scalars (far tiles) and zeroing of padded rows -------
@@ -48,7 +59,7 @@ __device__ void scalar_block(const Problem& p, int blk) {
   const int t = (blk % tiles) * kPlanThreads + threadIdx.x;
   const T* pk = static_cast<const T*>(p.pk);
   const T* pq = static_cast<const T*>(p.pq);
-  for (int e = threadIdx.x; e < 4 * d; e += kPlanThreads) {
+  for (int e = threadIdx.x; p.scal_needed && e < 4 * d; e += kPlanThreads) {
     const int which = e / d, c = e % d;
     const T* src = which < 2 ? pk : pq;
     const int prow = (which & 1) ? top : 0;
@@ -244,8 +255,7 @@ __global__ void __launch_bounds__(kPlanThreads)
   }
   const int bid = blockIdx.x - 1;
   if (bid < nb_table) {
-    const int e = bid * kPlanThreads + threadIdx.x;
-    if (e < 2 * p.lt - 1) index_entry(p, e);
+    index_run(p, bid);
     return;
   }
   if (bid < nb_table + nb_scal) {
@@ -264,7 +274,7 @@ index_table_kernel(int buckets, int max_rel, int span, int max_len, int32_t* idx
 }  // namespace
 
 cudaError_t launch_plan(const Problem& p, cudaStream_t s) {
-  const int nb_table = (2 * p.lt - 1 + kPlanThreads - 1) / kPlanThreads;
+  const int nb_table = (2 * p.lt - 1 + kTableRun - 1) / kTableRun;
   const int nb_scal = p.H * ((p.t_pad + kPlanThreads - 1) / kPlanThreads);
   // diagonal tables: 16-bit I/O types only (the strict-fp32 kernel does not use them)
   const int nb_diag = p.dtype == DF_FP32 ? 0 : 2 * p.n_diag * 256 / kDiagRows;
