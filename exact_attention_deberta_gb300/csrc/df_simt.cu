@@ -10,11 +10,21 @@
 // Per tile the three logit terms are formed directly:
 //   S   = Q_blk . K_blkᵀ                         (64 x 64 x d)
 //   c2p = Q_i . PK[idx(i-j)],  p2c = K_j . PQ[idx(i-j)]
-// For a near tile the PK / PQ rows of the tile's index band are staged in
-// shared memory and each thread gathers, for its 4x4 micro-tile (rows ty+16a,
-// columns tx+16b), the 7 band rows its diagonals touch.  A far tile lies
-// entirely in a saturated part of the index table, so c2p and p2c are the
-// per-token scalars prepared by the planning kernel.
+// Each thread owns a 4x4 micro-tile (rows ty + 16 a, keys tx + 16 b).  For a
+// near tile the PK / PQ rows of the tile's index band are staged in shared
+// memory and each thread reads, for its micro-tile, the 7 band rows its
+// diagonals touch.  A far tile lies entirely in a saturated part of the index
+// table, so c2p and p2c are the per-token scalars of the planning kernel.
+//
+// Shared memory holds every operand row-major, as in global memory, so that
+// the copies are plain 16-byte cp.async transfers, and the FFMA loops read
+// 16-byte vectors of four consecutive head-dimension (or key) elements: one
+// vector load feeds four FMAs per operand pair.  Row strides of 4 (mod 8)
+// words keep the eight lanes of each 16-byte load phase in distinct banks.
+// The query rows of a work unit stay resident; the key rows and band rows of
+// the next 32-column chunk are copied while the current one is multiplied
+// (two buffers), and the next tile's V while the current tile's softmax and
+// P.V run.
 #include "df_common.cuh"
 
 #include <math.h>
@@ -25,42 +35,62 @@ namespace dfa {
 
 namespace {
 
-constexpr int BM = 64;   // query rows per sub-block
+constexpr int BM = 64;   // query rows per work unit
 constexpr int BN = 64;   // keys per tile
-constexpr int DC = 32;   // head-dim chunk staged at once
+constexpr int DC = 32;   // head-dimension chunk staged at once
 constexpr int WB = 128;  // band capacity (BM + BN - 1 = 127 rows)
 constexpr int kThreads = 256;
+constexpr int SC = DC + 4;  // row stride (words) of the key and band chunks
+constexpr int SP = BN + 4;  // row stride of P
 
 template <int D>
 struct SimtSmem {
-  static constexpr int q = DC * (BM + 1);
-  static constexpr int k = DC * (BN + 1);
-  static constexpr int band = DC * (WB + 1);
-  static constexpr int v = BN * D;
-  static constexpr int p = BM * (BN + 1);
-  static constexpr int floats = q + k + 2 * band + v + p + 2 * BM + 3 * BN;
+  static constexpr int SQ = D + 4;  // row stride of Q and V
+  static constexpr int q = 0;                      // [BM][SQ]
+  static constexpr int v = q + BM * SQ;            // [BN][SQ]
+  static constexpr int p = v + BN * SQ;            // [BM][SP]
+  static constexpr int stage = p + BM * SP;        // [2][K chunk | PK band | PQ band]
+  static constexpr int k_off = 0, pk_off = BN * SC, pq_off = pk_off + WB * SC;
+  static constexpr int stage_floats = pq_off + WB * SC;
+  static constexpr int floats = stage + 2 * stage_floats;
   static constexpr size_t bytes = floats * sizeof(float);
+  static_assert((SQ / 4) % 2 == 1 && (SC / 4) % 2 == 1 && (SP / 4) % 2 == 1,
+                "odd 16-byte strides: conflict-free vector loads");
+  static_assert(v % 4 == 0 && p % 4 == 0 && stage % 4 == 0 && stage_floats % 4 == 0,
+                "16-byte aligned regions");
 };
 
-template <typename T, int D>
-__global__ void __launch_bounds__(kThreads) simt_fwd_kernel(Problem p) {
-  extern __shared__ float smem[];
-  using L = SimtSmem<D>;
-  float* Qs = smem;               // [DC][BM+1]
-  float* Ks = Qs + L::q;          // [DC][BN+1]
-  float* PKs = Ks + L::k;         // [DC][WB+1]
-  float* PQs = PKs + L::band;     // [DC][WB+1]
-  float* Vs = PQs + L::band;      // [BN][D]
-  float* Ps = Vs + L::v;          // [BM][BN+1]
-  float* rowA = Ps + L::p;        // [2][BM]  alpha (neg side, pos side)
-  float* colB = rowA + 2 * BM;    // [3][BN]  beta (neg, pos), key bias
+// 16-byte asynchronous copy global -> shared; src_bytes 0 fills zeros.
+__device__ __forceinline__ void cp16(float* dst, const float* src, int src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(
+                   (uint32_t)__cvta_generic_to_shared(dst)),
+               "l"(src), "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
 
-  const T* __restrict__ gq = static_cast<const T*>(p.q);
-  const T* __restrict__ gk = static_cast<const T*>(p.k);
-  const T* __restrict__ gv = static_cast<const T*>(p.v);
-  const T* __restrict__ gpk = static_cast<const T*>(p.pk);
-  const T* __restrict__ gpq = static_cast<const T*>(p.pq);
-  T* __restrict__ gout = static_cast<T*>(p.out);
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1) simt_fwd_kernel(Problem p) {
+  extern __shared__ __align__(16) float smem[];
+  using L = SimtSmem<D>;
+  constexpr int SQ = L::SQ;
+  constexpr int NCH = D / DC;  // chunks per tile
+  static_assert(D % DC == 0, "whole chunks");
+  float* Qs = smem + L::q;
+  float* Vs = smem + L::v;
+  float* Ps = smem + L::p;
+  float* stage0 = smem + L::stage;
+
+  const float* __restrict__ gq = static_cast<const float*>(p.q);
+  const float* __restrict__ gk = static_cast<const float*>(p.k);
+  const float* __restrict__ gv = static_cast<const float*>(p.v);
+  const float* __restrict__ gpk = static_cast<const float*>(p.pk);
+  const float* __restrict__ gpq = static_cast<const float*>(p.pq);
+  float* __restrict__ gout = static_cast<float*>(p.out);
 
   const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
   const int H = p.H;
@@ -68,7 +98,10 @@ __global__ void __launch_bounds__(kThreads) simt_fwd_kernel(Problem p) {
   const int n_items = p.hdr->n_items;
   const int rsp = p.hdr->r_sat_pos, rsn = p.hdr->r_sat_neg;
   const float ks = p.kscale;
-  constexpr int NC = D / 16;  // output columns per thread
+  // output columns of this thread: 4 tx + c + 64 m (d >= 64), 2 tx + c (d = 32)
+  constexpr int CW = D >= 64 ? 4 : 2;    // consecutive columns per group
+  constexpr int NG = D >= 64 ? D / 64 : 1;  // column groups
+  constexpr int NC = CW * NG;
 
   // one work unit per 64-row half of an item: a small problem still fills
   // twice as many blocks
@@ -76,174 +109,254 @@ __global__ void __launch_bounds__(kThreads) simt_fwd_kernel(Problem p) {
   for (int u = blockIdx.x; u < n_items * kSubs; u += gridDim.x) {
     const int4 item = p.items[u / kSubs];
     const int start = item.x, n = item.y, h = item.z, qb = item.w;
+    const int i0 = qb * kQBlock + (u % kSubs) * BM;
+    if (i0 >= n) continue;
     const float* scal_h = p.scal + (size_t)h * 4 * p.t_pad;
-    {
-      const int sub = u % kSubs;
-      const int i0 = qb * kQBlock + sub * BM;
-      if (i0 >= n) continue;
-      __syncthreads();
-      for (int e = tid; e < BM; e += kThreads) {
-        const int t = start + i0 + e;
-        rowA[e] = i0 + e < n ? scal_h[0 * (size_t)p.t_pad + t] : 0.f;
-        rowA[BM + e] = i0 + e < n ? scal_h[1 * (size_t)p.t_pad + t] : 0.f;
+    const int nkb = (n + BN - 1) / BN;
+    const int n_stages = nkb * NCH;
+
+    // tile geometry: far (and on which side) or the band [lo, lo + w) of PK / PQ
+    auto tile_far = [&](int jb, bool* pos) {
+      const int j0 = jb * BN;
+      const int rlo = i0 - j0 - (BN - 1), rhi = i0 - j0 + (BM - 1);
+      *pos = rlo >= rsp;
+      return rlo >= rsp || rhi <= rsn;
+    };
+    // copies of stage s: the key rows and (near tiles) band rows of its chunk
+    auto issue_stage = [&](int s) {
+      const int jb = s / NCH, kc = (s % NCH) * DC, j0 = jb * BN;
+      float* st = stage0 + (s & 1) * L::stage_floats;
+      for (int e = tid; e < BN * (DC / 4); e += kThreads) {
+        const int r = e / (DC / 4), c = 4 * (e % (DC / 4));
+        const bool ok = j0 + r < n;
+        cp16(st + L::k_off + r * SC + c, ok ? gk + (size_t)(start + j0 + r) * tok_stride + h * D + kc + c : gk,
+             ok ? 16 : 0);
       }
-      float m[4], l[4], o[4][NC];
-#pragma unroll
-      for (int a = 0; a < 4; ++a) {
-        m[a] = -INFINITY;
-        l[a] = 0.f;
-#pragma unroll
-        for (int c = 0; c < NC; ++c) o[a][c] = 0.f;
+      bool pos;
+      if (!tile_far(jb, &pos)) {
+        const int lo = p.idx[i0 - j0 - (BN - 1) + p.lt - 1];
+        const int w = p.idx[i0 - j0 + (BM - 1) + p.lt - 1] - lo + 1;
+        for (int e = tid; e < 2 * w * (DC / 4); e += kThreads) {
+          const int which = e / (w * (DC / 4)), f = e % (w * (DC / 4));
+          const int r = f / (DC / 4), c = 4 * (f % (DC / 4));
+          const float* src = (which ? gpq : gpk) + (size_t)(lo + r) * tok_stride + h * D + kc + c;
+          cp16(st + (which ? L::pq_off : L::pk_off) + r * SC + c, src, 16);
+        }
       }
-      const int nkb = (n + BN - 1) / BN;
-      for (int jb = 0; jb < nkb; ++jb) {
-        const int j0 = jb * BN;
-        const int rlo = i0 - j0 - (BN - 1), rhi = i0 - j0 + (BM - 1);
-        const bool far_pos = rlo >= rsp, far_neg = rhi <= rsn;
-        const bool far = far_pos || far_neg;
-        int lo = 0, w = 0;
-        int col[7];
+    };
+    auto issue_v = [&](int jb) {
+      const int j0 = jb * BN;
+      for (int e = tid; e < BN * (D / 4); e += kThreads) {
+        const int r = e / (D / 4), c = 4 * (e % (D / 4));
+        const bool ok = j0 + r < n;
+        cp16(Vs + r * SQ + c, ok ? gv + (size_t)(start + j0 + r) * tok_stride + h * D + c : gv, ok ? 16 : 0);
+      }
+    };
+
+    __syncthreads();  // the previous unit's readers of Q, V, P and the stages are done
+    for (int e = tid; e < BM * (D / 4); e += kThreads) {
+      const int r = e / (D / 4), c = 4 * (e % (D / 4));
+      const bool ok = i0 + r < n;
+      cp16(Qs + r * SQ + c, ok ? gq + (size_t)(start + i0 + r) * tok_stride + h * D + c : gq, ok ? 16 : 0);
+    }
+    issue_v(0);
+    issue_stage(0);
+    cp_commit();
+
+    float a_neg[4], a_pos[4];  // this thread's rows: Q.PK[0] and Q.PK[top] (log2 units)
+#pragma unroll
+    for (int a = 0; a < 4; ++a) {
+      const int i = i0 + ty + 16 * a;
+      a_neg[a] = i < n ? scal_h[start + i] : 0.f;
+      a_pos[a] = i < n ? scal_h[(size_t)p.t_pad + start + i] : 0.f;
+    }
+    float m[4], l[4], o[4][NC];
+#pragma unroll
+    for (int a = 0; a < 4; ++a) {
+      m[a] = -INFINITY;
+      l[a] = 0.f;
+#pragma unroll
+      for (int c = 0; c < NC; ++c) o[a][c] = 0.f;
+    }
+    float s[4][4], cp[4][4], pc[4][4];
+    int col[7];
+    bool far = false, far_pos = false;
+
+    for (int st_i = 0; st_i < n_stages; ++st_i) {
+      const int jb = st_i / NCH, kc = (st_i % NCH) * DC, j0 = jb * BN;
+      if (kc == 0) {
+        far = tile_far(jb, &far_pos);
         if (!far) {
-          lo = p.idx[rlo + p.lt - 1];
-          w = p.idx[rhi + p.lt - 1] - lo + 1;
+          const int lo = p.idx[i0 - j0 - (BN - 1) + p.lt - 1];
 #pragma unroll
           for (int dd = 0; dd < 7; ++dd)
             col[dd] = p.idx[i0 - j0 + ty - tx + 16 * (dd - 3) + p.lt - 1] - lo;
         }
-        __syncthreads();  // previous tile's Ps / Vs / colB readers are done
-        for (int e = tid; e < BN; e += kThreads) {
-          const int j = j0 + e;
-          const int t = start + j;
-          const bool ok = j < n;
-          colB[e] = ok ? scal_h[2 * (size_t)p.t_pad + t] : -INFINITY;
-          colB[BN + e] = ok ? scal_h[3 * (size_t)p.t_pad + t] : -INFINITY;
-          colB[2 * BN + e] = ok ? p.keybias[t] : -INFINITY;
-        }
-        stage_rows<T, D, kThreads>(gv + (size_t)(start + j0) * tok_stride + (size_t)h * D, tok_stride, BN,
-                                   n - j0, Vs);
-        float s[4][4], cp[4][4], pc[4][4];
 #pragma unroll
         for (int a = 0; a < 4; ++a)
 #pragma unroll
           for (int b = 0; b < 4; ++b) s[a][b] = cp[a][b] = pc[a][b] = 0.f;
-
-        for (int kc = 0; kc < D; kc += DC) {
-          if (kc) __syncthreads();
-          const size_t hc = (size_t)h * D + kc;
-          stage_transposed<T, DC, BM + 1, kThreads>(gq + (size_t)(start + i0) * tok_stride + hc, tok_stride,
-                                                   BM, n - i0, Qs);
-          stage_transposed<T, DC, BN + 1, kThreads>(gk + (size_t)(start + j0) * tok_stride + hc, tok_stride,
-                                                   BN, n - j0, Ks);
-          if (!far) {
-            stage_transposed<T, DC, WB + 1, kThreads>(gpk + (size_t)lo * tok_stride + hc, tok_stride, w, w, PKs);
-            stage_transposed<T, DC, WB + 1, kThreads>(gpq + (size_t)lo * tok_stride + hc, tok_stride, w, w, PQs);
-          }
-          __syncthreads();
-          if (far) {
-#pragma unroll 4
-            for (int c = 0; c < DC; ++c) {
-              float qa[4], kb[4];
-#pragma unroll
-              for (int a = 0; a < 4; ++a) qa[a] = Qs[c * (BM + 1) + ty + 16 * a];
-#pragma unroll
-              for (int b = 0; b < 4; ++b) kb[b] = Ks[c * (BN + 1) + tx + 16 * b];
-#pragma unroll
-              for (int a = 0; a < 4; ++a)
-#pragma unroll
-                for (int b = 0; b < 4; ++b) s[a][b] = fmaf(qa[a], kb[b], s[a][b]);
-            }
-          } else {
+      }
+      // the next stage's copies go out before this one is awaited
+      if (st_i + 1 < n_stages) {
+        issue_stage(st_i + 1);
+        cp_commit();
+        cp_wait<1>();
+      } else {
+        cp_wait<0>();
+      }
+      __syncthreads();
+      const float* st = stage0 + (st_i & 1) * L::stage_floats;
+      const float* kst = st + L::k_off;
+      const float* pkst = st + L::pk_off;
+      const float* pqst = st + L::pq_off;
 #pragma unroll 2
-            for (int c = 0; c < DC; ++c) {
-              float qa[4], kb[4], pkd[7], pqd[7];
+      for (int c4 = 0; c4 < DC; c4 += 4) {
+        float4 qa[4], kb[4];
 #pragma unroll
-              for (int a = 0; a < 4; ++a) qa[a] = Qs[c * (BM + 1) + ty + 16 * a];
+        for (int a = 0; a < 4; ++a) qa[a] = *reinterpret_cast<const float4*>(Qs + (ty + 16 * a) * SQ + kc + c4);
 #pragma unroll
-              for (int b = 0; b < 4; ++b) kb[b] = Ks[c * (BN + 1) + tx + 16 * b];
-#pragma unroll
-              for (int dd = 0; dd < 7; ++dd) {
-                pkd[dd] = PKs[c * (WB + 1) + col[dd]];
-                pqd[dd] = PQs[c * (WB + 1) + col[dd]];
-              }
-#pragma unroll
-              for (int a = 0; a < 4; ++a)
-#pragma unroll
-                for (int b = 0; b < 4; ++b) {
-                  s[a][b] = fmaf(qa[a], kb[b], s[a][b]);
-                  cp[a][b] = fmaf(qa[a], pkd[a - b + 3], cp[a][b]);
-                  pc[a][b] = fmaf(kb[b], pqd[a - b + 3], pc[a][b]);
-                }
-            }
-          }
-        }
-
-        // logits in log2 units, masked keys at -inf
-        float x[4][4];
+        for (int b = 0; b < 4; ++b) kb[b] = *reinterpret_cast<const float4*>(kst + (tx + 16 * b) * SC + c4);
 #pragma unroll
         for (int a = 0; a < 4; ++a)
 #pragma unroll
           for (int b = 0; b < 4; ++b) {
-            const int jj = tx + 16 * b;
-            float v;
-            if (far) {
-              const float al = far_pos ? rowA[BM + ty + 16 * a] : rowA[ty + 16 * a];
-              const float be = far_pos ? colB[BN + jj] : colB[jj];
-              v = fmaf(s[a][b], ks, al + be);
-            } else {
-              v = fmaf(s[a][b] + cp[a][b] + pc[a][b], ks, colB[2 * BN + jj]);
-            }
-            x[a][b] = j0 + jj < n ? v : -INFINITY;
+            s[a][b] = fmaf(qa[a].x, kb[b].x, s[a][b]);
+            s[a][b] = fmaf(qa[a].y, kb[b].y, s[a][b]);
+            s[a][b] = fmaf(qa[a].z, kb[b].z, s[a][b]);
+            s[a][b] = fmaf(qa[a].w, kb[b].w, s[a][b]);
           }
-        // online softmax, row partials reduced over the 16 lanes sharing a row
+        if (!far) {
+          float4 bd[7];
+#pragma unroll
+          for (int dd = 0; dd < 7; ++dd) bd[dd] = *reinterpret_cast<const float4*>(pkst + col[dd] * SC + c4);
+#pragma unroll
+          for (int a = 0; a < 4; ++a)
+#pragma unroll
+            for (int b = 0; b < 4; ++b) {
+              const float4 e = bd[a - b + 3];
+              cp[a][b] = fmaf(qa[a].x, e.x, cp[a][b]);
+              cp[a][b] = fmaf(qa[a].y, e.y, cp[a][b]);
+              cp[a][b] = fmaf(qa[a].z, e.z, cp[a][b]);
+              cp[a][b] = fmaf(qa[a].w, e.w, cp[a][b]);
+            }
+#pragma unroll
+          for (int dd = 0; dd < 7; ++dd) bd[dd] = *reinterpret_cast<const float4*>(pqst + col[dd] * SC + c4);
+#pragma unroll
+          for (int a = 0; a < 4; ++a)
+#pragma unroll
+            for (int b = 0; b < 4; ++b) {
+              const float4 e = bd[a - b + 3];
+              pc[a][b] = fmaf(kb[b].x, e.x, pc[a][b]);
+              pc[a][b] = fmaf(kb[b].y, e.y, pc[a][b]);
+              pc[a][b] = fmaf(kb[b].z, e.z, pc[a][b]);
+              pc[a][b] = fmaf(kb[b].w, e.w, pc[a][b]);
+            }
+        }
+      }
+      if (kc + DC < D) {
+        __syncthreads();  // this stage's buffer takes stage st_i + 2
+        continue;
+      }
+
+      // ---- the tile is complete: logits in log2 units, masked keys at -inf
+      float x[4][4];
+#pragma unroll
+      for (int b = 0; b < 4; ++b) {
+        const int j = j0 + tx + 16 * b;
+        const bool ok = j < n;
+        const size_t t = (size_t)start + j;
+        // key terms of this column: far tiles take the saturated p2c scalar,
+        // near tiles the key bias (0, or -inf for a masked key)
+        const float kterm = !ok ? -INFINITY
+                                : far ? scal_h[(far_pos ? 3 : 2) * (size_t)p.t_pad + t] : p.keybias[t];
 #pragma unroll
         for (int a = 0; a < 4; ++a) {
-          float mt = fmaxf(fmaxf(x[a][0], x[a][1]), fmaxf(x[a][2], x[a][3]));
-#pragma unroll
-          for (int off = 8; off > 0; off >>= 1) mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, off));
-          const float mn = fmaxf(m[a], mt);
-          const float base = mn == -INFINITY ? 0.f : mn;
-          const float corr = exp2f(m[a] - base);
-          m[a] = mn;
-          l[a] *= corr;
-#pragma unroll
-          for (int c = 0; c < NC; ++c) o[a][c] *= corr;
-#pragma unroll
-          for (int b = 0; b < 4; ++b) {
-            const float pv = exp2f(x[a][b] - base);
-            l[a] += pv;
-            Ps[(ty + 16 * a) * (BN + 1) + tx + 16 * b] = pv;
-          }
+          const float v = far ? fmaf(s[a][b], ks, (far_pos ? a_pos[a] : a_neg[a]) + kterm)
+                              : fmaf(s[a][b] + cp[a][b] + pc[a][b], ks, kterm);
+          x[a][b] = ok ? v : -INFINITY;
         }
-        __syncthreads();
-#pragma unroll 4
-        for (int j = 0; j < BN; ++j) {
-          float pa[4];
+      }
+      // online softmax, row partials reduced over the 16 lanes sharing a row
 #pragma unroll
-          for (int a = 0; a < 4; ++a) pa[a] = Ps[(ty + 16 * a) * (BN + 1) + j];
+      for (int a = 0; a < 4; ++a) {
+        float mt = fmaxf(fmaxf(x[a][0], x[a][1]), fmaxf(x[a][2], x[a][3]));
 #pragma unroll
-          for (int c = 0; c < NC; ++c) {
-            const float vv = Vs[j * D + tx + 16 * c];
+        for (int off = 8; off > 0; off >>= 1) mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, off));
+        const float mn = fmaxf(m[a], mt);
+        const float base = mn == -INFINITY ? 0.f : mn;
+        const float corr = exp2f(m[a] - base);
+        m[a] = mn;
+        l[a] *= corr;
 #pragma unroll
-            for (int a = 0; a < 4; ++a) o[a][c] = fmaf(pa[a], vv, o[a][c]);
+        for (int c = 0; c < NC; ++c) o[a][c] *= corr;
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+          const float pv = exp2f(x[a][b] - base);
+          l[a] += pv;
+          Ps[(ty + 16 * a) * SP + tx + 16 * b] = pv;
+        }
+      }
+      __syncthreads();  // P stored; every thread is done with this tile's stage buffers
+#pragma unroll 2
+      for (int j4 = 0; j4 < BN; j4 += 4) {
+        float4 pa[4];
+#pragma unroll
+        for (int a = 0; a < 4; ++a) pa[a] = *reinterpret_cast<const float4*>(Ps + (ty + 16 * a) * SP + j4);
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) {
+          float vv[NC];
+#pragma unroll
+          for (int g = 0; g < NG; ++g) {
+            if constexpr (CW == 4) {
+              const float4 t4 = *reinterpret_cast<const float4*>(Vs + (j4 + jj) * SQ + 64 * g + 4 * tx);
+              vv[4 * g] = t4.x;
+              vv[4 * g + 1] = t4.y;
+              vv[4 * g + 2] = t4.z;
+              vv[4 * g + 3] = t4.w;
+            } else {
+              const float2 t2 = *reinterpret_cast<const float2*>(Vs + (j4 + jj) * SQ + 2 * tx);
+              vv[0] = t2.x;
+              vv[1] = t2.y;
+            }
+          }
+#pragma unroll
+          for (int a = 0; a < 4; ++a) {
+            const float pj = jj == 0 ? pa[a].x : jj == 1 ? pa[a].y : jj == 2 ? pa[a].z : pa[a].w;
+#pragma unroll
+            for (int c = 0; c < NC; ++c) o[a][c] = fmaf(pj, vv[c], o[a][c]);
           }
         }
       }
-      // epilogue: normalise, write valid query rows (masked rows were zeroed by the planner)
+      __syncthreads();  // P and V are free
+      if (jb + 1 < nkb) {
+        issue_v(jb + 1);
+        cp_commit();
+      }
+    }
+
+    // epilogue: normalise, write valid query rows (masked rows were zeroed by the planner)
 #pragma unroll
-      for (int a = 0; a < 4; ++a) {
-        float lt = l[a];
+    for (int a = 0; a < 4; ++a) {
+      float lt = l[a];
 #pragma unroll
-        for (int off = 8; off > 0; off >>= 1) lt += __shfl_xor_sync(0xffffffffu, lt, off);
-        const int i = i0 + ty + 16 * a;
-        if (i < n && p.keybias[start + i] == 0.f) {
-          const float inv = 1.f / lt;
-          T* dst = gout + (start + i) * tok_stride + (size_t)h * D;
+      for (int off = 8; off > 0; off >>= 1) lt += __shfl_xor_sync(0xffffffffu, lt, off);
+      const int i = i0 + ty + 16 * a;
+      if (i < n && p.keybias[start + i] == 0.f) {
+        const float inv = 1.f / lt;
+        float* dst = gout + (start + i) * tok_stride + (size_t)h * D;
 #pragma unroll
-          for (int c = 0; c < NC; ++c) dst[tx + 16 * c] = IO<T>::from_f(o[a][c] * inv);
+        for (int g = 0; g < NG; ++g) {
+          if constexpr (CW == 4)
+            *reinterpret_cast<float4*>(dst + 64 * g + 4 * tx) =
+                make_float4(o[a][4 * g] * inv, o[a][4 * g + 1] * inv, o[a][4 * g + 2] * inv, o[a][4 * g + 3] * inv);
+          else
+            *reinterpret_cast<float2*>(dst + 2 * tx) = make_float2(o[a][0] * inv, o[a][1] * inv);
         }
       }
     }
   }
+  cp_wait<0>();  // no copy may still be landing when the CTA leaves
 }
 
 int num_sms() {
@@ -257,33 +370,25 @@ int num_sms() {
   return sms;
 }
 
-template <typename T, int D>
+template <int D>
 cudaError_t launch_typed(const Problem& p, cudaStream_t s) {
   const size_t bytes = SimtSmem<D>::bytes;
-  cudaError_t e = cudaFuncSetAttribute(simt_fwd_kernel<T, D>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  cudaError_t e = cudaFuncSetAttribute(simt_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)bytes);
   if (e != cudaSuccess) return e;
-  const int grid = std::min(p.max_items * (kQBlock / BM), num_sms() * 2);
+  const int grid = std::min(p.max_items * (kQBlock / BM), num_sms());
   if (grid <= 0) return cudaSuccess;
-  simt_fwd_kernel<T, D><<<grid, kThreads, bytes, s>>>(p);
+  simt_fwd_kernel<D><<<grid, kThreads, bytes, s>>>(p);
   return cudaGetLastError();
 }
 
 }  // namespace
 
+// fp32 I/O only: 16-bit inputs take the tensor-core kernels.
 cudaError_t launch_simt(const Problem& p, cudaStream_t s, int* launches) {
   *launches = p.max_items > 0 ? 1 : 0;
-  switch (p.dtype) {
-    case DF_BF16:
-      return p.d == 32 ? launch_typed<__nv_bfloat16, 32>(p, s)
-             : p.d == 64 ? launch_typed<__nv_bfloat16, 64>(p, s) : launch_typed<__nv_bfloat16, 128>(p, s);
-    case DF_FP16:
-      return p.d == 32 ? launch_typed<__half, 32>(p, s)
-             : p.d == 64 ? launch_typed<__half, 64>(p, s) : launch_typed<__half, 128>(p, s);
-    default:
-      return p.d == 32 ? launch_typed<float, 32>(p, s)
-             : p.d == 64 ? launch_typed<float, 64>(p, s) : launch_typed<float, 128>(p, s);
-  }
+  if (p.dtype != DF_FP32) return cudaErrorInvalidValue;
+  return p.d == 32 ? launch_typed<32>(p, s) : p.d == 64 ? launch_typed<64>(p, s) : launch_typed<128>(p, s);
 }
 
 }  // namespace dfa
