@@ -31,15 +31,20 @@
 // Tensor memory: a ring of three 128-column slots takes the products in the
 // order C0, P0, C1, P1, S of every tile (product x in slot x mod 3), so that
 // the tensor core computes the next products while the current ones are
-// drained; O 384-447; P (16-bit, for P.V) 448-511.
+// drained; P (16-bit pairs, for P.V) overwrites its tile's S; O 384-447; Q
+// (16-bit pairs, the A operand of C0, C1 and S) 448-479.
 //
 // Roles (one CTA per SM, persistent over the work list):
 //   warps 0-15  compute: warp w owns TMEM lanes 32 (w % 4) .. +31 (query rows
 //               for C, S and O; key rows for P) and score columns
 //               32 (w / 4) .. +31 of every tile; they drain the position
-//               products, gather, run the online softmax and write P into TMEM;
-//   warp 16     control: TMA loads (Q, K, V, the diagonal-table halves
-//               through a two-buffer ring) and every tcgen05.mma, one thread.
+//               products, gather, run the online softmax, write P into TMEM
+//               and store each item's Q rows into TMEM;
+//   warp 16     MMA issue (one thread): every tcgen05.mma;
+//   warp 17     TMA loads (one thread): K, V and the diagonal-table halves
+//               through a three-buffer ring; it also claims the work items
+//               (longest first, one global counter) and hands them to the
+//               other roles.
 // No barrier of the whole CTA inside a tile: the compute warps hand the skew
 // buffers over by lane quarter.  Quarter q's drains fill the rows 32 q .. +31
 // of Cw and the key columns 32 q .. +31 of Pw; a warp gathers from its own
@@ -49,9 +54,9 @@
 // exchanged between the four warps of a row quarter only.
 // A masked or absent key is masked through its P row: the P drains add the
 // key's bias (0 or -inf) to every position term they store for it.
-// The compute warps do not spill (only the control thread keeps a few
-// counters in local memory), so no destination register of an asynchronous
-// tensor-memory load is spilled or reused before its wait.
+// The kernel does not spill (ptxas: 96 registers, no local memory), so no
+// destination register of an asynchronous tensor-memory load is spilled or
+// reused before its wait.
 //
 // A query block whose key range also has far tiles leaves its un-normalised
 // partial state (O, running max, running sum) for the far-tile kernel;
