@@ -41,7 +41,7 @@ class _Layout(ctypes.Structure):
     _fields_ = [("header", _sz), ("idx_table", _sz), ("items", _sz), ("scalars", _sz),
                 ("keybias", _sz), ("partial", _sz), ("total", _sz), ("max_items", _i),
                 ("t_pad", _i), ("table_half", _i), ("diag_pk", _sz), ("diag_pq", _sz),
-                ("n_diag", _i), ("diag_m0", _i), ("kaug", _sz), ("kaug_sel", _sz)]
+                ("n_diag", _i), ("diag_m0", _i), ("kaug", _sz), ("kaug_sel", _sz), ("absel", _sz)]
 
 
 _lib.df_attn_fwd.argtypes = [_vp] * 7 + [_i] * 9 + [_vp, _vp, _sz, _vp]

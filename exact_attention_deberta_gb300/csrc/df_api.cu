@@ -33,7 +33,8 @@ constexpr unsigned long long kDefaultWaitBudget = 1ull << 31;
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 struct Layout {
-  size_t header, idx, items, seqs, scal, keybias, partial, diag_pk, diag_pq, kaug, kaug_sel, total;
+  size_t header, idx, items, seqs, scal, keybias, partial, diag_pk, diag_pq, kaug, kaug_sel, absel,
+      total;
   int max_items, t_pad, lt, n_diag, diag_m0;
 };
 
@@ -124,6 +125,8 @@ Layout make_layout(int B, int H, int L, int d, int buckets, int max_rel, int spa
   off = align256(off + (size_t)l.t_pad * H * 16 * 2);
   l.kaug_sel = off;
   off = align256(off + 256 * 16 * 2);
+  l.absel = off;
+  off = align256(off + (size_t)H * 16 * 64 * 2);
   l.total = off;
   return l;
 }
@@ -247,6 +250,7 @@ df_status build_problem(const void* q, const void* k, const void* v, const void*
   P.diag_pq = base + lay.diag_pq;
   P.kaug = base + lay.kaug;
   P.kaug_sel = base + lay.kaug_sel;
+  P.absel = base + lay.absel;
   P.n_diag = lay.n_diag;
   P.diag_m0 = lay.diag_m0;
   const unsigned long long wb = g_wait_budget.load();
@@ -308,6 +312,7 @@ df_status df_attn_workspace_layout(int B, int H, int L, int d, int buckets, int 
   layout->diag_m0 = l.diag_m0;
   layout->kaug = l.kaug;
   layout->kaug_sel = l.kaug_sel;
+  layout->absel = l.absel;
   return DF_OK;
 }
 
@@ -348,6 +353,7 @@ df_status df_attn_fwd(const void* q, const void* k, const void* v, const void* p
                        base + pl.o, workspace, pl.fwd, true, &w);
     if (st != DF_OK) return st;
     w.kscale = p.kscale;  // the scale of the true head size
+    w.scal_in_near = w.far_possible;
     const void* src[5] = {q, k, v, pos_key, pos_query};
     void* dst[5] = {base + pl.q, base + pl.k, base + pl.v, base + pl.pk, base + pl.pq};
     const long long tok_rows = (long long)total_tokens * H, pos_rows = 2ll * span * H;
@@ -360,6 +366,8 @@ df_status df_attn_fwd(const void* q, const void* k, const void* v, const void* p
     g_last_launches.store(3 + launches);
     return DF_OK;
   }
+  // the d = 64 near-tile kernel forms the far tiles' scalars itself
+  if (dtype != DF_FP32 && d == 64 && tc_enabled()) p.scal_in_near = p.far_possible;
   if (launch_plan(p, s) != cudaSuccess) return DF_ERR_CUDA;
   int launches = 0;
   cudaError_t e;

@@ -61,6 +61,9 @@ struct Problem {
   // in the I/O type, and the two selector blocks [256][16]
   void* kaug;
   void* kaug_sel;
+  // [H][16][64] in the I/O type: PK[0], PK[top], PQ[0], PQ[top] of each head
+  // (then zeros), the B operand of the d = 64 near-tile kernel's scalar MMAs
+  void* absel;
   int n_diag;
   int diag_m0;
   unsigned long long wait_budget;
@@ -68,6 +71,9 @@ struct Problem {
   int far_possible;           // 0: no tile of any sequence (length <= L) is a far tile
   int scal_needed;            // 0: no 64 x 64 tile is far either, so no kernel reads the
                               //    per-token scalars or the key-term block
+  int scal_in_near;           // 1: the d = 64 near-tile kernel writes the far tiles'
+                              //    query scalars and key-term blocks (the planner
+                              //    only writes the selector-row table)
 };
 
 // Views of the backward pass (gradients in fp32).

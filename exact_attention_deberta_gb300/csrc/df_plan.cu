@@ -59,7 +59,8 @@ __device__ void scalar_block(const Problem& p, int blk) {
   const int t = (blk % tiles) * kPlanThreads + threadIdx.x;
   const T* pk = static_cast<const T*>(p.pk);
   const T* pq = static_cast<const T*>(p.pq);
-  for (int e = threadIdx.x; p.scal_needed && e < 4 * d; e += kPlanThreads) {
+  const bool scal = p.scal_needed && !p.scal_in_near;
+  for (int e = threadIdx.x; scal && e < 4 * d; e += kPlanThreads) {
     const int which = e / d, c = e % d;
     const T* src = which < 2 ? pk : pq;
     const int prow = (which & 1) ? top : 0;
@@ -72,10 +73,10 @@ __device__ void scalar_block(const Problem& p, int blk) {
   if (h == 0) p.keybias[t] = valid ? 0.f : -INFINITY;
   float a0 = 0.f, a1 = 0.f, b0 = 0.f, b1 = 0.f;
   const size_t row = ((size_t)t * H + h) * d;
-  // No far tile at all (every sequence shorter than the saturation distance):
-  // no kernel reads the scalars or the key-term block, only the key bias and
-  // the zeroed padded rows remain.
-  if (!p.scal_needed) {
+  // No far tile at all (every sequence shorter than the saturation distance),
+  // or the near-tile kernel forms the scalars and key-term blocks itself: only
+  // the key bias and the zeroed padded rows remain.
+  if (!scal) {
     if (!valid && in_range && p.zero_out) {
       uint4* o4 = reinterpret_cast<uint4*>(static_cast<T*>(p.out) + row);
       for (int v = 0; v < d * (int)sizeof(T) / 16; ++v) o4[v] = make_uint4(0u, 0u, 0u, 0u);
@@ -135,6 +136,20 @@ __device__ void scalar_block(const Problem& p, int blk) {
 template <typename T>
 __device__ void write_kaug_selectors(const Problem& p) {
   if constexpr (sizeof(T) == 2) {
+    if (p.scal_in_near) {
+      // per head: PK[0], PK[top], PQ[0], PQ[top], then twelve zero rows (d = 64)
+      const int top = 2 * p.span - 1, H = p.H;
+      T* dst = static_cast<T*>(p.absel);
+      for (int e = threadIdx.x; e < H * 16 * 64; e += blockDim.x) {
+        const int h = e / (16 * 64), row = (e / 64) % 16, c = e % 64;
+        T v = IO<T>::from_f(0.f);
+        if (row < 4) {
+          const T* src = static_cast<const T*>(row < 2 ? p.pk : p.pq);
+          v = src[((size_t)((row & 1) ? top : 0) * H + h) * 64 + c];
+        }
+        dst[e] = v;
+      }
+    }
     T* sel = static_cast<T*>(p.kaug_sel);
     for (int e = threadIdx.x; e < 256 * 16; e += blockDim.x) {
       const int row = e >> 4, c = e & 15;

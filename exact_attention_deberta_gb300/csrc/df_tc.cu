@@ -40,12 +40,12 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 // Row-major [rows][row_elems] 16-bit matrix in boxes of `inner` x 128 elements:
 // 64-element boxes with the 128-byte swizzle, 16-element boxes with the 32-byte one.
 bool encode_rows(CUtensorMap* m, const void* base, long long rows, long long row_elems, bool bf16,
-                 int inner = 64) {
+                 int inner = 64, int box_rows = 128) {
   auto enc = tensor_map_encoder();
   if (!enc) return false;
   const cuuint64_t dims[2] = {(cuuint64_t)row_elems, (cuuint64_t)rows};
   const cuuint64_t strides[1] = {(cuuint64_t)row_elems * 2};
-  const cuuint32_t box[2] = {(cuuint32_t)inner, 128};
+  const cuuint32_t box[2] = {(cuuint32_t)inner, (cuuint32_t)box_rows};
   const cuuint32_t es[2] = {1, 1};
   return enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
              const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -71,6 +71,9 @@ cudaError_t launch_tc(const Problem& p, cudaStream_t s, cudaEvent_t ev0, cudaEve
     return cudaErrorInvalidValue;
   if (!encode_rows(&maps.kaug, p.kaug, p.T, 16LL * p.H, bf16, 16) ||
       !encode_rows(&maps.kaug_sel, p.kaug_sel, 256, 16, bf16, 16))
+    return cudaErrorInvalidValue;
+  // the selector rows of the d = 64 near-tile kernel's scalar MMAs: 16 rows per head
+  if (p.scal_in_near && (p.d != 64 || !encode_rows(&maps.absel, p.absel, 16LL * p.H, 64, bf16, 64, 16)))
     return cudaErrorInvalidValue;
   if (p.d == 64 || p.d == 128) {
     if (p.n_diag < 1 || !encode_rows(&maps.dpk, p.diag_pk, 256LL * p.n_diag, row, bf16) ||

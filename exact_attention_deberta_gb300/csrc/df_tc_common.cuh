@@ -15,6 +15,7 @@ struct TcMaps {
   CUtensorMap q, k, v, pk, pq;
   CUtensorMap dpk, dpq;        // diagonal position tables (near tiles)
   CUtensorMap kaug, kaug_sel;  // far tiles: key-term block and selector rows (16 wide)
+  CUtensorMap absel;           // d = 64 near tiles: PK / PQ rows of the far-tile terms (16 x 64 boxes)
 };
 
 constexpr uint32_t kAugBytes = 128 * 16 * 2;  // one 128-row x 16-column 16-bit box

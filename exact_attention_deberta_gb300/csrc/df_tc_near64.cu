@@ -88,6 +88,12 @@ constexpr uint32_t kColQ = kColO + kD;          // 448: Q (16-bit pairs), the A 
 static_assert(tmem_region_fits(0, kSlots * kSlotCols, kColO), "product ring below O");
 static_assert(tmem_region_fits(kColO, kD, kColQ), "O below Q");
 static_assert(tmem_region_fits(kColQ, kD / 2, 512), "Q inside 512 columns");
+// The far tiles' per-token terms, when this kernel forms them: Q.[PK|PQ rows]
+// (16 columns, the query scalars in the first two) and K.[PK|PQ rows] of the
+// diagonal tile's keys (16 columns, the key terms in columns 2 and 3)
+constexpr uint32_t kColAB = kColQ + kD / 2;     // 480
+static_assert(tmem_region_fits(kColAB, 32, 512), "scalar products inside 512 columns");
+constexpr uint32_t kSelBytes = 16 * kD * 2;     // one head's 16 selector rows
 // P of a tile (16-bit pairs) overwrites its S: column group c's 32 keys at
 // columns 32 c .. 32 c + 15 of the S slot
 static_assert(32 * (kTile / 32 - 1) + 16 <= kSlotCols, "P inside the S slot");
@@ -98,11 +104,12 @@ struct Smem {
   static constexpr uint32_t k = 0;                     // K tile
   static constexpr uint32_t v = k + kBoxBytes;         // V tile
   static constexpr uint32_t e = v + kBoxBytes;         // [kRing] diagonal-table halves
-  static constexpr uint32_t cw = e + kRing * kBoxBytes;  // fp32 [128][132]
+  static constexpr uint32_t sel = e + kRing * kBoxBytes;  // [2] selector rows (by item parity)
+  static constexpr uint32_t cw = sel + 2 * kSelBytes;  // fp32 [128][132]
   static constexpr uint32_t pw = cw + 128 * kRowB;     // fp32 [128][132]
   static constexpr uint32_t red = pw + 128 * kRowB;    // float [3][4][128]: row max / sum exchange
   static constexpr uint32_t bars = red + 3 * 4 * 128 * 4;
-  static constexpr int kBars = 31 + 2 * kItemRing;
+  static constexpr int kBars = 36 + 2 * kItemRing;
   static constexpr uint32_t misc = bars + kBars * 8;   // abort flag, TMEM slot
   static constexpr uint32_t next = (misc + 16 + 15) & ~15u;  // int4: the compute warps' next item
   static constexpr uint32_t ring = next + 16;                // int4 [kItemRing]: items handed out
@@ -113,7 +120,7 @@ static_assert(Smem::next % 16 == 0 && Smem::ring % 16 == 0 && Smem::cw % 16 == 0
                   Smem::pw % 16 == 0,
               "16-byte aligned vector regions");
 static_assert(Smem::bytes <= 227 * 1024, "near-tile shared memory");
-static_assert(Smem::bars % 8 == 0 && Smem::e % 1024 == 0, "alignment");
+static_assert(Smem::bars % 8 == 0 && Smem::e % 1024 == 0 && Smem::sel % 1024 == 0, "alignment");
 
 // Run of 8-column groups (first group, count) that warp g of lane quarter qd
 // drains from position product `kind` (0: C0, 1: P0, 2: C1, 3: P1).  Lane quarter
@@ -146,6 +153,10 @@ __device__ __forceinline__ void st_run_p(uint32_t a0, const uint32_t* v, int i0)
   DFA_P(0) DFA_P(1) DFA_P(2) DFA_P(3) DFA_P(4) DFA_P(5) DFA_P(6) DFA_P(7)
 #undef DFA_P
 }
+
+// Bits of a 16-bit value, for packing two of them into a 32-bit word.
+__device__ __forceinline__ uint16_t bits16(__nv_bfloat16 v) { return __bfloat16_as_ushort(v); }
+__device__ __forceinline__ uint16_t bits16(__half v) { return __half_as_ushort(v); }
 
 template <bool BF16>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -191,6 +202,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   // have read it.  An item with n < 0 ends the CTA's list.
   uint64_t* item_full = bars + 31;  // [kItemRing]
   uint64_t* item_empty = bars + 31 + kItemRing;  // [kItemRing] (MMA thread and compute thread 0)
+  // Far tiles' terms (when p.scal_in_near): an item's selector rows landed
+  // (by item parity); the MMAs that read them are done; both products of the
+  // item are in tensor memory.
+  uint64_t* sel_full = bars + 31 + 2 * kItemRing;   // [2]
+  uint64_t* sel_empty = sel_full + 2;               // [2]
+  uint64_t* ab_full = sel_full + 4;
+  uint8_t* sSel = sm + SL::sel;
   int4* s_ring = reinterpret_cast<int4*>(sm + SL::ring);
   volatile int* s_abort = reinterpret_cast<volatile int*>(sm + SL::misc);
   uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + SL::misc + 4);
@@ -233,7 +251,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       // Products and P.V issued, tables consumed.  The n-th commit on a barrier
       // completes its phase n, parity n & 1.
-      uint32_t ec_n = 0, pp = 0, pv_n = 0, k_n = 0, v_n = 0, q_n = 0, g_n = 0;
+      uint32_t ec_n = 0, pp = 0, pv_n = 0, k_n = 0, v_n = 0, q_n = 0, g_n = 0, ia = 0;
+      constexpr uint32_t kIdescAB = idesc_f16(128, 16, BF16 ? 1 : 0, 0, 0);
       bool have_prev = false, prev_first = false;
       const uint64_t dk = kmajor_desc(sK, 0);
       const uint32_t dv_addr = smem_u32(sV);
@@ -296,6 +315,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         near_block_range(ib * kTile, nkb, rsp, rsn, &jlo, &jhi);
         const int nt = jhi - jlo;
         if (nt <= 0) continue;
+        const int t_diag = ib - jlo;  // the diagonal tile (never saturated)
+        const uint64_t dsel = kmajor_desc(sSel + (ia & 1) * kSelBytes, 0);
         for (int t = 0; t < nt; ++t) {
           // The previous tile's P.V goes first at an item's first tile: the
           // compute warps store this item's Q once that P.V is done.
@@ -303,10 +324,29 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (have_prev) issue_pv(prev_first, 320);
             wt(q_full, q_n & 1, 304);
             ++q_n;
+            // the query rows' far-tile scalars: Q.[PK|PQ rows]
+            if (p.scal_in_near && !*s_abort && wt(sel_full + (ia & 1), (ia >> 1) & 1, 324)) {
+              tc_fence_after();
+#pragma unroll
+              for (int k = 0; k < kD / 16; ++k)
+                mma_ts(tmem + kColAB, tQ + 8 * k, dsel + kmajor_step(k), kIdescAB, k > 0 ? 1u : 0u);
+            }
           }
           issue_pos(0, 310);
           wt(k_full, k_n & 1, 305);
           ++k_n;
+          // the diagonal tile's keys: K.[PK|PQ rows], the far tiles' key terms
+          if (p.scal_in_near && t == t_diag) {
+            if (!*s_abort) {
+              tc_fence_after();
+#pragma unroll
+              for (int k = 0; k < kD / 16; ++k)
+                mma_ss(tmem + kColAB + 16, dk + kmajor_step(k), dsel + kmajor_step(k), kIdescAB, k > 0);
+            }
+            mma_commit(ab_full);
+            mma_commit(sel_empty + (ia & 1));
+            ++ia;
+          }
           issue_pos(1, 312);
           if (t > 0) issue_pv(prev_first, 320);
           issue_pos(2, 314);
@@ -348,7 +388,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&maps.v);
       tma_prefetch_desc(&maps.dpk);
       tma_prefetch_desc(&maps.dpq);
-      uint32_t k_n = 0, v_n = 0, e_n = 0;
+      if (p.scal_in_near) tma_prefetch_desc(&maps.absel);
+      uint32_t k_n = 0, v_n = 0, e_n = 0, ia = 0;
       int v_head = 0, v_row = 0;
       bool v_pending = false;
       auto e_load = [&](const CUtensorMap* map, int head, int row, int where) {
@@ -389,6 +430,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         near_block_range(ib * kTile, nkb, rsp, rsn, &jlo, &jhi);
         const int nt = jhi - jlo;
         if (nt <= 0) continue;
+        // the head's selector rows, into the buffer of this item's parity once
+        // the MMAs of the item two back are done with it
+        if (p.scal_in_near) {
+          const uint32_t sb = ia & 1;
+          bool ok = !*s_abort;
+          if (ok && ia >= 2) ok = wt(sel_empty + sb, ((ia >> 1) - 1) & 1, 343);
+          if (ok) {
+            mbar_expect_tx(sel_full + sb, kSelBytes);
+            tma_load_2d(sSel + sb * kSelBytes, &maps.absel, 0, h * 16, sel_full + sb);
+          }
+          ++ia;
+        }
         for (int t = 0; t < nt; ++t) {
           const int kb = jlo + t;
           int drow = (ib - kb - p.diag_m0) * 256;   // first row of the tile's diagonal tables
@@ -418,6 +471,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // no copy may still be in flight when the CTA leaves
       if (k_n) mbar_wait(k_full, (k_n - 1) & 1, kDrainBudget);
       if (v_n) mbar_wait(v_full, (v_n - 1) & 1, kDrainBudget);
+      for (uint32_t x = ia > 2 ? ia - 2 : 0; x < ia; ++x) mbar_wait(sel_full + (x & 1), (x >> 1) & 1, kDrainBudget);
       for (uint32_t b = 0; b < kRing; ++b) {
         if (e_n > b) {
           const uint32_t x = b + kRing * ((e_n - 1 - b) / kRing);  // last load into buffer b
@@ -483,6 +537,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // barrier again.
     bool alive = true;
     uint32_t gt = 0;  // tiles of this CTA so far (each has five products and one P.V)
+    uint32_t ia = 0;  // items whose far-tile terms were formed (p.scal_in_near)
     // Compute thread 0 takes each work item from the load warp's ring and
     // leaves it in s_cur; the compute warps read it after a barrier of all of
     // them, so that every warp runs the same list.  A failed wait ends the list.
@@ -668,6 +723,45 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (alive && lane == 0) mbar_arrive(p_full);
+        // ---- after the diagonal tile: the far tiles' terms of this query block
+        // (query scalars, log2-scaled) and of its keys (raw key terms as
+        // hi + lo, masked keys at the finite stand-in), one warp per quarter
+        if (p.scal_in_near && t == item.w - jlo) {
+          if (g == 0) {
+            alive = __all_sync(kAll, alive && wait_ph(ab_full, ia & 1, 299));
+            tc_fence_after();
+            if (alive) {
+              uint32_t ra[8], rb[8];
+              tmem_ld8(tmem + kColAB + lane_off, ra);
+              tmem_ld8(tmem + kColAB + 16 + lane_off, rb);
+              tmem_ld_wait(ra);
+              tmem_ld_wait(rb);
+              const int i = i0 + rho;  // query row; also key row of the diagonal tile
+              if (i < n) {
+                const size_t tok = (size_t)start + i;
+                float* sc = p.scal + (size_t)h * 4 * p.t_pad + tok;
+                sc[0] = __uint_as_float(ra[0]) * ks;
+                sc[p.t_pad] = __uint_as_float(ra[1]) * ks;
+                const bool valid = kbias == 0.f;
+                const float c0 = valid ? __uint_as_float(rb[2]) : kMaskedKeyTerm;
+                const float c1 = valid ? __uint_as_float(rb[3]) : kMaskedKeyTerm;
+                const T h0 = IO<T>::from_f(c0), h1 = IO<T>::from_f(c1);
+                const T l0 = IO<T>::from_f(valid ? c0 - IO<T>::to_f(h0) : kMaskedKeyTerm);
+                const T l1 = IO<T>::from_f(valid ? c1 - IO<T>::to_f(h1) : kMaskedKeyTerm);
+                uint4 w0;
+                w0.x = (uint32_t)bits16(h0) | ((uint32_t)bits16(l0) << 16);
+                w0.y = (uint32_t)bits16(h1) | ((uint32_t)bits16(l1) << 16);
+                w0.z = 0u;
+                w0.w = 0u;
+                uint4* dst = reinterpret_cast<uint4*>(static_cast<T*>(p.kaug) + (tok * p.H + h) * 16);
+                dst[0] = w0;
+                dst[1] = make_uint4(0u, 0u, 0u, 0u);
+              }
+            }
+            tc_fence_before();
+          }
+          ++ia;
+        }
       }
 
       // the next item, taken while the tiles ran; read after this barrier (every

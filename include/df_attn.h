@@ -257,6 +257,11 @@ typedef struct {
    * it, kaug_sel: [256][16] selector rows (1, 1, 0, ...) and (0, 0, 1, 1, ...). */
   size_t kaug;
   size_t kaug_sel;
+  /* Position rows of the far-tile terms per head (16-bit I/O types, d = 64):
+   * [H][16][64] in the I/O type, rows PK[0], PK[2span-1], PQ[0], PQ[2span-1],
+   * then zeros.  With them the d = 64 near-tile kernel forms the far tiles'
+   * scalars and key-term blocks from the Q and K tiles it already holds. */
+  size_t absel;
 } df_ws_layout;
 
 /* Header at workspace offset 0, written on the device by every call. */
