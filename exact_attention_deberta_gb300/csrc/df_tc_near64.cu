@@ -32,7 +32,9 @@
 // order C0, P0, C1, P1, S of every tile (product x in slot x mod 3), so that
 // the tensor core computes the next products while the current ones are
 // drained; P (16-bit pairs, for P.V) overwrites its tile's S; O 384-447; Q
-// (16-bit pairs, the A operand of C0, C1 and S) 448-479.
+// (16-bit pairs, the A operand of C0, C1 and S) 448-479; when the kernel forms
+// the far tiles' query scalars and key terms (p.scal_in_near), Q and the
+// diagonal tile's K times the head's selector rows in 480-495 and 496-511.
 //
 // Roles (one CTA per SM, persistent over the work list):
 //   warps 0-15  compute: warp w owns TMEM lanes 32 (w % 4) .. +31 (query rows
