@@ -116,7 +116,7 @@ Layout make_layout(int B, int H, int L, int d, int buckets, int max_rel, int spa
   l.partial = off;
   off = align256(off + T * H * (size_t)(d + 2) * sizeof(float));
   if (d == 64 || d == 128) near_offsets(L, buckets, max_rel, span, l.lt, &l.diag_m0, &l.n_diag);
-  const size_t diag_bytes = (size_t)l.n_diag * 256 * H * d * 2;
+  const size_t diag_bytes = l.n_diag > 0 ? (size_t)(l.n_diag + 1) * 128 * H * d * 2 : 0;
   l.diag_pk = off;
   off = align256(off + diag_bytes);
   l.diag_pq = off;

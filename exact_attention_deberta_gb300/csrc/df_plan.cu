@@ -49,7 +49,9 @@ __device__ void index_run(const Problem& p, int blk) {
 // scal[h][0..3][t] = kscale * {Q_t.PK[0], Q_t.PK[top], K_t.PQ[0], K_t.PQ[top]}.
 // A masked (or out-of-range) key gets -inf in both K terms and in keybias.
 // One thread per (head, token); a block covers 256 tokens of one head and keeps
-// that head's four position rows in shared memory.
+// that head's four position rows in shared memory.  The output rows of masked
+// tokens (padded mode) are zeroed by each warp together, a whole row per group
+// of lanes, so that every store fills whole 32-byte sectors.
 template <typename T>
 __device__ void scalar_block(const Problem& p, int blk) {
   __shared__ float rows[4][128];
@@ -67,22 +69,31 @@ __device__ void scalar_block(const Problem& p, int blk) {
     rows[which][c] = IO<T>::load(src + ((size_t)prow * H + h) * d + c);
   }
   __syncthreads();
-  if (t >= p.t_pad) return;
   const bool in_range = t < p.T;
   const bool valid = in_range && (p.packed || p.key_mask[t] != 0);
+  if (!p.packed && p.zero_out) {
+    // the warp's 32 tokens (consecutive t, rows H * d elements apart): lanes
+    // take consecutive 16-byte pieces of one row after another
+    const int lane = threadIdx.x & 31;
+    const unsigned zero = __ballot_sync(0xffffffffu, in_range && !valid);
+    const int ppr = d * (int)sizeof(T) / 16;  // pieces per row: 4 .. 32
+    const int t0 = t - lane;
+    for (int e = lane; zero && e < 32 * ppr; e += 32) {
+      const int r = e / ppr;
+      if ((zero >> r) & 1u) {
+        uint4* o4 = reinterpret_cast<uint4*>(static_cast<T*>(p.out) + ((size_t)(t0 + r) * H + h) * d);
+        o4[e % ppr] = make_uint4(0u, 0u, 0u, 0u);
+      }
+    }
+  }
+  if (t >= p.t_pad) return;
   if (h == 0) p.keybias[t] = valid ? 0.f : -INFINITY;
   float a0 = 0.f, a1 = 0.f, b0 = 0.f, b1 = 0.f;
-  const size_t row = ((size_t)t * H + h) * d;
   // No far tile at all (every sequence shorter than the saturation distance),
   // or the near-tile kernel forms the scalars and key-term blocks itself: only
-  // the key bias and the zeroed padded rows remain.
-  if (!scal) {
-    if (!valid && in_range && p.zero_out) {
-      uint4* o4 = reinterpret_cast<uint4*>(static_cast<T*>(p.out) + row);
-      for (int v = 0; v < d * (int)sizeof(T) / 16; ++v) o4[v] = make_uint4(0u, 0u, 0u, 0u);
-    }
-    return;
-  }
+  // the key bias (and the zeroed padded rows, above) remain.
+  if (!scal) return;
+  const size_t row = ((size_t)t * H + h) * d;
   if (valid) {
     constexpr int kVec = 16 / sizeof(T);
     const uint4* q4 = reinterpret_cast<const uint4*>(static_cast<const T*>(p.q) + row);
@@ -101,9 +112,6 @@ __device__ void scalar_block(const Problem& p, int blk) {
         b1 = fmaf(kf, rows[3][c], b1);
       }
     }
-  } else if (in_range && p.zero_out) {
-    uint4* o4 = reinterpret_cast<uint4*>(static_cast<T*>(p.out) + row);
-    for (int v = 0; v < d * (int)sizeof(T) / 16; ++v) o4[v] = make_uint4(0u, 0u, 0u, 0u);
   }
   if constexpr (sizeof(T) == 2) {
     // key-term block of far tiles: raw p2c products as hi + lo, masked keys finite
@@ -233,23 +241,23 @@ __device__ void build_worklist(const Problem& p) {
 }
 
 // ---- diagonal position tables (near tiles of the 16-bit tensor-core kernels) ----
-// For tile offset m and diagonal t, row (m - diag_m0) * 256 + t of each table is
-// the PK (PQ) row at idx(128 m - 127 + t): with them the position products of a
-// near tile come out of the MMA already indexed by diagonal.  A block copies
-// kDiagRows rows of one table in 16-byte pieces; their source rows are looked
-// up once.
+// Row r of each table is the PK (PQ) row at idx(128 diag_m0 - 127 + r), for r in
+// [0, 128 (n_diag + 1)): the 256 diagonals t of tile offset m are rows
+// 128 (m - diag_m0) + t, so that neighbouring offsets share half their rows.
+// With them the position products of a near tile come out of the MMA already
+// indexed by diagonal.  A block copies kDiagRows rows of one table in 16-byte
+// pieces; their source rows are looked up once.
 constexpr int kDiagRows = 8;
 
 __device__ void diag_rows(const Problem& p, int blk) {
   __shared__ int src_row[kDiagRows];
   const int cpr = p.H * p.d * 2 / 16;  // 16-byte pieces per row (16-bit types)
-  const int rows = p.n_diag * 256;
+  const int rows = (p.n_diag + 1) * 128;
   const int which = blk / (rows / kDiagRows);
   const int row0 = (blk % (rows / kDiagRows)) * kDiagRows;
   if (threadIdx.x < kDiagRows) {
     const int row = row0 + threadIdx.x;
-    const int m = p.diag_m0 + row / 256;
-    src_row[threadIdx.x] = rel_index(128 * m - 127 + row % 256, p.buckets, p.max_rel, p.span);
+    src_row[threadIdx.x] = rel_index(128 * p.diag_m0 - 127 + row, p.buckets, p.max_rel, p.span);
   }
   __syncthreads();
   const uint4* src = static_cast<const uint4*>(which ? p.pq : p.pk);
@@ -292,7 +300,7 @@ cudaError_t launch_plan(const Problem& p, cudaStream_t s) {
   const int nb_table = (2 * p.lt - 1 + kTableRun - 1) / kTableRun;
   const int nb_scal = p.H * ((p.t_pad + kPlanThreads - 1) / kPlanThreads);
   // diagonal tables: 16-bit I/O types only (the strict-fp32 kernel does not use them)
-  const int nb_diag = p.dtype == DF_FP32 ? 0 : 2 * p.n_diag * 256 / kDiagRows;
+  const int nb_diag = p.dtype == DF_FP32 || p.n_diag < 1 ? 0 : 2 * (p.n_diag + 1) * 128 / kDiagRows;
   const int grid = nb_table + nb_scal + nb_diag + 1;
   switch (p.dtype) {
     case DF_BF16:

@@ -76,8 +76,8 @@ cudaError_t launch_tc(const Problem& p, cudaStream_t s, cudaEvent_t ev0, cudaEve
   if (p.scal_in_near && (p.d != 64 || !encode_rows(&maps.absel, p.absel, 16LL * p.H, 64, bf16, 64, 16)))
     return cudaErrorInvalidValue;
   if (p.d == 64 || p.d == 128) {
-    if (p.n_diag < 1 || !encode_rows(&maps.dpk, p.diag_pk, 256LL * p.n_diag, row, bf16) ||
-        !encode_rows(&maps.dpq, p.diag_pq, 256LL * p.n_diag, row, bf16))
+    if (p.n_diag < 1 || !encode_rows(&maps.dpk, p.diag_pk, 128LL * (p.n_diag + 1), row, bf16) ||
+        !encode_rows(&maps.dpq, p.diag_pq, 128LL * (p.n_diag + 1), row, bf16))
       return cudaErrorInvalidValue;
   } else {
     maps.dpk = maps.pk;

@@ -446,7 +446,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int t = 0; t < nt; ++t) {
           const int kb = jlo + t;
-          int drow = (ib - kb - p.diag_m0) * 256;   // first row of the tile's diagonal tables
+          int drow = (ib - kb - p.diag_m0) * 128;   // first row of the tile's 256 diagonals
           if (ib - kb - p.diag_m0 < 0 || ib - kb - p.diag_m0 >= p.n_diag) {
             raise_device_error(hdr, DF_ERR_INVALID_ARG, 261);
             drow = 0;

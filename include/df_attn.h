@@ -241,11 +241,12 @@ typedef struct {
   int max_items;     /* capacity of the work-item list                        */
   int t_pad;         /* Tpad = round_up(B*L + 128, 128)                       */
   int table_half;    /* round_up(L, 128) + 128: the table covers |r| < table_half */
-  /* Diagonal position tables (d = 64 and 128; 0 bytes otherwise).  For every tile
-   * offset m in [diag_m0, diag_m0 + n_diag) -- query block minus key block of a
-   * near tile -- and every diagonal t in [0, 256): row (m - diag_m0) * 256 + t
-   * holds PK[idx(128 m - 127 + t)] (diag_pk) and PQ[idx(128 m - 127 + t)]
-   * (diag_pq), [rows][H][d] in the I/O type of PK / PQ. */
+  /* Diagonal position tables (d = 64 and 128; 0 bytes otherwise), 128 (n_diag + 1)
+   * rows each: row r holds PK[idx(128 diag_m0 - 127 + r)] (diag_pk) and
+   * PQ[idx(128 diag_m0 - 127 + r)] (diag_pq), [rows][H][d] in the I/O type of
+   * PK / PQ.  For a tile offset m in [diag_m0, diag_m0 + n_diag) -- query block
+   * minus key block of a near tile -- diagonal t in [0, 256) is row
+   * 128 (m - diag_m0) + t. */
   size_t diag_pk;
   size_t diag_pq;
   int n_diag;

@@ -94,7 +94,7 @@ def test_diagonal_table_range(binding, buckets, max_rel, span, L):
     m0, n = lay["diag_m0"], lay["n_diag"]
     assert m0 <= min(near) and m0 + n - 1 >= max(near)
     assert n <= len(near) + 2
-    rows = n * 256 * 4 * 64 * 2
+    rows = (n + 1) * 128 * 4 * 64 * 2
     assert lay["diag_pq"] - lay["diag_pk"] >= rows and lay["total"] - lay["diag_pq"] >= rows
     # head size 128: the same offsets, rows twice as wide
     assert (lay128["diag_m0"], lay128["n_diag"]) == (m0, n)

@@ -91,8 +91,9 @@ def test_plan_worklist_and_scalars(lib, name):
 
 @pytest.mark.parametrize("name", ["v3base_padded_bf16", "packed_varlen_h12d64", "packed_varlen_h6d128"])
 def test_plan_diagonal_tables(lib, name):
-    """Row (m - diag_m0) * 256 + t of the diagonal tables is PK / PQ at
-    idx(128 m - 127 + t), byte for byte."""
+    """Row r of the diagonal tables is PK / PQ at idx(128 diag_m0 - 127 + r),
+    byte for byte, so that diagonal t of tile offset m (row 128 (m - diag_m0)
+    + t) is PK / PQ at idx(128 m - 127 + t)."""
     x = synth.make_inputs(name)
     dev = {n: None if getattr(x, n) is None else getattr(x, n).cuda()
            for n in ("q", "k", "pk", "pq", "key_mask", "cu_seqlens")}
@@ -108,12 +109,18 @@ def test_plan_diagonal_tables(lib, name):
     lay = lib.df_attn_workspace_layout(B, x.w.H, L, x.w.d, **kw)
     n, m0 = lay["n_diag"], lay["diag_m0"]
     assert n > 0
-    r = (128 * (m0 + np.arange(n))[:, None] - 127 + np.arange(256)[None, :]).reshape(-1)
+    rows = 128 * (n + 1)
+    r = 128 * m0 - 127 + np.arange(rows)
     u = torch.from_numpy(rel_index(r, **kw).astype(np.int64))
     for name_t, src in (("diag_pk", x.pk), ("diag_pq", x.pq)):
-        got = _read_ws(ws, lay, name_t, torch.int16, n * 256 * x.w.H * x.w.d).view(n * 256, x.w.H, x.w.d)
+        got = _read_ws(ws, lay, name_t, torch.int16, rows * x.w.H * x.w.d).view(rows, x.w.H, x.w.d)
         want = src.view(torch.int16)[u]
         assert torch.equal(got, want), name_t
+        # diagonal t of offset m, as the near-tile kernels address it
+        for m in (m0, m0 + n - 1):
+            t = np.arange(256)
+            um = torch.from_numpy(rel_index(128 * m - 127 + t, **kw).astype(np.int64))
+            assert torch.equal(got[128 * (m - m0) + t], src.view(torch.int16)[um]), (name_t, m)
 
 
 FULL = ["tiny_fp32", "tiny_fp32_pad97", "v3base_padded_bf16", "v2xl_heavypad_fp16"]
