@@ -188,6 +188,37 @@ __device__ __forceinline__ void raise_device_error(df_ws_header* hdr, int code, 
   if (atomicCAS(&hdr->status, 0, code) == 0) hdr->status_where = where;
 }
 
+// Programmatic dependent launch.  The planning kernel lets the attention
+// kernel after it be scheduled early; that kernel sets up its shared memory,
+// barriers and tensor memory, then waits here for the planning grid to finish
+// (and its writes to be visible) before its first global-memory access.  The
+// wait returns at once for a launch without the programmatic attribute.
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void allow_dependent_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Launches `kernel` on `s` with the programmatic-serialisation attribute: it
+// may start while the kernel before it on the stream is still running, and
+// must call grid_dependency_wait() before it touches global memory.
+template <typename... Params, typename... Args>
+cudaError_t launch_after_plan(void (*kernel)(Params...), int grid, int threads, size_t smem,
+                              cudaStream_t s, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(threads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 }  // namespace dfa
 
 // Host-side launchers (defined in the .cu files).

@@ -271,6 +271,7 @@ __device__ void diag_rows(const Problem& p, int blk) {
 template <typename T>
 __global__ void __launch_bounds__(kPlanThreads)
     plan_kernel(Problem p, int nb_table, int nb_scal, int nb_diag) {
+  allow_dependent_launch();  // the attention kernel waits for this grid's end
   if (blockIdx.x == 0) {  // the single work-list block starts first
     write_kaug_selectors<T>(p);
     build_worklist(p);

@@ -95,6 +95,7 @@ __global__ void __launch_bounds__(kThreads, 1) simt_fwd_kernel(Problem p) {
   const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
   const int H = p.H;
   const size_t tok_stride = (size_t)H * D;
+  grid_dependency_wait();  // the planner's outputs (first global access below)
   const int n_items = p.hdr->n_items;
   const int rsp = p.hdr->r_sat_pos, rsn = p.hdr->r_sat_neg;
   const float ks = p.kscale;
@@ -378,8 +379,8 @@ cudaError_t launch_typed(const Problem& p, cudaStream_t s) {
   if (e != cudaSuccess) return e;
   const int grid = std::min(p.max_items * (kQBlock / BM), num_sms());
   if (grid <= 0) return cudaSuccess;
-  simt_fwd_kernel<D><<<grid, kThreads, bytes, s>>>(p);
-  return cudaGetLastError();
+  e = launch_after_plan(simt_fwd_kernel<D>, grid, kThreads, bytes, s, p);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace

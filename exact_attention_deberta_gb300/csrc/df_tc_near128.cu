@@ -195,6 +195,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   if ((smem_u32(smem_raw) & 1023u) != 0) {  // swizzled tiles need 1024-byte alignment
+    grid_dependency_wait();
     if (threadIdx.x == 0 && blockIdx.x == 0) raise_device_error(p.hdr, DF_ERR_CUDA, 400);
     return;
   }
@@ -247,6 +248,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tslot;
+  grid_dependency_wait();  // the planner's outputs (first global access below)
   const uint32_t tO = tmem + kColO, tQ = tmem + kColQ, tP = tmem + kColP;
 
   const int n_items = p.hdr->n_items;
@@ -801,8 +803,8 @@ cudaError_t launch_typed(const Problem& p, const TcMaps& maps, cudaStream_t s) {
                                        (int)Smem::bytes);
   if (e != cudaSuccess) return e;
   const int grid = std::min(p.max_items, near_sm_count());
-  tc_near128_kernel<BF16><<<grid, kThreads, Smem::bytes, s>>>(p, maps);
-  return cudaGetLastError();
+  e = launch_after_plan(tc_near128_kernel<BF16>, grid, kThreads, Smem::bytes, s, p, maps);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace
