@@ -49,7 +49,10 @@ __device__ void index_run(const Problem& p, int blk) {
 // scal[h][0..3][t] = kscale * {Q_t.PK[0], Q_t.PK[top], K_t.PQ[0], K_t.PQ[top]}.
 // A masked (or out-of-range) key gets -inf in both K terms and in keybias.
 // One thread per (head, token); a block covers 256 tokens of one head and keeps
-// that head's four position rows in shared memory.  The output rows of masked
+// that head's four position rows in shared memory.  A warp reads its 32 tokens'
+// Q and K rows whole (a row's 16-byte pieces on consecutive lanes, so each load
+// instruction covers whole rows), sums each row's products over its lanes and
+// hands the four sums to the token's own thread.  The output rows of masked
 // tokens (padded mode) are zeroed by each warp together, a whole row per group
 // of lanes, so that every store fills whole 32-byte sectors.
 template <typename T>
@@ -86,33 +89,60 @@ __device__ void scalar_block(const Problem& p, int blk) {
       }
     }
   }
+  float a0 = 0.f, a1 = 0.f, b0 = 0.f, b1 = 0.f;
+  if (scal) {
+    constexpr int kVec = 16 / sizeof(T);
+    const int lane = threadIdx.x & 31;
+    const int ppr = d / kVec;   // 16-byte pieces per row: 8 .. 32, a power of two
+    const int rpi = 32 / ppr;   // rows per load instruction
+    const int c = lane % ppr;   // this lane's piece, the same in every row
+    const int t0 = t - lane;
+    float w[4][kVec];           // the piece of the four position rows
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+#pragma unroll
+      for (int e = 0; e < kVec; ++e) w[j][e] = rows[j][c * kVec + e];
+    const unsigned live = __ballot_sync(0xffffffffu, valid);
+    for (int it = 0; it < ppr; ++it) {
+      const int r = it * rpi + lane / ppr;  // token t0 + r
+      float s[4] = {0.f, 0.f, 0.f, 0.f};
+      if ((live >> r) & 1u) {
+        const size_t off = ((size_t)(t0 + r) * H + h) * d + (size_t)c * kVec;
+        const uint4 qv = *reinterpret_cast<const uint4*>(static_cast<const T*>(p.q) + off);
+        const uint4 kv = *reinterpret_cast<const uint4*>(static_cast<const T*>(p.k) + off);
+        const T* qe = reinterpret_cast<const T*>(&qv);
+        const T* ke = reinterpret_cast<const T*>(&kv);
+#pragma unroll
+        for (int e = 0; e < kVec; ++e) {
+          const float qf = IO<T>::to_f(qe[e]), kf = IO<T>::to_f(ke[e]);
+          s[0] = fmaf(qf, w[0][e], s[0]);
+          s[1] = fmaf(qf, w[1][e], s[1]);
+          s[2] = fmaf(kf, w[2][e], s[2]);
+          s[3] = fmaf(kf, w[3][e], s[3]);
+        }
+      }
+      for (int o = ppr / 2; o > 0; o >>= 1)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) s[j] += __shfl_xor_sync(0xffffffffu, s[j], o);
+      // token t0 + lane was summed in iteration lane / rpi by lanes
+      // (lane % rpi) * ppr ..
+      const int src = (lane % rpi) * ppr;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) s[j] = __shfl_sync(0xffffffffu, s[j], src);
+      if (lane / rpi == it) {
+        a0 = s[0];
+        a1 = s[1];
+        b0 = s[2];
+        b1 = s[3];
+      }
+    }
+  }
   if (t >= p.t_pad) return;
   if (h == 0) p.keybias[t] = valid ? 0.f : -INFINITY;
-  float a0 = 0.f, a1 = 0.f, b0 = 0.f, b1 = 0.f;
   // No far tile at all (every sequence shorter than the saturation distance),
   // or the near-tile kernel forms the scalars and key-term blocks itself: only
   // the key bias (and the zeroed padded rows, above) remain.
   if (!scal) return;
-  const size_t row = ((size_t)t * H + h) * d;
-  if (valid) {
-    constexpr int kVec = 16 / sizeof(T);
-    const uint4* q4 = reinterpret_cast<const uint4*>(static_cast<const T*>(p.q) + row);
-    const uint4* k4 = reinterpret_cast<const uint4*>(static_cast<const T*>(p.k) + row);
-    for (int v = 0; v < d / kVec; ++v) {
-      const uint4 qv = q4[v], kv = k4[v];
-      const T* qe = reinterpret_cast<const T*>(&qv);
-      const T* ke = reinterpret_cast<const T*>(&kv);
-#pragma unroll
-      for (int e = 0; e < kVec; ++e) {
-        const int c = v * kVec + e;
-        const float qf = IO<T>::to_f(qe[e]), kf = IO<T>::to_f(ke[e]);
-        a0 = fmaf(qf, rows[0][c], a0);
-        a1 = fmaf(qf, rows[1][c], a1);
-        b0 = fmaf(kf, rows[2][c], b0);
-        b1 = fmaf(kf, rows[3][c], b1);
-      }
-    }
-  }
   if constexpr (sizeof(T) == 2) {
     // key-term block of far tiles: raw p2c products as hi + lo, masked keys finite
     T v[16];
