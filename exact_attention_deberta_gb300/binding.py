@@ -165,6 +165,40 @@ def df_attn_fwd(q, k, v, pos_key, pos_query, key_mask=None, cu_seqlens=None, *, 
     return out
 
 
+_lib.df_attn_fwd_fp32_fast.argtypes = [_vp] * 7 + [_i] * 8 + [_vp, _vp, _sz, _vp]
+_lib.df_attn_fwd_fp32_fast.restype = _i
+_lib.df_attn_fwd_fp32_fast_workspace_size.argtypes = [_i] * 7
+_lib.df_attn_fwd_fp32_fast_workspace_size.restype = _sz
+
+
+def df_attn_fwd_fp32_fast_workspace_size(B, H, L, d, buckets=256, max_rel=512, span=None) -> int:
+    span = default_span(buckets, max_rel) if span is None else span
+    return int(_lib.df_attn_fwd_fp32_fast_workspace_size(B, H, L, d, buckets, max_rel, span))
+
+
+def df_attn_fwd_fp32_fast(q, k, v, pos_key, pos_query, key_mask=None, cu_seqlens=None, *,
+                          max_seqlen=None, buckets=256, max_rel=512, span=None, out=None,
+                          workspace=None, stream=None):
+    """Fast fp32 mode: fp32 tensors, computed on the fp16 tensor-core path
+    (inputs rounded to fp16, |x| <= 65504); returns ``out`` (fp32)."""
+    if q.dtype != torch.float32:
+        raise ValueError("df_attn_fwd_fp32_fast takes float32 tensors")
+    B, H, L, T, d = _shape_args(q, key_mask, cu_seqlens, max_seqlen)
+    span = default_span(buckets, max_rel) if span is None else span
+    if workspace is None:
+        size = df_attn_fwd_fp32_fast_workspace_size(B, H, L, d, buckets, max_rel, span)
+        workspace = torch.empty(max(size, 256), dtype=torch.uint8, device=q.device)
+    B, H, L, T, d, span, out, workspace = _prepare(q, k, v, pos_key, pos_query, key_mask,
+                                                   cu_seqlens, max_seqlen, buckets, max_rel,
+                                                   span, out, workspace)
+    st = _lib.df_attn_fwd_fp32_fast(_ptr(q), _ptr(k), _ptr(v), _ptr(pos_key), _ptr(pos_query),
+                                    _ptr(key_mask), _ptr(cu_seqlens), B, H, L, T, d, buckets,
+                                    max_rel, span, _ptr(out), _ptr(workspace), workspace.numel(),
+                                    _stream(stream))
+    _check(st, "df_attn_fwd_fp32_fast")
+    return out
+
+
 _lib.df_attn_bwd.argtypes = [_vp] * 8 + [_i] * 9 + [_vp] * 5 + [_vp, _sz, _vp]
 _lib.df_attn_bwd.restype = _i
 _lib.df_attn_bwd_workspace_size.argtypes = [_i] * 7

@@ -194,6 +194,29 @@ size_t workspace_bytes_for(int B, int H, int L, int d, int buckets, int max_rel,
   return own > wide ? own : wide;
 }
 
+// Fast fp32 mode: the fp16 forward's own workspace first (its header, and so
+// the device status word, at offset 0), then fp16 copies of q, k, v, out (B L
+// rows each), pos_key, pos_query and the conversion's range flag.
+struct Fast32Layout {
+  size_t inner, q, k, v, o, pk, pq, flag, total;
+};
+
+Fast32Layout make_fast32_layout(int B, int H, int L, int d, int buckets, int max_rel, int span) {
+  Fast32Layout l{};
+  l.inner = workspace_bytes_for(B, H, L, d, buckets, max_rel, span);
+  const size_t tok = align256((size_t)B * L * H * d * 2);
+  const size_t pos = align256((size_t)2 * span * H * d * 2);
+  l.q = align256(l.inner);
+  l.k = l.q + tok;
+  l.v = l.k + tok;
+  l.o = l.v + tok;
+  l.pk = l.o + tok;
+  l.pq = l.pk + pos;
+  l.flag = l.pq + pos;
+  l.total = l.flag + 256;
+  return l;
+}
+
 df_status check_params(int H, int L, int d, df_dtype dtype, int buckets, int max_rel, int span) {
   if (H < 1 || L < 1 || span < 1) return DF_ERR_INVALID_ARG;
   if (dtype != DF_BF16 && dtype != DF_FP16 && dtype != DF_FP32) return DF_ERR_INVALID_ARG;
@@ -381,6 +404,55 @@ df_status df_attn_fwd(const void* q, const void* k, const void* v, const void* p
   }
   if (e != cudaSuccess) return DF_ERR_CUDA;
   g_last_launches.store(1 + launches);
+  return DF_OK;
+}
+
+size_t df_attn_fwd_fp32_fast_workspace_size(int B, int H, int L, int d, int buckets, int max_rel,
+                                            int span) {
+  if (B < 0 || check_params(H, L, d, DF_FP16, buckets, max_rel, span) != DF_OK) return 0;
+  return make_fast32_layout(B, H, L, d, buckets, max_rel, span).total;
+}
+
+df_status df_attn_fwd_fp32_fast(const void* q, const void* k, const void* v, const void* pos_key,
+                                const void* pos_query, const uint8_t* key_mask,
+                                const int32_t* cu_seqlens, int B, int H, int L, int total_tokens,
+                                int d, int buckets, int max_rel, int span, void* out,
+                                void* workspace, size_t workspace_bytes, df_stream_t stream) {
+  df_status st = check_params(H, L, d, DF_FP16, buckets, max_rel, span);
+  if (st != DF_OK) return st;
+  if (B < 0 || total_tokens < 0 || (long long)total_tokens > (long long)B * L) return DF_ERR_INVALID_ARG;
+  if (total_tokens > 0 && (!q || !k || !v || !out)) return DF_ERR_INVALID_ARG;
+  if (!pos_key || !pos_query) return DF_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(pos_key) || !aligned16(pos_query) ||
+      !aligned16(out))
+    return DF_ERR_ALIGNMENT;
+  const Fast32Layout fl = make_fast32_layout(B, H, L, d, buckets, max_rel, span);
+  if (!workspace || workspace_bytes < fl.total) return DF_ERR_WORKSPACE;
+  if (((uintptr_t)workspace & 255) != 0) return DF_ERR_ALIGNMENT;
+  char* base = static_cast<char*>(workspace);
+  // every remaining check of the fp16 forward, before anything is enqueued
+  Problem chk;
+  st = build_problem(base + fl.q, base + fl.k, base + fl.v, base + fl.pk, base + fl.pq, key_mask,
+                     cu_seqlens, B, H, L, total_tokens, d, buckets, max_rel, span, DF_FP16,
+                     base + fl.o, workspace, fl.inner, true, &chk);
+  if (st != DF_OK) return st;
+  cudaStream_t s = (cudaStream_t)stream;
+  int* flag = reinterpret_cast<int*>(base + fl.flag);
+  const long long tok = (long long)total_tokens * H * d, pos = 2ll * span * H * d;
+  const float* src[5] = {static_cast<const float*>(q), static_cast<const float*>(k),
+                         static_cast<const float*>(v), static_cast<const float*>(pos_key),
+                         static_cast<const float*>(pos_query)};
+  void* dst[5] = {base + fl.q, base + fl.k, base + fl.v, base + fl.pk, base + fl.pq};
+  const long long n[5] = {tok, tok, tok, pos, pos};
+  if (launch_to_half(src, dst, n, flag, s) != cudaSuccess) return DF_ERR_CUDA;
+  st = df_attn_fwd(base + fl.q, base + fl.k, base + fl.v, base + fl.pk, base + fl.pq, key_mask,
+                   cu_seqlens, B, H, L, total_tokens, d, buckets, max_rel, span, DF_FP16,
+                   base + fl.o, workspace, fl.inner, stream);
+  if (st != DF_OK) return st;
+  const int inner = g_last_launches.load();
+  if (launch_to_float(base + fl.o, static_cast<float*>(out), tok, flag, workspace, s) != cudaSuccess)
+    return DF_ERR_CUDA;
+  g_last_launches.store(inner + 2);
   return DF_OK;
 }
 

@@ -230,6 +230,13 @@ cudaError_t launch_simt(const Problem& p, cudaStream_t s, int* launches);
 cudaError_t launch_pad32(const void* const src[5], void* const dst[5], const long long rows[5],
                          cudaStream_t s);
 cudaError_t launch_unpad32(const void* src, void* dst, long long rows, cudaStream_t s);
+// Fast fp32 mode: fp32 -> fp16 copies of five arrays (n values each, a multiple
+// of 4; *flag set to 1 if a value is out of fp16's range), and fp16 -> fp32 of
+// the output (DF_ERR_INVALID_ARG recorded in the status word at hdr if *flag).
+cudaError_t launch_to_half(const float* const src[5], void* const dst[5], const long long n[5], int* flag,
+                           cudaStream_t s);
+cudaError_t launch_to_float(const void* src, float* dst, long long n, const int* flag, void* hdr,
+                            cudaStream_t s);
 cudaError_t launch_bwd(const BwdProblem& b, cudaStream_t s, cudaEvent_t ev0, cudaEvent_t ev_mid,
                        cudaEvent_t ev1, int* launches);
 }  // namespace dfa

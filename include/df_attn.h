@@ -119,6 +119,37 @@ df_status df_attn_fwd(const void* q, const void* k, const void* v,
 size_t df_attn_workspace_size(int B, int H, int L, int d, int buckets, int max_rel, int span);
 
 /*
+ * Fast fp32 mode (DisentangledFlash 0.2.0 README, "Status": the optional fast
+ * FP32/TF32 mode).  The same forward as df_attn_fwd for fp32 q, k, v, pos_key,
+ * pos_query and out (arguments, layouts and the padded / packed modes as
+ * there, without `dtype`), computed on the fp16 tensor-core path: every input
+ * is rounded to fp16 (RNE; an 11-bit significand, as TF32 keeps), the scores
+ * and P.V accumulate in fp32 as for fp16 I/O, and the output is rounded to
+ * fp16 and widened back to fp32.  Not the strict-fp32 result: expect the fp16
+ * path's error plus the rounding of the inputs.  Range: every input value must
+ * satisfy |x| <= 65504 (fp16's largest finite value); a value outside it (or
+ * not finite) makes the call record DF_ERR_INVALID_ARG in the device status
+ * word (df_attn_get_device_status on this workspace), and the output is then
+ * undefined.  workspace: at least df_attn_fwd_fp32_fast_workspace_size() bytes,
+ * 256-byte aligned; it holds df_attn_fwd's workspace at offset 0 and fp16
+ * copies of the inputs and the output after it.  Host-side errors as for
+ * df_attn_fwd (checked before anything is enqueued).  Two kernel launches
+ * more than df_attn_fwd's (the conversions) and one 4-byte memset.
+ */
+df_status df_attn_fwd_fp32_fast(const void* q, const void* k, const void* v,
+                                const void* pos_key, const void* pos_query,
+                                const uint8_t* key_mask, const int32_t* cu_seqlens,
+                                int B, int H, int L, int total_tokens, int d,
+                                int buckets, int max_rel, int span,
+                                void* out, void* workspace, size_t workspace_bytes,
+                                df_stream_t stream);
+
+/* Bytes of workspace df_attn_fwd_fp32_fast needs (T bounded by B*L); 0 for
+ * arguments df_attn_supported() rejects. */
+size_t df_attn_fwd_fp32_fast_workspace_size(int B, int H, int L, int d, int buckets, int max_rel,
+                                            int span);
+
+/*
  * Backward pass: gradients of sum(out * dout) with respect to q, k, v, pos_key
  * and pos_query, for the forward defined above.  The pages have no backward
  * (DisentangledFlash 0.2.0 README, "Status": training keeps the stock path);

@@ -245,3 +245,49 @@ def test_head_size_32_workspace_holds_the_widened_copies(binding):
     d64 = binding.df_attn_workspace_layout(B, H, L, 64)["total"]
     widened = 4 * B * L * H * 64 * 2 + 2 * 512 * H * 64 * 2
     assert binding.df_attn_workspace_size(B, H, L, 32) >= d64 + widened
+
+
+def _fast_raw(binding, **over):
+    """Call df_attn_fwd_fp32_fast with fake (never dereferenced) aligned pointers."""
+    a = dict(q=0x10000, k=0x20000, v=0x30000, pk=0x40000, pq=0x50000, mask=0x60000, cu=None,
+             B=2, H=2, L=64, T=128, d=64, buckets=256, max_rel=512, span=256,
+             out=0x70000, ws=0x100000, ws_bytes=1 << 30)
+    a.update(over)
+    vp = lambda x: None if x is None else ctypes.c_void_p(x)  # noqa: E731
+    return binding.raw_library.df_attn_fwd_fp32_fast(
+        vp(a["q"]), vp(a["k"]), vp(a["v"]), vp(a["pk"]), vp(a["pq"]), vp(a["mask"]), vp(a["cu"]),
+        a["B"], a["H"], a["L"], a["T"], a["d"], a["buckets"], a["max_rel"], a["span"],
+        vp(a["out"]), vp(a["ws"]), a["ws_bytes"], None)
+
+
+def test_fast_fp32_host_side_rejections(binding):
+    """Every argument error of the fast fp32 mode is caught before anything is
+    enqueued (the pointers are never dereferenced)."""
+    b = binding
+    need = b.df_attn_fwd_fp32_fast_workspace_size(2, 2, 64, 64, 256, 512, 256)
+    assert _fast_raw(b, mask=None) == b.DF_ERR_INVALID_ARG               # neither mask nor cu
+    assert _fast_raw(b, cu=0x80000) == b.DF_ERR_INVALID_ARG              # both
+    assert _fast_raw(b, d=96) == b.DF_ERR_UNSUPPORTED
+    assert _fast_raw(b, T=127) == b.DF_ERR_INVALID_ARG                   # padded needs T = B*L
+    assert _fast_raw(b, mask=None, cu=0x80000, T=129) == b.DF_ERR_INVALID_ARG  # T > B*L
+    assert _fast_raw(b, q=0x10008) == b.DF_ERR_ALIGNMENT
+    assert _fast_raw(b, v=0x30004) == b.DF_ERR_ALIGNMENT
+    assert _fast_raw(b, pq=0x50008) == b.DF_ERR_ALIGNMENT
+    assert _fast_raw(b, ws=0x100010) == b.DF_ERR_ALIGNMENT
+    assert _fast_raw(b, ws_bytes=need - 1) == b.DF_ERR_WORKSPACE
+    assert _fast_raw(b, ws=None) == b.DF_ERR_WORKSPACE
+    assert _fast_raw(b, v=None) == b.DF_ERR_INVALID_ARG
+    assert _fast_raw(b, pk=None) == b.DF_ERR_INVALID_ARG
+    assert _fast_raw(b, B=-1) == b.DF_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("B,H,L,d", [(2, 2, 64, 64), (16, 12, 512, 64), (4, 8, 2048, 128), (3, 4, 300, 32)])
+def test_fast_fp32_workspace_holds_the_fp16_forward_and_copies(binding, B, H, L, d):
+    """The fast mode's workspace is the fp16 forward's workspace plus fp16
+    copies of q, k, v, out (B L rows) and of PK, PQ."""
+    span = 256
+    fast = binding.df_attn_fwd_fp32_fast_workspace_size(B, H, L, d, 256, 512, span)
+    base = binding.df_attn_workspace_size(B, H, L, d, 256, 512, span)
+    assert fast >= base + 4 * B * L * H * d * 2 + 2 * (2 * span * H * d * 2)
+    assert fast % 256 == 0
+    assert binding.df_attn_fwd_fp32_fast_workspace_size(B, H, L, 96, 256, 512, span) == 0
