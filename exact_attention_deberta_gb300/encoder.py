@@ -64,7 +64,10 @@ class Encoder:
     def __init__(self, cfg: EncoderConfig, layers: List[dict], shared: dict):
         self.cfg, self.layers, self.shared = cfg, layers, shared
 
-    def __call__(self, hidden, cu_seqlens, max_seqlen, stream=None):
+    def __call__(self, hidden, cu_seqlens, max_seqlen, stream=None, trace=None):
+        """``trace``: an optional list; each layer appends a dict of the tensors
+        its attention call took and gave (q, k, v, pk, pq, ctx), which the layer
+        computes anyway (nothing extra runs)."""
         cfg = self.cfg
         hid, H = cfg.hidden, cfg.heads
         T = hidden.shape[0]
@@ -83,6 +86,8 @@ class Encoder:
             ctx = binding.df_attn_fwd(q, k, v, pk, pq, cu_seqlens=cu_seqlens, max_seqlen=max_seqlen,
                                       buckets=cfg.buckets, max_rel=cfg.max_rel, span=cfg.span, workspace=ws,
                                       stream=stream)
+            if trace is not None:
+                trace.append(dict(q=q, k=k, v=v, pk=pk, pq=pq, ctx=ctx))
             (a,) = binding.df_linear(ctx.view(T, hid), [p["w_o"]], [p["b_o"]], stream=stream)
             h1 = binding.df_layernorm(a, p["ln1_g"], p["ln1_b"], residual=h, eps=cfg.eps, stream=stream)
             (f,) = binding.df_linear(h1, [p["w_1"]], [p["b_1"]], stream=stream, activation=binding.LINEAR_GELU)

@@ -42,3 +42,41 @@ def test_zero_weight_layer_is_layer_norm_of_input():
     rel = rng.standard_normal((512, hid))
     out = encoder_layer(h, p, rel, np.array([0, 25, 40]), H, buckets=256, max_rel=512, span=256, eps=1e-7)
     np.testing.assert_allclose(out, layer_norm(h, np.ones(hid), z(hid), 1e-7), atol=1e-6)
+
+
+def test_one_wrong_head_fails_the_per_head_attention_bound():
+    """The GPU encoder test checks every head's attention output per layer
+    (relative L2 <= 1e-2, the bf16 attention tolerance) besides the final
+    hidden states (mean |err| < 1e-2, max < 0.15).  With the encoder's synthetic
+    weights a mistake confined to one head of twelve moves the final states by
+    about 2e-3 on average and 2e-2 at most, inside that bound; planted in the
+    oracle, each plausible mistake (a position term dropped, PK and PQ swapped,
+    the content term lost) moves that head's attention output by more than ten
+    times the per-head bound."""
+    import torch
+    from oracle import attend_packed, linear
+    from exact_attention_deberta_gb300.encoder import EncoderConfig, synthetic_weights
+    cfg = EncoderConfig(hidden=768, heads=12, layers=2, ffn=3072)
+    layers, shared = synthetic_weights(cfg, device="cpu", seed=5)
+    lengths = [300, 150, 77]
+    T, hid, H = sum(lengths), cfg.hidden, cfg.heads
+    d = hid // H
+    cu = np.concatenate([[0], np.cumsum(lengths)]).astype(np.int32)
+    g = torch.Generator().manual_seed(9)
+    h = torch.randn(T, hid, generator=g).to(torch.bfloat16).double().numpy()
+    p = {k: v.double().numpy() for k, v in layers[0].items()}
+    rel = layer_norm(shared["rel_embeddings"].double().numpy(), shared["rel_g"].double().numpy(),
+                     shared["rel_b"].double().numpy(), cfg.eps)
+    w, b = p["w_qkv"], p["b_qkv"]
+    q, k, v = linear(h, [w[:hid], w[hid:2 * hid], w[2 * hid:]], [b[:hid], b[hid:2 * hid], b[2 * hid:]])
+    pk, pq = linear(rel, [w[hid:2 * hid], w[:hid]], [b[hid:2 * hid], b[:hid]])
+    q, k, v = (t.reshape(T, H, d) for t in (q, k, v))
+    pk, pq = pk.reshape(-1, H, d), pq.reshape(-1, H, d)
+    kw = dict(buckets=cfg.buckets, max_rel=cfg.max_rel, span=cfg.span)
+    right = attend_packed(q, k, v, pk, pq, cu, **kw)
+    planted = {"no c2p": (q, k, v, 0 * pk, pq), "no p2c": (q, k, v, pk, 0 * pq),
+               "PK and PQ swapped": (q, k, v, pq, pk), "no content term": (q, 0 * k, v, pk, pq)}
+    for name, args in planted.items():
+        wrong = attend_packed(*args, cu, **kw)
+        rel_err = np.linalg.norm(wrong[:, 5] - right[:, 5]) / np.linalg.norm(right[:, 5])
+        assert rel_err > 10 * 1e-2, (name, rel_err)

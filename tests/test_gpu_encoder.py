@@ -7,6 +7,7 @@ import pytest
 import torch
 
 import oracle
+from _parity import errors
 
 pytestmark = pytest.mark.gpu
 
@@ -52,8 +53,20 @@ def test_two_encoder_layers_match_oracle(lib):
     cu = torch.tensor(np.concatenate([[0], np.cumsum(lengths)]), dtype=torch.int32)
     g = torch.Generator().manual_seed(9)
     h = torch.randn(T, cfg.hidden, generator=g).to(torch.bfloat16).cuda()
-    out = Encoder(cfg, layers, shared)(h, cu.cuda(), max(lengths))
+    trace = []
+    out = Encoder(cfg, layers, shared)(h, cu.cuda(), max(lengths), trace=trace)
     torch.cuda.synchronize()
+    # every head of every layer's attention against the oracle on the layer's own
+    # (rounded) q, k, v, PK, PQ, at the bf16 attention tolerance per head: the
+    # final hidden states below cannot resolve one wrong head of twelve
+    # (tests/test_encoder_oracle.py shows both)
+    for li, t in enumerate(trace):
+        ref = oracle.attend_packed(_np(t["q"]), _np(t["k"]), _np(t["v"]), _np(t["pk"]), _np(t["pq"]),
+                                   cu.numpy(), buckets=cfg.buckets, max_rel=cfg.max_rel, span=cfg.span)
+        ctx = _np(t["ctx"])
+        for hh in range(cfg.heads):
+            max_abs, rel = errors(ctx[:, hh], ref[:, hh])
+            assert max_abs <= 3e-2 and rel <= 1e-2, (li, hh, max_abs, rel)
     want = oracle.encoder(_np(h), [{k: _np(v) for k, v in p.items()} for p in layers],
                           _np(shared["rel_embeddings"]), _np(shared["rel_g"]), _np(shared["rel_b"]), cu.numpy(),
                           cfg.heads, buckets=cfg.buckets, max_rel=cfg.max_rel, span=cfg.span, eps=cfg.eps)
