@@ -11,6 +11,7 @@
 #include <string.h>
 
 #include <atomic>
+#include <mutex>
 
 namespace dfa {
 cudaError_t launch_tc(const Problem& p, cudaStream_t s, cudaEvent_t ev0, cudaEvent_t ev_mid,
@@ -57,16 +58,51 @@ int host_rel_index(int r, int buckets, int max_rel, int span) {
 
 int floor_div(int a, int b) { return a >= 0 ? a / b : -((-a + b - 1) / b); }
 
+// Saturation points of the bucket function within |r| < lt: rsp = the smallest
+// r >= 0 with idx(r) = 2 span - 1 (lt + 128 if there is none), rsn = the largest
+// r <= 0 with idx(r) = 0 (-(lt + 128) if none).  Finding them scans up to lt
+// double-precision buckets per side, tens of microseconds of host time, so the
+// last few parameter sets a process used are kept (the result depends on
+// nothing else).
+struct SatPoints {
+  int rsp, rsn;
+};
+
+SatPoints saturation_points(int buckets, int max_rel, int span, int lt) {
+  struct Entry {
+    int buckets, max_rel, span, lt;
+    SatPoints s;
+  };
+  constexpr int kKept = 8;
+  static std::mutex mu;
+  static Entry kept[kKept];
+  static int n_kept = 0, next = 0;
+  {
+    std::lock_guard<std::mutex> g(mu);
+    for (int i = 0; i < n_kept; ++i) {
+      const Entry& e = kept[i];
+      if (e.buckets == buckets && e.max_rel == max_rel && e.span == span && e.lt == lt) return e.s;
+    }
+  }
+  const int top = 2 * span - 1;
+  SatPoints s{lt + kQBlock, -(lt + kQBlock)};
+  for (int r = 0; r < lt; ++r)
+    if (host_rel_index(r, buckets, max_rel, span) == top) { s.rsp = r; break; }
+  for (int r = 0; r > -lt; --r)
+    if (host_rel_index(r, buckets, max_rel, span) == 0) { s.rsn = r; break; }
+  std::lock_guard<std::mutex> g(mu);
+  kept[next] = Entry{buckets, max_rel, span, lt, s};
+  next = (next + 1) % kKept;
+  if (n_kept < kKept) ++n_kept;
+  return s;
+}
+
 // Tile offsets m = query block - key block that can hold a near tile: the tile's
 // distances [128 m - 127, 128 m + 127] are not all saturated.  One offset of
 // slack on each side absorbs a last-ulp difference between host and device logs.
 void near_offsets(int L, int buckets, int max_rel, int span, int lt, int* m0, int* n) {
-  const int top = 2 * span - 1;
-  int rsp = lt + kQBlock, rsn = -(lt + kQBlock);
-  for (int r = 0; r < lt; ++r)
-    if (host_rel_index(r, buckets, max_rel, span) == top) { rsp = r; break; }
-  for (int r = 0; r > -lt; --r)
-    if (host_rel_index(r, buckets, max_rel, span) == 0) { rsn = r; break; }
+  const SatPoints sat = saturation_points(buckets, max_rel, span, lt);
+  const int rsp = sat.rsp, rsn = sat.rsn;
   const int nkb = (L + kKBlock - 1) / kKBlock;
   // strict range: floor((rsn - 127) / 128) + 1 .. ceil((rsp + 127) / 128) - 1
   int lo = floor_div(rsn - 127, 128);
@@ -84,12 +120,8 @@ void near_offsets(int L, int buckets, int max_rel, int span, int lt, int* m0, in
 // Whether a tile of `tile` queries x `tile` keys of some sequence (length <= L)
 // can lie wholly beyond a saturation point (a far tile).
 bool far_tiles_possible(int L, int buckets, int max_rel, int span, int lt, int tile) {
-  const int top = 2 * span - 1;
-  int rsp = lt + kQBlock, rsn = -(lt + kQBlock);
-  for (int r = 0; r < lt; ++r)
-    if (host_rel_index(r, buckets, max_rel, span) == top) { rsp = r; break; }
-  for (int r = 0; r > -lt; --r)
-    if (host_rel_index(r, buckets, max_rel, span) == 0) { rsn = r; break; }
+  const SatPoints sat = saturation_points(buckets, max_rel, span, lt);
+  const int rsp = sat.rsp, rsn = sat.rsn;
   const int reach = tile * ((L + tile - 1) / tile - 1) - (tile - 1);
   return reach >= rsp - 2 || -reach <= rsn + 2;
 }
