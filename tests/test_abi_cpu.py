@@ -291,3 +291,19 @@ def test_fast_fp32_workspace_holds_the_fp16_forward_and_copies(binding, B, H, L,
     assert fast >= base + 4 * B * L * H * d * 2 + 2 * (2 * span * H * d * 2)
     assert fast % 256 == 0
     assert binding.df_attn_fwd_fp32_fast_workspace_size(B, H, L, 96, 256, 512, span) == 0
+
+
+def test_layout_is_the_same_whatever_the_call_history(binding):
+    """The host keeps the bucket function's saturation points of the last few
+    parameter sets; layouts (near-tile offsets, sizes) must not depend on which
+    sets were used before or in what order (more sets than are kept, so some
+    are computed again)."""
+    sets = [(256, 512, 256, 8192), (256, 512, 256, 300), (0, 512, 512, 2048), (64, 128, 64, 1000),
+            (8, 16, 8, 100), (256, 4096, 256, 65536), (128, 256, 128, 4096), (32, 64, 32, 700),
+            (16, 64, 16, 5000), (256, 1024, 256, 3000), (2, 8, 2, 50), (0, 64, 64, 64)]
+    first = {}
+    for s in sets:
+        first[s] = dict(binding.df_attn_workspace_layout(2, 4, s[3], 64, buckets=s[0], max_rel=s[1], span=s[2]))
+    for s in reversed(sets + sets[::3]):
+        got = dict(binding.df_attn_workspace_layout(2, 4, s[3], 64, buckets=s[0], max_rel=s[1], span=s[2]))
+        assert got == first[s], s
