@@ -201,3 +201,62 @@ def test_packed_and_padded_layouts_agree():
             np.testing.assert_allclose(g_pd[b, :n], g_pk[cu[b]:cu[b + 1]], rtol=1e-12, atol=1e-12)
     np.testing.assert_allclose(padded[3], packed[3], rtol=1e-12, atol=1e-12)
     np.testing.assert_allclose(padded[4], packed[4], rtol=1e-12, atol=1e-12)
+
+
+# Parity bound for a backward whose contractions run on the tensor cores with
+# P and dS rounded to bf16 as MMA operands (fp32 accumulation; the bucket sums
+# of dS, and with them dPK and dPQ, stay in fp32): written down before such a
+# kernel exists.  Each rounded operand carries a relative error of at most the
+# bf16 unit roundoff 2^-9; the bound is four times that, relative to the
+# largest entry of the oracle's gradient.
+TC_BWD_TOL = {"dq": 4 * 2.0 ** -9, "dk": 4 * 2.0 ** -9, "dv": 4 * 2.0 ** -9, "dpk": 2e-4, "dpq": 2e-4}
+
+
+def _bf16(x):
+    return torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).to(torch.bfloat16).double().numpy()
+
+
+def _backward_bf16_operands(q, k, v, pk, pq, dout, *, buckets, max_rel, span):
+    """The gradients of one head as such a kernel forms them: the exact
+    softmax and dS (the chain rule of the module docstring), then P and dS
+    rounded to bf16 wherever they enter a contraction (dV = P^T dO,
+    dQ = dS K, dK = dS^T Q), the bucket sums of dS unrounded."""
+    from oracle import rel_index
+    n, d = q.shape
+    R, scale = 2 * span, 1.0 / math.sqrt(3.0 * d)
+    keys = np.arange(n)
+    idx = rel_index(keys[:, None] - keys[None, :], buckets, max_rel, span)
+    z = q @ k.T + np.take_along_axis(q @ pk.T, idx, axis=1) + (k @ pq.T)[keys[None, :], idx]
+    z = scale * z
+    z -= z.max(axis=1, keepdims=True)
+    p = np.exp(z)
+    p /= p.sum(axis=1, keepdims=True)
+    dP = dout @ v.T
+    dS = scale * p * (dP - (p * dP).sum(axis=1, keepdims=True))
+    pb, dSb = _bf16(p), _bf16(dS)
+    g_c2p = np.zeros((n, R))
+    g_p2c = np.zeros((n, R))
+    np.add.at(g_c2p, (np.repeat(keys, n), idx.ravel()), dS.ravel())
+    np.add.at(g_p2c, (np.tile(keys, n), idx.ravel()), dS.ravel())
+    return (dSb @ k + g_c2p @ pk, dSb.T @ q + g_p2c @ pq, pb.T @ dout, g_c2p.T @ q, g_p2c.T @ k)
+
+
+@pytest.mark.parametrize("n,d,sigma,seed", [(300, 64, 1.0, 1), (500, 64, 4.0, 5), (400, 128, 2.0, 6)])
+def test_bf16_operand_backward_stays_within_its_bound(n, d, sigma, seed):
+    """bf16 inputs with distances through the identity zone, the log zone and
+    saturation (DeBERTa's 256 / 512 / 256); the bf16-operand gradients stay
+    within TC_BWD_TOL of the oracle, and dQ, dK, dV would not meet the fp32
+    kernels' 2e-4 bound (so the looser one is needed, not just allowed)."""
+    rng = np.random.default_rng(seed)
+    q, k, pk, pq = (_bf16(rng.standard_normal(s) * sigma) for s in ((n, d), (n, d), (512, d), (512, d)))
+    v, dout = (_bf16(rng.standard_normal((n, d))) for _ in range(2))
+    kw = dict(buckets=256, max_rel=512, span=256)
+    exact = backward_head(q, k, v, pk, pq, dout, **kw)
+    rounded = _backward_bf16_operands(q, k, v, pk, pq, dout, **kw)
+    worst_main = 0.0
+    for name, a, b in zip(("dq", "dk", "dv", "dpk", "dpq"), exact, rounded):
+        rel = np.abs(a - b).max() / np.abs(a).max()
+        assert rel <= TC_BWD_TOL[name], (name, rel)
+        if name in ("dq", "dk", "dv"):
+            worst_main = max(worst_main, rel)
+    assert worst_main > 2e-4
