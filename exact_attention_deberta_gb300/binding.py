@@ -183,6 +183,8 @@ def df_attn_fwd_fp32_fast(q, k, v, pos_key, pos_query, key_mask=None, cu_seqlens
     (inputs rounded to fp16, |x| <= 65504); returns ``out`` (fp32)."""
     if q.dtype != torch.float32:
         raise ValueError("df_attn_fwd_fp32_fast takes float32 tensors")
+    if not q.is_cuda:
+        raise ValueError("q must be a contiguous CUDA tensor")
     B, H, L, T, d = _shape_args(q, key_mask, cu_seqlens, max_seqlen)
     span = default_span(buckets, max_rel) if span is None else span
     if workspace is None:

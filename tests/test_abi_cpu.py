@@ -307,3 +307,22 @@ def test_layout_is_the_same_whatever_the_call_history(binding):
     for s in reversed(sets + sets[::3]):
         got = dict(binding.df_attn_workspace_layout(2, 4, s[3], 64, buckets=s[0], max_rel=s[1], span=s[2]))
         assert got == first[s], s
+
+
+def test_binding_refuses_host_tensors_instead_of_computing_on_the_cpu(binding):
+    """There is no CPU path: the Python entry points reject tensors that are
+    not on a CUDA device before anything reaches the library."""
+    import torch
+    T, H, d = 64, 2, 64
+    q = torch.zeros(T, H, d, dtype=torch.bfloat16)
+    pos = torch.zeros(512, H, d, dtype=torch.bfloat16)
+    cu = torch.tensor([0, T], dtype=torch.int32)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        binding.df_attn_fwd(q, q, q, pos, pos, cu_seqlens=cu, max_seqlen=T)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        binding.df_attn_fwd_fp32_fast(q.float(), q.float(), q.float(), pos.float(), pos.float(),
+                                      cu_seqlens=cu, max_seqlen=T)
+    with pytest.raises(ValueError, match="float32"):
+        binding.df_attn_fwd_fp32_fast(q, q, q, pos, pos, cu_seqlens=cu, max_seqlen=T)
+    with pytest.raises(ValueError, match="exactly one"):
+        binding.df_attn_fwd(q, q, q, pos, pos)
