@@ -216,11 +216,12 @@ def _bf16(x):
     return torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).to(torch.bfloat16).double().numpy()
 
 
-def _backward_bf16_operands(q, k, v, pk, pq, dout, *, buckets, max_rel, span):
+def _backward_bf16_operands(q, k, v, pk, pq, dout, *, buckets, max_rel, span, rounded_o=False):
     """The gradients of one head as such a kernel forms them: the exact
     softmax and dS (the chain rule of the module docstring), then P and dS
     rounded to bf16 wherever they enter a contraction (dV = P^T dO,
-    dQ = dS K, dK = dS^T Q), the bucket sums of dS unrounded."""
+    dQ = dS K, dK = dS^T Q), the bucket sums of dS unrounded.  With
+    rounded_o, D_i = dO_i . O_i takes the forward's output rounded to bf16."""
     from oracle import rel_index
     n, d = q.shape
     R, scale = 2 * span, 1.0 / math.sqrt(3.0 * d)
@@ -232,7 +233,10 @@ def _backward_bf16_operands(q, k, v, pk, pq, dout, *, buckets, max_rel, span):
     p = np.exp(z)
     p /= p.sum(axis=1, keepdims=True)
     dP = dout @ v.T
-    dS = scale * p * (dP - (p * dP).sum(axis=1, keepdims=True))
+    if rounded_o:
+        dS = scale * p * (dP - (dout * _bf16(p @ v)).sum(axis=1, keepdims=True))
+    else:
+        dS = scale * p * (dP - (p * dP).sum(axis=1, keepdims=True))
     pb, dSb = _bf16(p), _bf16(dS)
     g_c2p = np.zeros((n, R))
     g_p2c = np.zeros((n, R))
@@ -260,3 +264,18 @@ def test_bf16_operand_backward_stays_within_its_bound(n, d, sigma, seed):
         if name in ("dq", "dk", "dv"):
             worst_main = max(worst_main, rel)
     assert worst_main > 2e-4
+
+
+def test_d_from_the_rounded_output_breaks_the_position_gradients():
+    """D_i = dO_i . O_i must come from an fp32 O: taken from the bf16-rounded
+    forward output, its error enters every dS of the row and the position
+    gradients (bucket sums of dS) leave their 2e-4 bound."""
+    rng = np.random.default_rng(7)
+    n, d = 400, 64
+    q, k, pk, pq = (_bf16(rng.standard_normal(s)) for s in ((n, d), (n, d), (512, d), (512, d)))
+    v, dout = (_bf16(rng.standard_normal((n, d))) for _ in range(2))
+    kw = dict(buckets=256, max_rel=512, span=256)
+    exact = backward_head(q, k, v, pk, pq, dout, **kw)
+    rounded = _backward_bf16_operands(q, k, v, pk, pq, dout, rounded_o=True, **kw)
+    worst_pos = max(np.abs(a - b).max() / np.abs(a).max() for a, b in zip(exact[3:], rounded[3:]))
+    assert worst_pos > 10 * TC_BWD_TOL["dpk"]
